@@ -1,0 +1,347 @@
+"""Pins for the oracle's AdamW / AdEMAMix step.
+
+* one step from zero state: the update is -lr g/(|g|+eps), AdEMAMix adds
+  alpha (1-b3) g to the numerator, and the two weight-decay orderings sit
+  lr^2 wd |u| apart ("Fix decoupled weight decay ordering in the CUDA
+  Adam/AdEMAMix kernels", 'Why the current tests do not catch it' and
+  'Verification');
+* constant-gradient closed form over many steps (bias-corrected EMAs of a
+  constant equal the constant);
+* torch.optim.AdamW / Adam in float64 (same ordering, per the PR body);
+* low-precision invariants of "When Small Updates Disappear" sec. 2.2;
+* a mutation check: the decay-after oracle fails the pins above.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+ADAMW, ADEMAMIX = oracle.ADAMW, oracle.ADEMAMIX
+
+
+def f32arr(x):
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
+def run_step(algo, p, g, hp, step=1, m=None, v=None, m2=None, decay_after=False, **kw):
+    n = p.size
+    m = np.zeros(n, p.dtype) if m is None else m
+    v = np.zeros(n, p.dtype) if v is None else v
+    if algo == ADEMAMIX and m2 is None:
+        m2 = np.zeros(n, p.dtype)
+    oracle.adam_tensor(algo, p, g, m, v, hp, step, m2=m2, decay_after=decay_after, **kw)
+    return p, m, v, m2
+
+
+@pytest.fixture
+def one_step_case():
+    rng = np.random.default_rng(7)
+    p0 = f32arr(rng.standard_normal(4096) * 0.1)
+    g = f32arr(rng.standard_normal(4096) * 0.01)
+    return p0, g
+
+
+def closed_form_step1(p0, g, lr, wd, eps, extra=0.0):
+    p0 = p0.astype(np.float64)
+    g = g.astype(np.float64)
+    return p0 * (1 - lr * wd) - lr * (1 + extra) * g / (np.abs(g) + eps)
+
+
+def test_step1_closed_form_adamw(one_step_case, pages):
+    cfg = pages["ordering_one_step"]
+    lr, wd = cfg["lr"], cfg["weight_decay"]
+    p0, g = one_step_case
+    hp = oracle.hparams(lr=lr, weight_decay=wd, eps=1e-8)
+    p, m, v, _ = run_step(ADAMW, p0.copy(), g, hp)
+    want = closed_form_step1(p0, g, np.float32(lr), np.float32(wd), np.float32(1e-8))
+    assert np.max(np.abs(p - want)) < 1e-7          # fp32 storage rounding only
+    assert np.allclose(m, (1 - np.float32(0.9)) * g.astype(np.float64), rtol=1e-6, atol=0)
+
+
+def test_step1_closed_form_ademamix(one_step_case):
+    p0, g = one_step_case
+    lr, wd, a, b3 = 0.1, 0.1, 5.0, 0.9999
+    hp = oracle.hparams(lr=lr, weight_decay=wd, alpha=a, beta3=b3, eps=1e-8)
+    p, _, _, m2 = run_step(ADEMAMIX, p0.copy(), g, hp)
+    extra = float(np.float32(a)) * (1 - float(np.float32(b3)))
+    want = closed_form_step1(p0, g, np.float32(lr), np.float32(wd), np.float32(1e-8), extra)
+    assert np.max(np.abs(p - want)) < 1e-7
+    assert np.allclose(m2, (1 - float(np.float32(b3))) * g, rtol=1e-6, atol=0)
+
+
+def test_ordering_separation_one_step(one_step_case, pages):
+    """lr = wd = 0.1: the orderings separate by lr^2 wd |u| ~ 1.0e-3 (the page
+    prints |p - decay_after| = 9.971e-4 for a correct kernel)."""
+    cfg = pages["ordering_one_step"]
+    p0, g = one_step_case
+    hp = oracle.hparams(lr=cfg["lr"], weight_decay=cfg["weight_decay"], eps=1e-8)
+    first = run_step(ADAMW, p0.copy(), g, hp)[0].astype(np.float64)
+    after = run_step(ADAMW, p0.copy(), g, hp, decay_after=True)[0].astype(np.float64)
+    sep = np.max(np.abs(first - after))
+    assert sep == pytest.approx(cfg["decay_after_minus_decay_first"], rel=2e-3)
+    assert sep >= cfg["printed_abs_p_minus_decay_after"] - cfg["printed_abs_p_minus_decay_first"]
+
+
+def test_mutation_decay_after_fails_closed_form(one_step_case, pages):
+    """The page re-registered kernels with the wrong ordering to show the tests
+    are not vacuous; here the oracle with the wrong ordering must fail the
+    closed-form pin by far more than its tolerance."""
+    cfg = pages["ordering_one_step"]
+    p0, g = one_step_case
+    hp = oracle.hparams(lr=cfg["lr"], weight_decay=cfg["weight_decay"], eps=1e-8)
+    bad = run_step(ADAMW, p0.copy(), g, hp, decay_after=True)[0]
+    want = closed_form_step1(p0, g, np.float32(0.1), np.float32(0.1), np.float32(1e-8))
+    assert np.max(np.abs(bad - want)) > 5e-4
+
+
+def test_ordering_twenty_steps_small_lr(pages):
+    """lr = 1e-3, wd = 0.01: 20 steps leave the orderings ~1.7e-7 apart,
+    inside a 1e-6 tolerance (why the bug went unnoticed)."""
+    cfg = pages["ordering_twenty_steps"]
+    rng = np.random.default_rng(8)
+    n = 4096
+    p0 = f32arr(rng.standard_normal(n) * 0.1)
+    hp = oracle.hparams(lr=cfg["lr"], weight_decay=cfg["weight_decay"], eps=1e-8)
+    pa, ma, va = p0.astype(np.float64).copy(), np.zeros(n), np.zeros(n)
+    pb, mb, vb = pa.copy(), np.zeros(n), np.zeros(n)
+    for t in range(1, cfg["steps"] + 1):
+        g = np.ascontiguousarray(rng.standard_normal(n) * 0.01)
+        oracle.adam_tensor(ADAMW, pa, g, ma, va, hp, t)
+        oracle.adam_tensor(ADAMW, pb, g, mb, vb, hp, t, decay_after=True)
+    sep = np.max(np.abs(pa - pb))
+    assert 0.3 * cfg["orderings_apart"] < sep < 1.5 * cfg["orderings_apart"]
+    assert sep < 1e-6
+
+
+@pytest.mark.parametrize("algo", [ADAMW, ADEMAMIX])
+def test_constant_gradient_closed_form_f64(algo):
+    """With g constant, the bias-corrected m and v are exactly g and g^2 at
+    every step, so u_t = g/(|g|+eps) (AdamW) or (g + alpha (1-b3^t) g)/(|g|+eps)
+    (AdEMAMix, m2 = (1-b3^t) g), and p_T follows by unrolling decay-first."""
+    rng = np.random.default_rng(9)
+    n, T = 257, 40
+    lr, wd, eps, a, b3 = 1e-2, 0.1, 1e-8, 5.0, 0.9999
+    hp = oracle.hparams(lr=lr, weight_decay=wd, eps=eps, alpha=a, beta3=b3)
+    lr, wd, eps, a, b3 = (float(np.float32(x)) for x in (lr, wd, eps, a, b3))
+    g = rng.standard_normal(n)
+    p = rng.standard_normal(n)
+    want = p.copy()
+    m, v, m2 = np.zeros(n), np.zeros(n), np.zeros(n)
+    for t in range(1, T + 1):
+        oracle.adam_tensor(algo, p, g, m, v, hp, t, m2=m2 if algo == ADEMAMIX else None)
+        u = g / (np.abs(g) + eps)
+        if algo == ADEMAMIX:
+            u = (g + a * (1 - b3 ** t) * g) / (np.abs(g) + eps)
+        want = want * (1 - lr * wd) - lr * u
+    assert np.max(np.abs(p - want)) < 1e-12
+
+
+@pytest.mark.parametrize("wd", [0.0, 0.1])
+def test_matches_torch_adamw_float64(wd):
+    rng = np.random.default_rng(10)
+    n, T = 1000, 25
+    lr, b1, b2, eps = 1e-2, 0.9, 0.999, 1e-8
+    hp = oracle.hparams(lr=lr, beta1=b1, beta2=b2, eps=eps, weight_decay=wd)
+    f = lambda x: float(np.float32(x))
+    p0 = rng.standard_normal(n)
+    tp = torch.tensor(p0.copy(), dtype=torch.float64, requires_grad=True)
+    if wd == 0.0:
+        opt = torch.optim.Adam([tp], lr=f(lr), betas=(f(b1), f(b2)), eps=f(eps), foreach=False)
+    else:
+        opt = torch.optim.AdamW([tp], lr=f(lr), betas=(f(b1), f(b2)), eps=f(eps),
+                                weight_decay=f(wd), foreach=False)
+    p, m, v = p0.copy(), np.zeros(n), np.zeros(n)
+    for t in range(1, T + 1):
+        g = rng.standard_normal(n) * 10.0 ** rng.uniform(-3, 1)
+        tp.grad = torch.tensor(g)
+        opt.step()
+        oracle.adam_tensor(ADAMW, p, np.ascontiguousarray(g), m, v, hp, t)
+    assert np.max(np.abs(p - tp.detach().numpy())) < 1e-12
+
+
+def test_ademamix_alpha_zero_is_adamw():
+    rng = np.random.default_rng(11)
+    n = 999
+    hp_a = oracle.hparams(lr=1e-3, weight_decay=0.1, alpha=0.0)
+    p1 = f32arr(rng.standard_normal(n))
+    p2 = p1.copy()
+    m1, v1, m2 = np.zeros(n, np.float32), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    mA, vA = np.zeros(n, np.float32), np.zeros(n, np.float32)
+    for t in range(1, 6):
+        g = f32arr(rng.standard_normal(n))
+        oracle.adam_tensor(ADEMAMIX, p1, g, m1, v1, hp_a, t, m2=m2)
+        oracle.adam_tensor(ADAMW, p2, g, mA, vA, hp_a, t)
+    assert np.array_equal(p1, p2) and np.array_equal(m1, mA) and np.array_equal(v1, vA)
+
+
+def test_clip_coefficient_scales_gradient():
+    """coef multiplies g before both EMAs: a step with g and coef c equals a
+    step with c*g and coef 1 (exact for power-of-two c)."""
+    rng = np.random.default_rng(12)
+    n = 500
+    hp = oracle.hparams(lr=1e-3, weight_decay=0.01)
+    g = f32arr(rng.standard_normal(n))
+    p0 = f32arr(rng.standard_normal(n))
+    a = run_step(ADAMW, p0.copy(), g, hp, coef=0.25)
+    b = run_step(ADAMW, p0.copy(), f32arr(g * 0.25), hp)
+    for x, y in zip(a[:3], b[:3]):
+        assert np.array_equal(x, y)
+
+
+# ------------------------------------------------------- low-precision states
+def bf16(x):
+    return torch.from_numpy(f32arr(x)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+
+
+def bf16_val(c):
+    return (c.astype(np.uint32) << 16).view(np.float32)
+
+
+def lp_state(v_dtype, vals):
+    if v_dtype == "bf16":
+        return bf16(vals)
+    if v_dtype == "e4m3":
+        return np.array([oracle.e4m3_encode(float(x)) for x in vals], np.uint8)
+    codes = [oracle.e2m2_encode(float(x)) for x in vals]
+    if len(codes) % 2:
+        codes.append(0)
+    return np.array([lo | (hi << 4) for lo, hi in zip(codes[::2], codes[1::2])], np.uint8)
+
+
+def lp_decode(v_dtype, arr, n):
+    if v_dtype == "bf16":
+        return bf16_val(arr).astype(np.float64)
+    if v_dtype == "e4m3":
+        return np.array([oracle.e4m3_decode(int(c)) for c in arr])
+    codes = np.stack([arr & 0xF, arr >> 4], axis=1).ravel()[:n]
+    return np.array([oracle.e2m2_decode(int(c)) for c in codes])
+
+
+def test_bf16_v_never_decreases_at_beta2_0999(pages):
+    """sec. 2.2: with b2 = 0.999 and nearest rounding the stored BF16 second
+    moment can never decrease; with g = 0 it never changes at all."""
+    assert pages["never_decrease_thresholds"]["bf16_beta2_above"] < 0.999
+    rng = np.random.default_rng(13)
+    n = 3000
+    hp = oracle.hparams(lr=1e-3, beta2=0.999)
+    p = f32arr(rng.standard_normal(n))
+    m = bf16(rng.standard_normal(n) * 0.1)
+    v = bf16(np.exp(rng.uniform(-10, 2, n)))
+    v0 = v.copy()
+    for t in range(1, 31):
+        unchanged = oracle.adam_tensor(ADAMW, p, bf16(np.zeros(n)), m, v, hp, t,
+                                       m_dtype="bf16", v_dtype="bf16")
+        assert unchanged == n
+    assert np.array_equal(v, v0)
+    for t in range(31, 61):
+        before = bf16_val(v).copy()
+        g = bf16(rng.standard_normal(n) * np.exp(rng.uniform(-6, 2, n)))
+        oracle.adam_tensor(ADAMW, p, g, m, v, hp, t, m_dtype="bf16", v_dtype="bf16")
+        assert np.all(bf16_val(v) >= before)
+
+
+def test_bf16_v_can_decrease_at_beta2_099():
+    """Negative control (sec. 2.2): with b2 = 0.99 downward updates get through."""
+    rng = np.random.default_rng(14)
+    n = 2000
+    hp = oracle.hparams(lr=1e-3, beta2=0.99)
+    p = f32arr(rng.standard_normal(n))
+    m = bf16(np.zeros(n))
+    v = bf16(np.exp(rng.uniform(-5, 2, n)))
+    before = bf16_val(v).copy()
+    oracle.adam_tensor(ADAMW, p, bf16(np.zeros(n)), m, v, hp, 5, m_dtype="bf16", v_dtype="bf16")
+    assert np.mean(bf16_val(v) < before) > 0.5
+
+
+def test_fp8_v_never_decreases_above_097_and_needs_large_g(pages):
+    """sec. 2.2: FP8 (E4M3) v cannot decrease for b2 above ~0.97, and an upward
+    move needs g^2 of roughly 30x the stored value or more."""
+    th = pages["never_decrease_thresholds"]
+    rng = np.random.default_rng(15)
+    n = 2000
+    vals = np.exp(rng.uniform(-4, 4, n))
+    for b2, must_hold in ((0.98, True), (0.9, False)):
+        hp = oracle.hparams(lr=1e-3, beta2=b2)
+        v = lp_state("e4m3", vals)
+        before = lp_decode("e4m3", v, n)
+        oracle.adam_tensor(ADAMW, f32arr(np.zeros(n)), bf16(np.zeros(n)), bf16(np.zeros(n)), v, hp, 3,
+                           m_dtype="bf16", v_dtype="e4m3")
+        dec = np.mean(lp_decode("e4m3", v, n) < before)
+        assert (dec == 0.0) == must_hold
+    hp = oracle.hparams(lr=1e-3, beta2=0.999)
+    v = lp_state("e4m3", vals)
+    before = lp_decode("e4m3", v, n)
+    ratio = th["fp8_upward_needs_g2_over_v_about"]
+    g = bf16(np.sqrt(before * ratio * 0.9))
+    oracle.adam_tensor(ADAMW, f32arr(np.zeros(n)), g, bf16(np.zeros(n)), v, hp, 2,
+                       m_dtype="bf16", v_dtype="e4m3")
+    assert np.array_equal(lp_decode("e4m3", v, n), before)
+    v = lp_state("e4m3", vals)
+    g = bf16(np.sqrt(before * ratio * 3.0))
+    oracle.adam_tensor(ADAMW, f32arr(np.zeros(n)), g, bf16(np.zeros(n)), v, hp, 2,
+                       m_dtype="bf16", v_dtype="e4m3")
+    assert np.all(lp_decode("e4m3", v, n) > before)
+
+
+@pytest.mark.parametrize("v_dtype", ["bf16", "e4m3", "e2m2"])
+def test_lowp_step_matches_fp32_formula_then_codec(v_dtype):
+    """The stored codes are exactly encode(fp32 m', v') -- checked by forming
+    m', v' here with numpy float32 (no FMA) and encoding with the codec."""
+    rng = np.random.default_rng(16)
+    n = 301
+    hp = oracle.hparams(lr=1e-3, beta1=0.9, beta2=0.999, weight_decay=0.1)
+    g = bf16(rng.standard_normal(n))
+    mvals = rng.standard_normal(n) * 0.1
+    vvals = np.exp(rng.uniform(-3, 1.5, n))
+    m, v = bf16(mvals), lp_state(v_dtype, vvals)
+    md, vd = bf16_val(m), lp_decode(v_dtype, v, n).astype(np.float32)
+    coef = np.float32(0.75)
+    for stochastic in (False, True):
+        mm, vv = m.copy(), v.copy()
+        oracle.adam_tensor(ADAMW, f32arr(np.zeros(n)), g, mm, vv, hp, 4, m_dtype="bf16",
+                           v_dtype=v_dtype, coef=float(coef), stochastic=stochastic, seed=77,
+                           tensor_index=2)
+        ge = bf16_val(g) * coef
+        b1, b2 = np.float32(0.9), np.float32(0.999)
+        omb1, omb2 = np.float32(1 - 0.9), np.float32(1 - float(np.float32(0.999)))
+        omb1 = np.float32(1.0 - float(np.float32(0.9)))
+        m_new = (b1 * md) + (omb1 * ge)
+        v_new = (b2 * vd) + (omb2 * (ge * ge))
+        enc = {"bf16": oracle.bf16_encode, "e4m3": oracle.e4m3_encode, "e2m2": oracle.e2m2_encode}[v_dtype]
+        for i in range(n):
+            rm, rv = oracle.draws(77, 4, 2, i) if stochastic else (0, 0)
+            assert mm[i] == oracle.bf16_encode(float(m_new[i]), stochastic, rm)
+            want_v = enc(float(v_new[i]), stochastic, rv)
+            got_v = vv[i] if v_dtype != "e2m2" else (vv[i // 2] >> (4 * (i & 1))) & 0xF
+            assert got_v == want_v
+
+
+def test_e2m2_odd_length_high_nibble_zero():
+    n = 7
+    hp = oracle.hparams()
+    v = np.full(4, 0xFF, np.uint8)
+    oracle.adam_tensor(ADAMW, f32arr(np.zeros(n)), bf16(np.ones(n)), bf16(np.zeros(n)), v, hp, 1,
+                       m_dtype="bf16", v_dtype="e2m2")
+    assert (v[3] >> 4) == 0
+
+
+def test_sr_state_update_unbiased_on_average():
+    """sec. 3.1: over many seeds the stored v averages to the FP32 value."""
+    n = 64
+    hp = oracle.hparams(beta2=0.999)
+    g = bf16(np.full(n, 0.5))
+    v0 = bf16(np.full(n, 1.0))
+    target = np.float32(0.999) * np.float32(1.0) + np.float32(1.0 - float(np.float32(0.999))) * np.float32(0.25)
+    acc = np.zeros(n)
+    seeds = 400
+    for s in range(seeds):
+        v = v0.copy()
+        oracle.adam_tensor(ADAMW, f32arr(np.zeros(n)), g, bf16(np.zeros(n)), v, hp, 1,
+                           m_dtype="bf16", v_dtype="bf16", stochastic=True, seed=s)
+        acc += bf16_val(v)
+    mean = acc.mean() / seeds
+    ulp = 2.0 ** -8  # spacing just below 1.0
+    assert abs(mean - float(target)) < 0.05 * ulp + 3 * ulp / math.sqrt(n * seeds)
