@@ -1,0 +1,253 @@
+/*
+ * opt.h -- C ABI of the GB300 (sm_103a) fused optimizer-step library.
+ *
+ * One optimizer step over a list of parameter tensors, in two calls:
+ *
+ *   opt_grad_norm      deterministic global gradient 2-norm and inf-norm,
+ *                      accumulated beyond fp32, NaN/Inf counted, and the clip
+ *                      coefficient derived from it -- all on the device.
+ *   opt_adamw_step     fused multi-tensor AdamW, decoupled weight decay
+ *   opt_ademamix_step  fused multi-tensor AdEMAMix, decoupled weight decay
+ *
+ * Sources (page title and section):
+ *  - "Fix decoupled weight decay ordering in the CUDA Adam/AdEMAMix kernels"
+ *    (bitsandbytes PR #2040), body: decay and update both taken from the old
+ *    parameter, p <- p (1 - lr wd) + step_size * update.
+ *  - "When Small Updates Disappear" (Topollai), sec. 1.1, 2.1, 3, 6.1, 7.3,
+ *    8.1: low-precision optimizer states (BF16, FP8, unsigned E2M2 "FP4"),
+ *    nearest and stochastic rounding, a counter-based draw tied to the
+ *    element, the fused step that reads and writes each tensor once.
+ *  - "perf(training): fused multi-tensor gradient-norm reduction" (NeMo
+ *    Automodel PR #3685), 'What' and 'Correctness properties': one launch per
+ *    dtype bucket, values widened in registers, host-side chunking from sizes
+ *    only with no atomics (bit-identical run to run), NaN counted and the
+ *    partial poisoned, the caller owning any cross-rank reduction.
+ *  - "Investigate SM103 bias-correction broadcast in 32-bit optimizers"
+ *    (bitsandbytes fork issue #7), 'Problem': bias-correction scalars are
+ *    uniform, so they are computed once per step on the host and passed in.
+ *
+ * Conventions for every call:
+ *  - Pointers named d_* or held in an opt_tensor_list are DEVICE pointers on
+ *    the device that was current when the plan was created; everything else
+ *    is host memory.  The caller owns every tensor; a plan owns only its
+ *    chunk table and a small workspace (about 16 bytes per 32768 elements).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls are stream-ordered and never synchronise, except where
+ *    a host output (h_*) is requested.
+ *  - Arguments are validated on the host before any launch.  Failures return
+ *    a negative status and launch nothing.  There is no CPU fallback.
+ *  - Not thread-safe per plan: calls on one plan must not overlap in time on
+ *    different host threads.  Concurrent device work on one plan (two streams)
+ *    races on the plan's workspace.
+ */
+#ifndef PS_OPT_H
+#define PS_OPT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define OPT_ABI_VERSION 1
+
+/* ---- status codes --------------------------------------------------- */
+#define OPT_OK            0
+#define OPT_ENONFINITE    1   /* a status, not a failure: the gradient norm was
+                                 NaN or Inf; a step given this norm changes
+                                 nothing */
+#define OPT_EINVAL       -1   /* NULL pointer, negative size, bad enum, step < 1 */
+#define OPT_EUNSUPPORTED -2   /* dtype combination not built (e.g. FP8 grads) */
+#define OPT_EALIGN       -3   /* a device pointer not 16-byte aligned */
+#define OPT_ECUDA        -4   /* a CUDA runtime call failed */
+#define OPT_ENOMEM       -5   /* workspace allocation failed */
+
+/* ---- storage types ----------------------------------------------------
+ * OPT_F32   IEEE binary32.
+ * OPT_BF16  top 16 bits of a binary32 word (2 bytes per element).
+ * OPT_E4M3  OCP FP8 E4M3FN: bias 7, 3 fraction bits, largest 448, no Inf,
+ *           NaN = S.1111.111 (1 byte per element).  Nearest rounding
+ *           saturates to +-448.
+ * OPT_E2M2  unsigned 4-bit float: 2 exponent bits (bias 1), 2 fraction bits,
+ *           values 0, 1/4, 1/2, 3/4, 1, 1.25 ... 7; no sign, NaN or Inf.
+ *           Negative inputs store 0, NaN stores 7.  Two codes per byte: the
+ *           LOW nibble holds the even element.  A tensor of n elements needs
+ *           ceil(n/2) bytes; for odd n the unused high nibble of the last byte
+ *           is written as 0.
+ * ("When Small Updates Disappear", sec. 2.1.) */
+typedef enum { OPT_F32 = 0, OPT_BF16 = 1, OPT_E4M3 = 2, OPT_E2M2 = 3 } opt_dtype;
+
+/* Rounding of low-precision states on write-back ("When Small Updates
+ * Disappear", sec. 3 and 6.1).  Stochastic rounding of value x adds a 16-bit
+ * draw r to the 16 bits of x that lie just below the target grid's last kept
+ * bit and rounds away from zero iff they carry: probability l / 2^16 where l
+ * is those 16 bits.  r comes from Philox4x32-10 (Salmon et al., SC'11) with
+ * key = (seed low 32, seed high 32) and counter = (q low 32, q high 32,
+ * tensor index, step low 32), q = element index / 4; word (index mod 4)
+ * gives the draw for m (its low 16 bits) and for v (its high 16 bits).  The
+ * draw therefore depends only on (seed, step, tensor, element), never on the
+ * launch shape. */
+typedef enum { OPT_ROUND_NEAREST = 0, OPT_ROUND_STOCHASTIC = 1 } opt_round;
+
+/* ---- tensor list ------------------------------------------------------
+ * All arrays are HOST arrays of length n; their entries are DEVICE pointers.
+ * Supported per-plan state combinations (m_dtype, v_dtype):
+ *   (F32, F32), (BF16, BF16), (BF16, E4M3), (BF16, E2M2).
+ * param_dtype must be F32; grad_dtype[i] is F32 or BF16 per tensor.  m2 is
+ * used only by opt_ademamix_step (FP32 states only); pass NULL otherwise.
+ * Every non-NULL pointer must be 16-byte aligned.  Tensors with numel 0 may
+ * have NULL pointers.  The plan copies what it needs: the arrays may be
+ * freed after opt_plan_create returns. */
+typedef struct opt_tensor_list {
+  int32_t n;
+  const int64_t* numel;
+  void* const* param;
+  const void* const* grad;
+  void* const* m;
+  void* const* v;
+  void* const* m2;             /* NULL unless AdEMAMix */
+  const int32_t* grad_dtype;   /* per tensor: OPT_F32 or OPT_BF16 */
+  int32_t param_dtype;
+  int32_t m_dtype;             /* also the dtype of m2 */
+  int32_t v_dtype;
+} opt_tensor_list;
+
+/* ---- hyperparameters ----------------------------------------------------
+ * Step t (1-based) computes, per element, with g the gradient (times the
+ * clip coefficient when a norm result is given):
+ *   m  <- beta1 m  + (1 - beta1) g
+ *   m2 <- beta3 m2 + (1 - beta3) g                       (AdEMAMix)
+ *   v  <- beta2 v  + (1 - beta2) g^2
+ *   u  <- (m / (1 - beta1^t) [+ alpha m2]) / (sqrt(v / (1 - beta2^t)) + eps)
+ *   p  <- p (1 - lr weight_decay) - lr u                  (decay-first)
+ * in fp32 arithmetic with the (1 - beta) constants and bias corrections
+ * formed once on the host in double and rounded to fp32.  m, v are formed in
+ * this order with no fused multiply-add, so that their values before
+ * rounding to a low-precision state are reproducible bit for bit. */
+typedef struct opt_hparams {
+  float lr, beta1, beta2, beta3, alpha, eps, weight_decay;
+  int32_t rounding;          /* opt_round; ignored for FP32 states */
+  uint64_t seed;             /* stochastic-rounding key */
+  int32_t count_unchanged;   /* nonzero: also count v codes left unchanged
+                                (read with opt_unchanged_count) */
+  int32_t reserved;          /* must be 0 */
+} opt_hparams;
+
+/* ---- norm result (48 bytes, written by opt_grad_norm) -------------------
+ * sumsq    sum of squares of all finite gradient elements (fp64)
+ * norm2    sqrt(sumsq); NaN if any NaN, else +Inf if any +-Inf
+ * norm_inf max |g|; NaN if any NaN, else +Inf if any +-Inf
+ * clip_coef  (float) min(1, max_norm / (norm2 + 1e-6)) computed in double;
+ *          1 when max_norm <= 0 or the norm is not finite
+ * status   OPT_OK or OPT_ENONFINITE */
+typedef struct opt_norm_result {
+  double sumsq, norm2, norm_inf;
+  uint64_t nan_count, inf_count;
+  float clip_coef;
+  int32_t status;
+} opt_norm_result;
+
+typedef struct opt_plan opt_plan;
+
+/* ---- library ------------------------------------------------------------ */
+int opt_version(void);                 /* OPT_ABI_VERSION */
+const char* opt_strerror(int status);  /* static string, never NULL */
+
+/* Validate `list`, build the chunk table (host, from sizes only), allocate
+ * the workspace on the current device and upload the tables (synchronous).
+ * On success *out owns the plan; destroy it with opt_plan_destroy. */
+int opt_plan_create(const opt_tensor_list* list, opt_plan** out);
+void opt_plan_destroy(opt_plan* plan);   /* NULL is a no-op; synchronises the device */
+/* Plan facts: chunks, elements, device workspace bytes (any may be NULL). */
+int opt_plan_info(const opt_plan* plan, int64_t* n_chunks, int64_t* total_numel,
+                  int64_t* workspace_bytes);
+
+/* Global gradient norm over every tensor of the plan ("perf(training): fused
+ * multi-tensor gradient-norm reduction", 'Correctness properties').  One
+ * partial-sum launch per gradient dtype into fixed slots, then one finishing
+ * launch; bit-identical run to run for the same inputs and plan.  Writes the
+ * result to d_out (device, 48 bytes, may be NULL to use the plan's own
+ * buffer, whose device address opt_plan_norm_buffer returns).  If h_out is
+ * non-NULL the result is also copied to it and the stream is synchronised.
+ * Returns OPT_OK, OPT_ENONFINITE (only when h_out is given), or an error. */
+int opt_grad_norm(opt_plan* plan, double max_norm, opt_norm_result* d_out,
+                  opt_norm_result* h_out, void* stream);
+const opt_norm_result* opt_plan_norm_buffer(const opt_plan* plan);
+
+/* One fused step over every tensor of the plan, in place.  d_norm: a device
+ * opt_norm_result from opt_grad_norm, or NULL for no clipping.  When
+ * d_norm->status is OPT_ENONFINITE the kernels leave p and every state
+ * untouched (the step is skipped on the device, no host sync).  step >= 1.
+ * One launch per gradient-dtype bucket. */
+int opt_adamw_step(opt_plan* plan, const opt_hparams* hp, int64_t step,
+                   const opt_norm_result* d_norm, void* stream);
+/* As opt_adamw_step plus m2 and alpha; needs FP32 states and m2 pointers. */
+int opt_ademamix_step(opt_plan* plan, const opt_hparams* hp, int64_t step,
+                      const opt_norm_result* d_norm, void* stream);
+
+/* Number of v codes (FP32 words for FP32 v) the last step with
+ * count_unchanged set left bitwise unchanged ("stalled", "When Small Updates
+ * Disappear" sec. 1.1).  Copies to host and synchronises the stream; resets
+ * the counter. */
+int opt_unchanged_count(opt_plan* plan, uint64_t* h_count, void* stream);
+
+/* Copy each tensor's gradient from host memory (pinned for asynchrony) into
+ * the plan's device gradient buffers: one cudaMemcpyAsync per tensor. */
+int opt_grads_upload(opt_plan* plan, const void* const* h_grad, void* stream);
+
+/* Standalone conversion of n fp32 values to a state format (and back), with
+ * the same codecs and draws the step uses: element i takes the v draw of
+ * element i of tensor `tensor_index` at step `step` ("When Small Updates
+ * Disappear", sec. 6-8: the stand-alone cast).  d_out holds n elements of
+ * `dtype` (ceil(n/2) bytes for E2M2).  Pointers 16-byte aligned. */
+int opt_encode(const float* d_in, void* d_out, int64_t n, int32_t dtype,
+               int32_t rounding, uint64_t seed, uint32_t tensor_index,
+               int64_t step, void* stream);
+int opt_decode(const void* d_in, float* d_out, int64_t n, int32_t dtype, void* stream);
+
+/* ---- host-only helpers (no GPU needed) ----------------------------------- */
+
+/* Elements per chunk of the chunk table. */
+#define OPT_CHUNK_ELEMS 32768
+/* Number of fixed partial-sum slots per gradient-dtype bucket. */
+#define OPT_NORM_SLOTS 1216
+
+typedef struct opt_chunk {
+  uint32_t tensor;   /* index into the list */
+  uint32_t len;      /* 1..OPT_CHUNK_ELEMS */
+  int64_t start;     /* element offset in the tensor, multiple of OPT_CHUNK_ELEMS */
+} opt_chunk;
+
+/* Chunk table from sizes and gradient dtypes only: bucket 0 (FP32 grads)
+ * first, then bucket 1 (BF16 grads); within a bucket, tensors in list order
+ * and chunks in element order.  Writes up to `cap` entries to `out` (may be
+ * NULL to count) and the bucket boundaries to bucket_begin[0..2] (chunks of
+ * bucket b are [bucket_begin[b], bucket_begin[b+1])).  Returns the chunk
+ * count, or a negative status. */
+int64_t opt_chunk_table(int32_t n, const int64_t* numel, const int32_t* grad_dtype,
+                        opt_chunk* out, int64_t cap, int64_t bucket_begin[3]);
+
+/* Per-step scalars, formed in double and rounded once to fp32. */
+typedef struct opt_step_scalars {
+  float lr, decay;            /* decay = 1 - lr wd */
+  float beta1, omb1;          /* omb = 1 - beta */
+  float beta2, omb2;
+  float beta3, omb3;
+  float alpha, eps;
+  float inv_bc1, inv_bc2;     /* 1 / (1 - beta^t) */
+} opt_step_scalars;
+int opt_step_scalars_compute(const opt_hparams* hp, int64_t step, opt_step_scalars* out);
+
+/* Combine per-rank norm results (each rank's opt_grad_norm over its own
+ * shard) in rank order: fp64 sum of sumsq in index order, max of norm_inf,
+ * sum of counts; then norm2, clip_coef and status as opt_grad_norm defines
+ * them.  Deterministic for a fixed rank order ("perf(training): fused
+ * multi-tensor gradient-norm reduction", 'Correctness properties': the
+ * caller owns the cross-rank scalar reduction). */
+int opt_norm_combine(const opt_norm_result* parts, int32_t n, double max_norm,
+                     opt_norm_result* out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PS_OPT_H */

@@ -355,8 +355,9 @@ int oracle_adam_tensor(int algo, int64_t n,
                        void* v, int v_dtype,
                        const oracle_hparams* hp, int64_t step, float coef,
                        int stochastic, uint64_t seed, uint32_t tensor_index,
-                       int decay_after, int64_t* unchanged) {
-  if (step < 1) return -1;
+                       int64_t index_base, int decay_after, int64_t* unchanged) {
+  if (step < 1 || index_base < 0) return -1;
+  if (v_dtype == ORC_E2M2 && (index_base & 1)) return -1;
   if (algo == ORC_ADEMAMIX && m2 == 0) return -1;
   int wide = (p_dtype == ORC_F64);
   if (wide && (g_dtype != ORC_F64 || m_dtype != ORC_F64 || v_dtype != ORC_F64)) return -1;
@@ -404,7 +405,8 @@ int oracle_adam_tensor(int algo, int64_t n,
       float vf = t3 + t4;
       m_new = mf;
       v_new = vf;
-      if (stochastic) oracle_draws(seed, step, tensor_index, i, &r16_m, &r16_v);
+      if (stochastic)
+        oracle_draws(seed, step, tensor_index, index_base + i, &r16_m, &r16_v);
     }
     double num = m_new / bc1;
     if (algo == ORC_ADEMAMIX) num += alpha * m2_new;

@@ -86,7 +86,9 @@ enum { ORC_ADAMW = 0, ORC_ADEMAMIX = 1 };
  * p_dtype == ORC_F64, then every state is f64 too).  g is f32 or bf16 (f64
  * with p_dtype == ORC_F64).  m is f32 or bf16 (AdEMAMix: m, m2, v all f32); v is f32, bf16, e4m3
  * or e2m2 (two codes per byte, low nibble = even element).  `coef` is the
- * clip coefficient (1 = none).  `decay_after` != 0 selects the wrong,
+ * clip coefficient (1 = none).  Element i of the arrays is element
+ * index_base + i of the tensor (it selects the stochastic-rounding draws; it
+ * must be even for E2M2).  `decay_after` != 0 selects the wrong,
  * decay-after ordering; it exists only so tests can show that the pins catch
  * it.  *unchanged (if non-NULL) receives the count of v codes (or f32 words)
  * left bitwise unchanged by this step.  Returns 0, or -1 on an unsupported
@@ -98,7 +100,7 @@ int oracle_adam_tensor(int algo, int64_t n,
                        void* v, int v_dtype,
                        const oracle_hparams* hp, int64_t step, float coef,
                        int stochastic, uint64_t seed, uint32_t tensor_index,
-                       int decay_after, int64_t* unchanged);
+                       int64_t index_base, int decay_after, int64_t* unchanged);
 
 #ifdef __cplusplus
 }

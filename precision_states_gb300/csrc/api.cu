@@ -1,0 +1,348 @@
+// api.cu -- the device-facing part of the C ABI: plan creation (validation,
+// chunk table, one workspace allocation, upload), the gradient norm, the
+// fused steps, and the standalone codecs.  Every argument is checked on the
+// host before anything is launched; failures return a status and launch
+// nothing.
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+using namespace psopt;
+
+struct opt_plan {
+  int device = 0;
+  int sm_count = 0;
+  int32_t n = 0;
+  int64_t total_numel = 0;
+  int64_t n_chunks = 0;
+  int64_t bucket_begin[3] = {0, 0, 0};
+  int32_t m_dtype = OPT_F32, v_dtype = OPT_F32;
+  int combo = SC_F32;
+  bool has_m2 = false;
+  std::vector<void*> grad_dev;          // per tensor, for opt_grads_upload
+  std::vector<int64_t> grad_bytes;
+  // one device allocation: tensors | chunks | slots | result | counter
+  void* d_mem = nullptr;
+  int64_t d_bytes = 0;
+  TensorDesc* d_tensors = nullptr;
+  opt_chunk* d_chunks = nullptr;
+  NormSlot* d_slots = nullptr;
+  opt_norm_result* d_result = nullptr;
+  unsigned long long* d_unchanged = nullptr;
+};
+
+namespace psopt {
+int state_combo(int32_t m_dtype, int32_t v_dtype) {
+  if (m_dtype == OPT_F32 && v_dtype == OPT_F32) return SC_F32;
+  if (m_dtype == OPT_BF16 && v_dtype == OPT_BF16) return SC_BF16_BF16;
+  if (m_dtype == OPT_BF16 && v_dtype == OPT_E4M3) return SC_BF16_E4M3;
+  if (m_dtype == OPT_BF16 && v_dtype == OPT_E2M2) return SC_BF16_E2M2;
+  return -1;
+}
+}  // namespace psopt
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+int64_t state_bytes(int32_t dtype, int64_t n) {
+  switch (dtype) {
+    case OPT_F32: return 4 * n;
+    case OPT_BF16: return 2 * n;
+    case OPT_E4M3: return n;
+    case OPT_E2M2: return (n + 1) / 2;
+  }
+  return -1;
+}
+
+int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return OPT_OK;
+  if (e == cudaErrorMemoryAllocation) return OPT_ENOMEM;
+  return OPT_ECUDA;
+}
+
+// Make the plan's device current for the duration of a call.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) { ok = false; return; }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+int validate_list(const opt_tensor_list* L) {
+  if (L == nullptr || L->n < 0) return OPT_EINVAL;
+  if (L->n > 0 && (L->numel == nullptr || L->param == nullptr || L->grad == nullptr ||
+                   L->m == nullptr || L->v == nullptr || L->grad_dtype == nullptr))
+    return OPT_EINVAL;
+  if (L->param_dtype != OPT_F32) return OPT_EUNSUPPORTED;
+  if (state_combo(L->m_dtype, L->v_dtype) < 0) return OPT_EUNSUPPORTED;
+  for (int32_t i = 0; i < L->n; ++i) {
+    if (L->numel[i] < 0) return OPT_EINVAL;
+    if (L->grad_dtype[i] != OPT_F32 && L->grad_dtype[i] != OPT_BF16) return OPT_EUNSUPPORTED;
+    if (L->numel[i] == 0) continue;
+    const void* ptrs[5] = {L->param[i], L->grad[i], L->m[i], L->v[i],
+                           L->m2 ? L->m2[i] : nullptr};
+    for (int k = 0; k < 4; ++k)
+      if (ptrs[k] == nullptr) return OPT_EINVAL;
+    for (int k = 0; k < 5; ++k)
+      if (ptrs[k] != nullptr && !aligned16(ptrs[k])) return OPT_EALIGN;
+  }
+  return OPT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
+  if (out == nullptr) return OPT_EINVAL;
+  *out = nullptr;
+  int st = validate_list(L);
+  if (st != OPT_OK) return st;
+
+  opt_plan* P = new (std::nothrow) opt_plan();
+  if (P == nullptr) return OPT_ENOMEM;
+  P->n = L->n;
+  P->m_dtype = L->m_dtype;
+  P->v_dtype = L->v_dtype;
+  P->combo = state_combo(L->m_dtype, L->v_dtype);
+  P->has_m2 = L->m2 != nullptr;
+  if (P->has_m2)
+    for (int32_t i = 0; i < L->n; ++i)
+      if (L->numel[i] > 0 && L->m2[i] == nullptr) P->has_m2 = false;
+
+  // chunk table on the host, from sizes only
+  int64_t nch = opt_chunk_table(L->n, L->numel, L->grad_dtype, nullptr, 0, P->bucket_begin);
+  if (nch < 0) { delete P; return (int)nch; }
+  std::vector<opt_chunk> chunks((size_t)nch);
+  opt_chunk_table(L->n, L->numel, L->grad_dtype, chunks.data(), nch, P->bucket_begin);
+  P->n_chunks = nch;
+
+  std::vector<TensorDesc> tds((size_t)L->n);
+  P->grad_dev.resize((size_t)L->n);
+  P->grad_bytes.resize((size_t)L->n);
+  for (int32_t i = 0; i < L->n; ++i) {
+    TensorDesc& t = tds[(size_t)i];
+    t.p = static_cast<float*>(L->param[i]);
+    t.g = L->grad[i];
+    t.m = L->m[i];
+    t.v = L->v[i];
+    t.m2 = P->has_m2 ? static_cast<float*>(L->m2[i]) : nullptr;
+    t.numel = L->numel[i];
+    P->total_numel += L->numel[i];
+    P->grad_dev[(size_t)i] = const_cast<void*>(L->grad[i]);
+    P->grad_bytes[(size_t)i] = state_bytes(L->grad_dtype[i], L->numel[i]);
+  }
+
+  if (cudaGetDevice(&P->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&P->sm_count, cudaDevAttrMultiProcessorCount, P->device) != cudaSuccess) {
+    delete P;
+    return OPT_ECUDA;
+  }
+
+  const int64_t off_t = 0;
+  const int64_t off_c = align_up(off_t + (int64_t)sizeof(TensorDesc) * L->n, 256);
+  const int64_t off_s = align_up(off_c + (int64_t)sizeof(opt_chunk) * nch, 256);
+  const int64_t off_r = align_up(off_s + (int64_t)sizeof(NormSlot) * 2 * OPT_NORM_SLOTS, 256);
+  const int64_t off_u = align_up(off_r + (int64_t)sizeof(opt_norm_result), 256);
+  P->d_bytes = align_up(off_u + 8, 256);
+  cudaError_t e = cudaMalloc(&P->d_mem, (size_t)P->d_bytes);
+  if (e != cudaSuccess) { delete P; return cuda_status(e); }
+  char* base = static_cast<char*>(P->d_mem);
+  P->d_tensors = reinterpret_cast<TensorDesc*>(base + off_t);
+  P->d_chunks = reinterpret_cast<opt_chunk*>(base + off_c);
+  P->d_slots = reinterpret_cast<NormSlot*>(base + off_s);
+  P->d_result = reinterpret_cast<opt_norm_result*>(base + off_r);
+  P->d_unchanged = reinterpret_cast<unsigned long long*>(base + off_u);
+
+  e = cudaMemset(P->d_mem, 0, (size_t)P->d_bytes);
+  if (e == cudaSuccess && L->n > 0)
+    e = cudaMemcpy(P->d_tensors, tds.data(), sizeof(TensorDesc) * (size_t)L->n, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && nch > 0)
+    e = cudaMemcpy(P->d_chunks, chunks.data(), sizeof(opt_chunk) * (size_t)nch, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    cudaFree(P->d_mem);
+    delete P;
+    return cuda_status(e);
+  }
+  *out = P;
+  return OPT_OK;
+}
+
+void opt_plan_destroy(opt_plan* P) {
+  if (P == nullptr) return;
+  {
+    DeviceGuard g(P->device);
+    cudaDeviceSynchronize();
+    cudaFree(P->d_mem);
+  }
+  delete P;
+}
+
+int opt_plan_info(const opt_plan* P, int64_t* n_chunks, int64_t* total_numel, int64_t* workspace_bytes) {
+  if (P == nullptr) return OPT_EINVAL;
+  if (n_chunks) *n_chunks = P->n_chunks;
+  if (total_numel) *total_numel = P->total_numel;
+  if (workspace_bytes) *workspace_bytes = P->d_bytes;
+  return OPT_OK;
+}
+
+const opt_norm_result* opt_plan_norm_buffer(const opt_plan* P) {
+  return P ? P->d_result : nullptr;
+}
+
+int opt_grad_norm(opt_plan* P, double max_norm, opt_norm_result* d_out, opt_norm_result* h_out,
+                  void* stream) {
+  if (P == nullptr) return OPT_EINVAL;
+  if (d_out != nullptr && ((uintptr_t)d_out & 7u)) return OPT_EALIGN;
+  DeviceGuard g(P->device);
+  if (!g.ok) return OPT_ECUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  opt_norm_result* dst = d_out ? d_out : P->d_result;
+  cudaError_t e = cudaSuccess;
+  // one partial-sum launch per non-empty dtype bucket, each into its own
+  // OPT_NORM_SLOTS slots; the finish reduces the slots of the buckets used
+  int first = -1, last = -1;
+  for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+    if (P->bucket_begin[b + 1] <= P->bucket_begin[b]) continue;
+    if (first < 0) first = b;
+    last = b;
+    const int dt = b == 0 ? OPT_F32 : OPT_BF16;
+    e = launch_norm_partials(dt, P->d_tensors, P->d_chunks, P->bucket_begin[b], P->bucket_begin[b + 1],
+                             P->d_slots + b * OPT_NORM_SLOTS, s);
+  }
+  if (e == cudaSuccess) {
+    const int n_slots = first < 0 ? 0 : (last - first + 1) * OPT_NORM_SLOTS;
+    e = launch_norm_finalize(P->d_slots + (first < 0 ? 0 : first * OPT_NORM_SLOTS), n_slots, max_norm,
+                             dst, s);
+  }
+  if (e != cudaSuccess) return cuda_status(e);
+  if (h_out != nullptr) {
+    e = cudaMemcpyAsync(h_out, dst, sizeof(opt_norm_result), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_status(e);
+    return h_out->status;
+  }
+  return OPT_OK;
+}
+
+static int do_step(opt_plan* P, const opt_hparams* hp, int64_t step, const opt_norm_result* d_norm,
+                   void* stream, int algo) {
+  if (P == nullptr || hp == nullptr || step < 1 || hp->reserved != 0) return OPT_EINVAL;
+  if (hp->rounding != OPT_ROUND_NEAREST && hp->rounding != OPT_ROUND_STOCHASTIC) return OPT_EINVAL;
+  if (d_norm != nullptr && ((uintptr_t)d_norm & 7u)) return OPT_EALIGN;
+  if (algo == ALGO_ADEMAMIX) {
+    if (P->combo != SC_F32) return OPT_EUNSUPPORTED;
+    if (!P->has_m2) return OPT_EINVAL;
+  }
+  StepArgs a;
+  std::memset(&a, 0, sizeof a);
+  int st = opt_step_scalars_compute(hp, step, &a.sc);
+  if (st != OPT_OK) return st;
+  a.tensors = P->d_tensors;
+  a.chunks = P->d_chunks;
+  a.seed_lo = (uint32_t)hp->seed;
+  a.seed_hi = (uint32_t)(hp->seed >> 32);
+  a.step32 = (uint32_t)step;
+  a.d_norm = d_norm;
+  a.unchanged = hp->count_unchanged ? P->d_unchanged : nullptr;
+
+  DeviceGuard g(P->device);
+  if (!g.ok) return OPT_ECUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+    a.chunk_begin = P->bucket_begin[b];
+    a.chunk_end = P->bucket_begin[b + 1];
+    if (a.chunk_end <= a.chunk_begin) continue;
+    const int dt = b == 0 ? OPT_F32 : OPT_BF16;
+    if (P->combo == SC_F32) e = launch_step_fp32_states(dt, algo, a, P->sm_count, s);
+    else e = launch_step_lowp_states(dt, P->combo, hp->rounding == OPT_ROUND_STOCHASTIC, a,
+                                     P->sm_count, s);
+  }
+  return cuda_status(e);
+}
+
+int opt_adamw_step(opt_plan* P, const opt_hparams* hp, int64_t step, const opt_norm_result* d_norm,
+                   void* stream) {
+  return do_step(P, hp, step, d_norm, stream, ALGO_ADAMW);
+}
+
+int opt_ademamix_step(opt_plan* P, const opt_hparams* hp, int64_t step, const opt_norm_result* d_norm,
+                      void* stream) {
+  return do_step(P, hp, step, d_norm, stream, ALGO_ADEMAMIX);
+}
+
+int opt_unchanged_count(opt_plan* P, uint64_t* h_count, void* stream) {
+  if (P == nullptr || h_count == nullptr) return OPT_EINVAL;
+  DeviceGuard g(P->device);
+  if (!g.ok) return OPT_ECUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned long long v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, P->d_unchanged, 8, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(P->d_unchanged, 0, 8, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_status(e);
+  *h_count = v;
+  return OPT_OK;
+}
+
+int opt_grads_upload(opt_plan* P, const void* const* h_grad, void* stream) {
+  if (P == nullptr || (P->n > 0 && h_grad == nullptr)) return OPT_EINVAL;
+  for (int32_t i = 0; i < P->n; ++i)
+    if (P->grad_bytes[(size_t)i] > 0 && h_grad[i] == nullptr) return OPT_EINVAL;
+  DeviceGuard g(P->device);
+  if (!g.ok) return OPT_ECUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int32_t i = 0; i < P->n; ++i) {
+    if (P->grad_bytes[(size_t)i] == 0) continue;
+    cudaError_t e = cudaMemcpyAsync(P->grad_dev[(size_t)i], h_grad[i], (size_t)P->grad_bytes[(size_t)i],
+                                    cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  return OPT_OK;
+}
+
+int opt_encode(const float* d_in, void* d_out, int64_t n, int32_t dtype, int32_t rounding, uint64_t seed,
+               uint32_t tensor_index, int64_t step, void* stream) {
+  if (n < 0 || step < 0) return OPT_EINVAL;
+  if (dtype != OPT_BF16 && dtype != OPT_E4M3 && dtype != OPT_E2M2) return OPT_EUNSUPPORTED;
+  if (rounding != OPT_ROUND_NEAREST && rounding != OPT_ROUND_STOCHASTIC) return OPT_EINVAL;
+  if (n == 0) return OPT_OK;
+  if (d_in == nullptr || d_out == nullptr) return OPT_EINVAL;
+  if (!aligned16(d_in) || !aligned16(d_out)) return OPT_EALIGN;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return OPT_ECUDA;
+  return cuda_status(launch_encode(d_in, d_out, n, dtype, rounding == OPT_ROUND_STOCHASTIC,
+                                   (uint32_t)seed, (uint32_t)(seed >> 32), tensor_index, (uint32_t)step,
+                                   sms, static_cast<cudaStream_t>(stream)));
+}
+
+int opt_decode(const void* d_in, float* d_out, int64_t n, int32_t dtype, void* stream) {
+  if (n < 0) return OPT_EINVAL;
+  if (dtype != OPT_BF16 && dtype != OPT_E4M3 && dtype != OPT_E2M2) return OPT_EUNSUPPORTED;
+  if (n == 0) return OPT_OK;
+  if (d_in == nullptr || d_out == nullptr) return OPT_EINVAL;
+  if (!aligned16(d_in) || !aligned16(d_out)) return OPT_EALIGN;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return OPT_ECUDA;
+  return cuda_status(launch_decode(d_in, d_out, n, dtype, sms, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

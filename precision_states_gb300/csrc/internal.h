@@ -1,0 +1,43 @@
+// internal.h -- host-side declarations shared by the API layer and the
+// kernel launch files.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "opt.h"
+
+namespace psopt {
+
+struct TensorDesc;
+struct NormSlot;
+struct StepArgs;
+
+// state combinations (m_dtype, v_dtype) built into the library
+enum StateCombo { SC_F32 = 0, SC_BF16_BF16 = 1, SC_BF16_E4M3 = 2, SC_BF16_E2M2 = 3 };
+enum Algo { ALGO_ADAMW = 0, ALGO_ADEMAMIX = 1 };
+
+int state_combo(int32_t m_dtype, int32_t v_dtype);   // -1 if not built
+
+// gradient norm: pass 1 for one dtype bucket into slots[0 .. OPT_NORM_SLOTS)
+cudaError_t launch_norm_partials(int grad_dtype, const TensorDesc* tensors,
+                                 const opt_chunk* chunks, int64_t chunk_begin,
+                                 int64_t chunk_end, NormSlot* slots, cudaStream_t s);
+// gradient norm: pass 2 over n_slots slots
+cudaError_t launch_norm_finalize(const NormSlot* slots, int n_slots, double max_norm,
+                                 opt_norm_result* out, cudaStream_t s);
+
+// fused step for one bucket (persistent grid of sm_count x occupancy CTAs)
+cudaError_t launch_step_fp32_states(int grad_dtype, int algo, const StepArgs& args, int sm_count,
+                                    cudaStream_t s);
+cudaError_t launch_step_lowp_states(int grad_dtype, int combo, int stochastic, const StepArgs& args,
+                                    int sm_count, cudaStream_t s);
+
+// standalone codecs
+cudaError_t launch_encode(const float* in, void* out, int64_t n, int dtype, int stochastic,
+                          uint32_t seed_lo, uint32_t seed_hi, uint32_t tensor,
+                          uint32_t step32, int sm_count, cudaStream_t s);
+cudaError_t launch_decode(const void* in, float* out, int64_t n, int dtype, int sm_count,
+                          cudaStream_t s);
+
+}  // namespace psopt

@@ -1,0 +1,341 @@
+// norm.cu -- deterministic global gradient norm in two launches.
+//
+// "perf(training): fused multi-tensor gradient-norm reduction" (NeMo
+// Automodel PR #3685), 'Correctness properties': values are widened in
+// registers (never squared in BF16), the decomposition into chunks comes from
+// sizes only and there are no atomics, so the norm is bit-identical run to
+// run; NaNs are counted because a max that ignores NaN would hide them.
+//
+// GB300 design.  Blackwell Ultra's FP64 rate is a small fraction of its FP32
+// rate, so one fp64 operation per element would make this streaming pass
+// compute-bound.  Instead each thread accumulates squares in error-free
+// float-float form (Knuth's TwoSum, exact; BF16 squares are exact in fp32 and
+// FP32 squares are split exactly with an FMA), two lanes at a time with the
+// packed f32x2 instructions.  The per-chunk float-float sums are merged into
+// a per-thread float-float accumulator, converted to double once per thread,
+// and reduced across the CTA in double in a fixed tree.  Only a thread whose
+// elements in a chunk hold a NaN, an Inf, or a magnitude outside
+// [2^-40, 2^40] (where fp32 squares could overflow or lose bits) re-reads
+// those elements and accumulates them in double -- a rare, exact slow path.
+//
+// Pass 1 runs OPT_NORM_SLOTS CTAs per dtype bucket; slot s sums chunks
+// s, s + OPT_NORM_SLOTS, ... of the bucket in that order.  Pass 2 is one CTA
+// that reduces all slots in a fixed order and derives norm2, the inf-norm,
+// the NaN/Inf status and the clip coefficient.
+#include "common.cuh"
+#include "internal.h"
+
+namespace psopt {
+namespace {
+
+constexpr int kNormThreads = 256;
+
+// ---------------------------------------------------- packed f32x2 helpers
+typedef unsigned long long f2_t;   // two fp32 lanes in one 64-bit register
+
+__device__ __forceinline__ f2_t pk(float a, float b) {
+  f2_t r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpk(f2_t v, float& a, float& b) {
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ f2_t add2(f2_t a, f2_t b) {
+  f2_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2_t sub2(f2_t a, f2_t b) {
+  f2_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2_t mul2(f2_t a, f2_t b) {
+  f2_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2_t fma2(f2_t a, f2_t b, f2_t c) {
+  f2_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// Two float-float accumulators (lane x, lane y): value = hi + lo per lane.
+struct FF2 {
+  f2_t hi, lo;
+};
+
+// TwoSum of hi and x per lane; the exact rounding error goes into lo.
+__device__ __forceinline__ void ff2_add(FF2& a, f2_t x) {
+  const f2_t s = add2(a.hi, x);
+  const f2_t bb = sub2(s, a.hi);
+  const f2_t aa = sub2(s, bb);
+  const f2_t e = add2(sub2(a.hi, aa), sub2(x, bb));
+  a.lo = add2(a.lo, e);
+  a.hi = s;
+}
+
+// BF16 pair in one 32-bit word -> exact squares of both, added.
+__device__ __forceinline__ void acc_bf16x2(FF2& a, uint32_t w) {
+  const f2_t x = pk(u2f(w << 16), u2f(w & 0xFFFF0000u));
+  ff2_add(a, mul2(x, x));
+}
+
+// FP32 pair: x*x = p + pe exactly (FMA split), both parts added.
+__device__ __forceinline__ void acc_f32x2(FF2& a, float x0, float x1) {
+  const f2_t x = pk(x0, x1);
+  const f2_t p = mul2(x, x);
+  const f2_t pe = fma2(x, x, p ^ 0x8000000080000000ull);   // x*x - p, exact
+  ff2_add(a, p);
+  a.lo = add2(a.lo, pe);
+}
+
+// Scalar float-float accumulator (H, L) += (h, l).
+__device__ __forceinline__ void ff_merge(float& H, float& L, float h, float l) {
+  const float s = __fadd_rn(H, h);
+  const float bb = __fsub_rn(s, H);
+  const float aa = __fsub_rn(s, bb);
+  float e = __fadd_rn(__fsub_rn(H, aa), __fsub_rn(h, bb));
+  e = __fadd_rn(e, __fadd_rn(L, l));
+  H = __fadd_rn(s, e);
+  L = __fsub_rn(e, __fsub_rn(H, s));
+}
+
+template <int GT>
+struct GradTraits;
+template <>
+struct GradTraits<OPT_BF16> {
+  static constexpr int kVec = 8;                 // elements per 16-byte vector
+  static constexpr uint32_t kHi = 0x5380u;       // |g| <= 2^40 (BF16 bits)
+  static constexpr uint32_t kLo = 0x2B80u;       // |g| >= 2^-40
+  __device__ static float elem(const void* g, int64_t i) {
+    return u2f((uint32_t)(static_cast<const uint16_t*>(g)[i]) << 16);
+  }
+};
+template <>
+struct GradTraits<OPT_F32> {
+  static constexpr int kVec = 4;
+  static constexpr uint32_t kHi = 0x53800000u;   // 2^40
+  static constexpr uint32_t kLo = 0x2B800000u;   // 2^-40
+  __device__ static float elem(const void* g, int64_t i) {
+    return static_cast<const float*>(g)[i];
+  }
+};
+
+// Accumulate one 16-byte vector; returns the max of |x| bits over it.
+template <int GT>
+__device__ __forceinline__ uint32_t acc_vec(FF2& a, uint4 w);
+
+template <>
+__device__ __forceinline__ uint32_t acc_vec<OPT_BF16>(FF2& a, uint4 w) {
+  acc_bf16x2(a, w.x);
+  acc_bf16x2(a, w.y);
+  acc_bf16x2(a, w.z);
+  acc_bf16x2(a, w.w);
+  const uint32_t m = __vmaxu2(__vmaxu2(w.x & 0x7FFF7FFFu, w.y & 0x7FFF7FFFu),
+                              __vmaxu2(w.z & 0x7FFF7FFFu, w.w & 0x7FFF7FFFu));
+  return max(m & 0xFFFFu, m >> 16);
+}
+
+template <>
+__device__ __forceinline__ uint32_t acc_vec<OPT_F32>(FF2& a, uint4 w) {
+  acc_f32x2(a, u2f(w.x), u2f(w.y));
+  acc_f32x2(a, u2f(w.z), u2f(w.w));
+  return max(max(w.x & 0x7FFFFFFFu, w.y & 0x7FFFFFFFu), max(w.z & 0x7FFFFFFFu, w.w & 0x7FFFFFFFu));
+}
+
+// Exact slow path over one thread's own elements of a chunk (rare: only
+// when they hold a NaN, an Inf or an extreme magnitude).
+struct SlowAcc {
+  double sum;
+  unsigned long long nans, infs;
+  uint32_t mxbits;
+};
+
+template <int GT>
+__device__ __noinline__ void slow_chunk(const char* g, int nvec, int rem, int tid, bool owns_tail,
+                                        SlowAcc& a) {
+  using T = GradTraits<GT>;
+  constexpr int V = T::kVec;
+  auto visit = [&](float x) {
+    if (x != x) { ++a.nans; return; }
+    if (fabsf(x) == __int_as_float(0x7F800000)) { ++a.infs; return; }
+    a.sum += (double)x * (double)x;
+    a.mxbits = max(a.mxbits, f2u(fabsf(x)));
+  };
+  for (int vv = tid; vv < nvec; vv += kNormThreads)
+    for (int j = 0; j < V; ++j) visit(T::elem(g, (int64_t)vv * V + j));
+  if (owns_tail)
+    for (int j = 0; j < rem; ++j) visit(T::elem(g, (int64_t)nvec * V + j));
+}
+
+template <int GT>
+__global__ void __launch_bounds__(kNormThreads, 8)
+norm_partials_kernel(const TensorDesc* __restrict__ tensors, const opt_chunk* __restrict__ chunks,
+                     int64_t cbegin, int64_t cend, NormSlot* __restrict__ slots) {
+  using T = GradTraits<GT>;
+  constexpr int V = T::kVec;
+  const int tid = threadIdx.x;
+  const int slot = blockIdx.x;
+
+  float AH = 0.0f, AL = 0.0f;      // fast-path float-float accumulator
+  uint32_t mxbits = 0;             // fast-path max |g|, fp32 bits
+  SlowAcc slow = {0.0, 0ull, 0ull, 0u};
+
+  for (int64_t c = cbegin + slot; c < cend; c += OPT_NORM_SLOTS) {
+    const opt_chunk ch = chunks[c];
+    const char* g = static_cast<const char*>(tensors[ch.tensor].g) +
+                    ch.start * (int64_t)(GT == OPT_BF16 ? 2 : 4);
+    const int nvec = (int)(ch.len / V);
+    const int rem = (int)(ch.len % V);
+
+    FF2 acc = {0ull, 0ull};
+    uint32_t cmax = 0;
+    int v = tid;
+    // four independent 16-byte loads in flight per thread per iteration
+    for (; v + 3 * kNormThreads < nvec; v += 4 * kNormThreads) {
+      const uint4 w0 = ld_nc_u4(g + (int64_t)v * 16);
+      const uint4 w1 = ld_nc_u4(g + (int64_t)(v + kNormThreads) * 16);
+      const uint4 w2 = ld_nc_u4(g + (int64_t)(v + 2 * kNormThreads) * 16);
+      const uint4 w3 = ld_nc_u4(g + (int64_t)(v + 3 * kNormThreads) * 16);
+      cmax = max(cmax, acc_vec<GT>(acc, w0));
+      cmax = max(cmax, acc_vec<GT>(acc, w1));
+      cmax = max(cmax, acc_vec<GT>(acc, w2));
+      cmax = max(cmax, acc_vec<GT>(acc, w3));
+    }
+    for (; v < nvec; v += kNormThreads) cmax = max(cmax, acc_vec<GT>(acc, ld_nc_u4(g + (int64_t)v * 16)));
+    // ragged tail: the thread that would own vector nvec loads it element-wise
+    const bool owns_tail = rem > 0 && (nvec % kNormThreads) == tid;
+    if (owns_tail) {
+      uint32_t wv[4] = {0u, 0u, 0u, 0u};
+      for (int j = 0; j < rem; ++j) {
+        const uint32_t bits = f2u(T::elem(g, (int64_t)nvec * V + j));
+        if (GT == OPT_BF16) wv[j >> 1] |= (bits >> 16) << (16 * (j & 1));
+        else                wv[j] = bits;
+      }
+      cmax = max(cmax, acc_vec<GT>(acc, make_uint4(wv[0], wv[1], wv[2], wv[3])));
+    }
+
+    const bool fast = cmax <= T::kHi && (cmax >= T::kLo || cmax == 0u);
+    if (fast) {
+      float hx, hy, lx, ly;
+      unpk(acc.hi, hx, hy);
+      unpk(acc.lo, lx, ly);
+      ff_merge(AH, AL, hx, lx);
+      ff_merge(AH, AL, hy, ly);
+      mxbits = max(mxbits, GT == OPT_BF16 ? (cmax << 16) : cmax);
+    } else {
+      slow_chunk<GT>(g, nvec, rem, tid, owns_tail, slow);
+    }
+  }
+
+  // fixed-order CTA reduction in double
+  __shared__ double s_sum[kNormThreads];
+  __shared__ unsigned long long s_nan[kNormThreads], s_inf[kNormThreads];
+  __shared__ uint32_t s_max[kNormThreads];
+  s_sum[tid] = ((double)AH + (double)AL) + slow.sum;
+  s_nan[tid] = slow.nans;
+  s_inf[tid] = slow.infs;
+  s_max[tid] = max(mxbits, slow.mxbits);
+  __syncthreads();
+  for (int w = kNormThreads / 2; w > 0; w >>= 1) {
+    if (tid < w) {
+      s_sum[tid] += s_sum[tid + w];
+      s_nan[tid] += s_nan[tid + w];
+      s_inf[tid] += s_inf[tid + w];
+      s_max[tid] = max(s_max[tid], s_max[tid + w]);
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    NormSlot r;
+    r.sum = s_sum[0];
+    r.nan_count = s_nan[0];
+    r.inf_count = s_inf[0];
+    r.maxabs = u2f(s_max[0]);
+    r.pad = 0;
+    slots[slot] = r;
+  }
+}
+
+__global__ void __launch_bounds__(kNormThreads)
+norm_finalize_kernel(const NormSlot* __restrict__ slots, int n, double max_norm,
+                     opt_norm_result* __restrict__ out) {
+  __shared__ double s_sum[kNormThreads];
+  __shared__ unsigned long long s_nan[kNormThreads], s_inf[kNormThreads];
+  __shared__ float s_max[kNormThreads];
+  const int tid = threadIdx.x;
+  double sum = 0.0;
+  unsigned long long nans = 0, infs = 0;
+  float mx = 0.0f;
+  for (int i = tid; i < n; i += kNormThreads) {
+    sum += slots[i].sum;
+    nans += slots[i].nan_count;
+    infs += slots[i].inf_count;
+    mx = fmaxf(mx, slots[i].maxabs);
+  }
+  s_sum[tid] = sum;
+  s_nan[tid] = nans;
+  s_inf[tid] = infs;
+  s_max[tid] = mx;
+  __syncthreads();
+  for (int w = kNormThreads / 2; w > 0; w >>= 1) {
+    if (tid < w) {
+      s_sum[tid] += s_sum[tid + w];
+      s_nan[tid] += s_nan[tid + w];
+      s_inf[tid] += s_inf[tid + w];
+      s_max[tid] = fmaxf(s_max[tid], s_max[tid + w]);
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    opt_norm_result r;
+    r.nan_count = s_nan[0];
+    r.inf_count = s_inf[0];
+    if (r.nan_count > 0) {
+      r.sumsq = r.norm2 = r.norm_inf = __longlong_as_double(0x7FF8000000000000ll);
+      r.clip_coef = 1.0f;
+      r.status = OPT_ENONFINITE;
+    } else if (r.inf_count > 0) {
+      r.sumsq = r.norm2 = r.norm_inf = __longlong_as_double(0x7FF0000000000000ll);
+      r.clip_coef = 1.0f;
+      r.status = OPT_ENONFINITE;
+    } else {
+      r.sumsq = s_sum[0];
+      r.norm2 = sqrt(r.sumsq);
+      r.norm_inf = (double)s_max[0];
+      double coef = 1.0;
+      if (max_norm > 0.0) {
+        coef = max_norm / (r.norm2 + 1e-6);
+        if (coef > 1.0) coef = 1.0;
+      }
+      r.clip_coef = (float)coef;
+      r.status = OPT_OK;
+    }
+    *out = r;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_norm_partials(int grad_dtype, const TensorDesc* tensors, const opt_chunk* chunks,
+                                 int64_t chunk_begin, int64_t chunk_end, NormSlot* slots,
+                                 cudaStream_t s) {
+  if (grad_dtype == OPT_BF16)
+    norm_partials_kernel<OPT_BF16><<<OPT_NORM_SLOTS, kNormThreads, 0, s>>>(tensors, chunks, chunk_begin,
+                                                                           chunk_end, slots);
+  else
+    norm_partials_kernel<OPT_F32><<<OPT_NORM_SLOTS, kNormThreads, 0, s>>>(tensors, chunks, chunk_begin,
+                                                                          chunk_end, slots);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_norm_finalize(const NormSlot* slots, int n_slots, double max_norm,
+                                 opt_norm_result* out, cudaStream_t s) {
+  norm_finalize_kernel<<<1, kNormThreads, 0, s>>>(slots, n_slots, max_norm, out);
+  return cudaGetLastError();
+}
+
+}  // namespace psopt

@@ -1,0 +1,118 @@
+"""GPU parity of opt_grad_norm with the oracle: relative error <= 1e-12,
+bit-identical repeats, NaN/Inf counts and status, the exact slow path for
+extreme magnitudes, dtype buckets, empty and ragged lists."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import precision_states_gb300 as ps
+import workloads as W
+from harness import oracle_norm_parallel, rel_err
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-12
+
+
+def plan_for(grads):
+    params = [torch.zeros(g.numel(), device="cuda") for g in grads]
+    m = [torch.zeros(g.numel(), device="cuda") for g in grads]
+    v = [torch.zeros(g.numel(), device="cuda") for g in grads]
+    return ps.Plan(params, grads, m, v)
+
+
+def host(grads):
+    return [W.to_numpy_codes(g) for g in grads]
+
+
+def check(grads, max_norm=1.0):
+    plan = plan_for(grads)
+    got = plan.grad_norm(max_norm)
+    want = oracle.grad_norm(host(grads), max_norm)
+    assert got.nan_count == want["nan_count"] and got.inf_count == want["inf_count"]
+    assert got.status == want["status"]
+    if want["status"] == 0:
+        assert rel_err(got.norm2, want["norm2"]) <= TOL, (got.norm2, want["norm2"])
+        assert rel_err(got.sumsq, want["sumsq"]) <= 2 * TOL
+        assert got.norm_inf == want["norm_inf"]
+        assert got.clip_coef == want["clip_coef"]
+    else:
+        for k in ("norm2", "norm_inf"):
+            a, b = getattr(got, k), want[k]
+            assert (math.isnan(a) and math.isnan(b)) or a == b, k
+    return plan, got
+
+
+@pytest.mark.parametrize("gdt", ["bf16", "f32"])
+def test_sweep_sizes(gdt):
+    w = W.workload("sweep", grad_dtype=gdt)
+    grads = W.make_grads(w, "cuda", step=1, seed=3)
+    check(grads)
+
+
+def test_mixed_dtype_buckets():
+    w = W.workload("sweep")
+    g16 = W.make_grads(w, "cuda", step=1, seed=4)
+    g32 = W.make_grads(W.workload("sweep", grad_dtype="f32"), "cuda", step=1, seed=5)
+    mixed = [g16[i] if i % 3 else g32[i] for i in range(len(g16))]
+    check(mixed)
+
+
+def test_repeatable_bitwise():
+    w = W.workload("clip_740")
+    grads = W.make_grads(w, "cuda", step=1, seed=6)
+    plan = plan_for(grads)
+    a = plan.grad_norm(1.0).as_dict()
+    for _ in range(3):
+        assert plan.grad_norm(1.0).as_dict() == a
+
+
+def test_clip740_full_size():
+    w = W.workload("clip_740")
+    grads = W.make_grads(w, "cuda", step=1, seed=7)
+    plan = plan_for(grads)
+    got = plan.grad_norm(w.max_norm)
+    want = oracle_norm_parallel(host(grads), w.max_norm)
+    assert rel_err(got.norm2, want["norm2"]) <= TOL
+    assert got.norm_inf == want["norm_inf"] and got.clip_coef == want["clip_coef"]
+
+
+@pytest.mark.parametrize("kinds", [("nan", "+inf", "-inf"), ("nan",), ("+inf",), ("-inf",)])
+def test_nonfinite_run(kinds):
+    w = W.workload("clip_740")
+    grads = W.make_grads(w, "cuda", step=1, seed=8)
+    touched = W.inject_nonfinite(grads, seed=21, kinds=kinds)
+    assert len(touched) == 7
+    _, got = check(grads)
+    assert got.status == ps.OPT_ENONFINITE
+
+
+@pytest.mark.parametrize("gdt", ["bf16", "f32"])
+def test_extreme_magnitudes_slow_path(gdt):
+    rng = np.random.default_rng(11)
+    dt = torch.bfloat16 if gdt == "bf16" else torch.float32
+    vals = [np.full(1000, 3.0e30), rng.standard_normal(5000) * 1e-30, np.full(17, 1e-38),
+            rng.standard_normal(70001), np.array([1e-45, 2e38, -3e38, 1e-20])]
+    grads = [torch.from_numpy(v.astype(np.float32)).to(dt).cuda() for v in vals]
+    check(grads, max_norm=0.0)
+    # tiny-only list: every chunk on the exact path
+    check([torch.from_numpy((rng.standard_normal(9999) * 1e-25).astype(np.float32)).to(dt).cuda()], 0.0)
+
+
+def test_empty_and_zero_sized():
+    plan = ps.Plan([], [], [], [])
+    r = plan.grad_norm(1.0)
+    assert r.norm2 == 0.0 and r.norm_inf == 0.0 and r.status == 0 and r.clip_coef == 1.0
+    z = torch.zeros(0, dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(5, dtype=torch.bfloat16, device="cuda")
+    _, r = check([z, g, z])
+    assert r.norm2 == math.sqrt(5.0)
+
+
+def test_all_zero_and_no_clip():
+    grads = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for n in (1, 33, 70000)]
+    _, r = check(grads, max_norm=0.0)
+    assert r.norm2 == 0.0 and r.clip_coef == 1.0

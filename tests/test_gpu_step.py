@@ -1,0 +1,155 @@
+"""GPU parity of the fused steps with the oracle on the size sweep (tile edges
+and ragged tails): FP32 states within 1e-6 (1+|x|) after one step and 1e-5
+(1+|x|) after 100 steps; low-precision state codes identical (stochastic
+rounding) or >= 99.99 % identical, one step off (nearest); unchanged counts
+exact; non-finite norm skips the step; the BF16 v invariant on the GPU."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import precision_states_gb300 as ps
+import workloads as W
+from harness import (GpuSide, OracleSide, assert_close_scaled, compare_codes, decode, hp_for)
+
+pytestmark = pytest.mark.gpu
+
+
+def run_parity(w, steps, tol, rounding="nearest", clip=True, seed=0, count=False, check_every=None):
+    gpu = GpuSide(w, seed=seed)
+    orc = OracleSide(gpu, range(len(w.sizes)))
+    ghp, ohp = hp_for(w, rounding=rounding, seed=77, count=count)
+    sr = rounding == "stochastic"
+    for t in range(1, steps + 1):
+        W.fill_grads(w, gpu.grads, t, seed)
+        g_np = [W.to_numpy_codes(g) for g in gpu.grads]
+        coef = 1.0
+        if clip and w.max_norm > 0:
+            coef = oracle.grad_norm(g_np, w.max_norm)["clip_coef"]
+        gpu.step(t, ghp, clip and w.max_norm > 0)
+        same = orc.step(t, g_np, ohp, coef, sr, 77)
+        if count:
+            assert gpu.plan.unchanged_count() == same
+        if check_every and t % check_every == 0:
+            compare(gpu, orc, w, tol, sr)
+    torch.cuda.synchronize()
+    compare(gpu, orc, w, tol, sr)
+    return gpu, orc
+
+
+def compare(gpu, orc, w, tol, sr):
+    for k, i in enumerate(orc.idx):
+        n = w.sizes[i]
+        assert_close_scaled(W.to_numpy_codes(gpu.params[i]), orc.p[k], tol, f"p[{i}]")
+        gm, gv = W.to_numpy_codes(gpu.m[i]), W.to_numpy_codes(gpu.v[i])
+        if w.m_dtype == "f32":
+            assert_close_scaled(gm, orc.m[k], tol, f"m[{i}]")
+            assert_close_scaled(gv, orc.v[k], tol, f"v[{i}]")
+        else:
+            compare_codes(gm, orc.m[k], "bf16", n, exact=sr, what=f"m[{i}]")
+            compare_codes(gv, orc.v[k], w.v_dtype, n, exact=sr, what=f"v[{i}]")
+        if orc.m2 is not None:
+            assert_close_scaled(W.to_numpy_codes(gpu.m2[i]), orc.m2[k], tol, f"m2[{i}]")
+
+
+@pytest.mark.parametrize("algo", ["adamw", "ademamix"])
+@pytest.mark.parametrize("gdt", ["bf16", "f32"])
+def test_fp32_states_one_step(algo, gdt):
+    w = W.workload("sweep", algo=algo, grad_dtype=gdt, hp=dict(lr=0.1, weight_decay=0.1))
+    run_parity(w, 1, 1e-6)
+
+
+@pytest.mark.parametrize("algo", ["adamw", "ademamix"])
+def test_fp32_states_hundred_steps(algo):
+    w = W.workload("sweep", algo=algo, hp=dict(lr=1e-2, weight_decay=0.1))
+    run_parity(w, 100, 1e-5, check_every=25)
+
+
+def test_adamw_1m_config():
+    """The 1M-element AdamW workload itself: lr = wd = 0.1, 10 steps."""
+    w = W.workload("adamw_1m")
+    run_parity(w, 1, 1e-6, clip=False)
+    run_parity(w, 10, 1e-5, clip=False)
+
+
+@pytest.mark.parametrize("v_dtype", ["bf16", "e4m3", "e2m2"])
+@pytest.mark.parametrize("rounding", ["nearest", "stochastic"])
+@pytest.mark.parametrize("gdt", ["bf16", "f32"])
+def test_lowp_states_codes(v_dtype, rounding, gdt):
+    w = W.workload("sweep", grad_dtype=gdt, m_dtype="bf16", v_dtype=v_dtype,
+                   hp=dict(lr=1e-3, weight_decay=0.1, beta2=0.999), sigma_decay_steps=12)
+    run_parity(w, 12, 1e-6, rounding=rounding, count=True, check_every=4)
+
+
+def test_nonfinite_norm_skips_step():
+    w = W.workload("clip_740")
+    gpu = GpuSide(w, seed=3)
+    W.inject_nonfinite(gpu.grads, seed=5)
+    before = [t.clone() for t in gpu.params + gpu.m + gpu.v]
+    ghp, _ = hp_for(w)
+    r = gpu.plan.grad_norm(w.max_norm)
+    assert r.status == ps.OPT_ENONFINITE
+    gpu.step(1, ghp, clip=True)
+    torch.cuda.synchronize()
+    for a, b in zip(before, gpu.params + gpu.m + gpu.v):
+        assert torch.equal(a, b)
+
+
+def test_bf16_v_never_moves_with_zero_grad():
+    """"When Small Updates Disappear" sec. 2.2 on the GPU: b2 = 0.999,
+    nearest rounding, g = 0 -> every BF16 v code stays put."""
+    w = W.workload("sweep", m_dtype="bf16", v_dtype="bf16", hp=dict(beta2=0.999))
+    gpu = GpuSide(w, seed=1)
+    rng = np.random.default_rng(2)
+    for v in gpu.v:
+        vals = torch.from_numpy(np.exp(rng.uniform(-10, 2, v.numel())).astype(np.float32))
+        v.copy_(vals.to(torch.bfloat16).view(torch.int16).cuda())
+    before = [v.clone() for v in gpu.v]
+    ghp, _ = hp_for(w, count=True)
+    for t in range(1, 6):
+        for g in gpu.grads:
+            g.zero_()
+        gpu.step(t, ghp, clip=False)
+        assert gpu.plan.unchanged_count() == w.numel
+    for a, b in zip(before, gpu.v):
+        assert torch.equal(a, b)
+
+
+def test_repeatable_and_seed_sensitive():
+    w = W.workload("sweep", m_dtype="bf16", v_dtype="e4m3")
+    outs = []
+    for seed in (5, 5, 6):
+        gpu = GpuSide(w, seed=0)
+        ghp, _ = hp_for(w, rounding="stochastic", seed=seed)
+        for t in (1, 2):
+            W.fill_grads(w, gpu.grads, t, 0)
+            gpu.step(t, ghp, clip=False)
+        torch.cuda.synchronize()
+        outs.append(torch.cat([x.view(torch.uint8) for x in gpu.m + gpu.v]))
+    assert torch.equal(outs[0], outs[1])
+    assert not torch.equal(outs[0], outs[2])
+
+
+def test_invalid_arguments():
+    w = W.workload("sweep")
+    gpu = GpuSide(w)
+    ghp, _ = hp_for(w)
+    with pytest.raises(ps.OptError) as e:
+        gpu.plan.adamw_step(ghp, 0)
+    assert e.value.status == ps.OPT_EINVAL
+    with pytest.raises(ps.OptError) as e:
+        gpu.plan.ademamix_step(ghp, 1)          # no m2 buffers in this plan
+    assert e.value.status == ps.OPT_EINVAL
+    bad = ps.hparams(rounding="nearest")
+    bad.rounding = 7
+    with pytest.raises(ps.OptError):
+        gpu.plan.adamw_step(bad, 1)
+    p = torch.zeros(9, device="cuda")
+    with pytest.raises(ps.OptError) as e:      # misaligned pointer
+        ps.Plan([p[1:]], [torch.zeros(8, device="cuda")], [torch.zeros(8, device="cuda")],
+                [torch.zeros(8, device="cuda")])
+    assert e.value.status == ps.OPT_EALIGN
+    with pytest.raises(ps.OptError) as e:      # FP8 gradients are not supported
+        ps.Plan([p[:8]], [torch.zeros(8, dtype=torch.float8_e4m3fn, device="cuda")],
+                [torch.zeros(8, device="cuda")], [torch.zeros(8, device="cuda")])
+    assert e.value.status == ps.OPT_EUNSUPPORTED
