@@ -61,6 +61,7 @@ extern "C" {
 #define OPT_EALIGN       -3   /* a device pointer not 16-byte aligned */
 #define OPT_ECUDA        -4   /* a CUDA runtime call failed */
 #define OPT_ENOMEM       -5   /* workspace allocation failed */
+#define OPT_ELIMIT       -6   /* list exceeds opt_grad_norm_noalloc's fixed limits */
 
 /* ---- storage types ----------------------------------------------------
  * OPT_F32   IEEE binary32.
@@ -204,6 +205,40 @@ int opt_encode(const float* d_in, void* d_out, int64_t n, int32_t dtype,
                int32_t rounding, uint64_t seed, uint32_t tensor_index,
                int64_t step, void* stream);
 int opt_decode(const void* d_in, float* d_out, int64_t n, int32_t dtype, void* stream);
+
+/* ---- gradient norm without allocation ------------------------------------
+ * The same global norm as opt_grad_norm (same kernels, same chunk order, so
+ * the same result bit for bit), for callers that cannot allocate device
+ * memory and therefore cannot build a plan: code running under a framework
+ * whose caching allocator owns all device memory, in a runtime with a fixed
+ * memory budget reserved up front, or at a point where a synchronising
+ * cudaMalloc would stall the pipeline.  This call allocates nothing -- no
+ * cudaMalloc, cudaFree or allocating library routine, and no host heap.  The
+ * pages describe no such variant; it has no counterpart there.
+ *
+ * Scratch: one fixed device array inside the library (4,927,488 bytes, held
+ * by every GPU that loads the library until the process exits), large enough
+ * for OPT_NOALLOC_MAX_TENSORS tensors and OPT_NOALLOC_MAX_CHUNKS chunks of
+ * OPT_CHUNK_ELEMS elements (about 8.6e9 elements).  Larger lists are rejected
+ * with OPT_ELIMIT before any GPU work.
+ *
+ * Inputs: n tensors; numel, grad (device pointers, 16-byte aligned) and
+ * grad_dtype (OPT_F32 or OPT_BF16) are HOST arrays, copied into the scratch
+ * array on `stream` during the call, so they may be reused when it returns.
+ * d_out: device, 8-byte aligned, 48 bytes.  Returns OPT_OK or an error
+ * status; the norm's own status (OPT_ENONFINITE) is in d_out->status.
+ *
+ * The first call on each device looks up the scratch array's device address
+ * (with that device current) and caches it; make that first call before any
+ * stream capture.  Every call shares the one array: calls whose device work
+ * overlaps (on two streams, or from two host threads) race and must be
+ * serialised by the caller.  Each call overwrites every part of the array it
+ * reads, so nothing carries over from an earlier call. */
+#define OPT_NOALLOC_MAX_TENSORS 8192
+#define OPT_NOALLOC_MAX_CHUNKS 262144
+int opt_grad_norm_noalloc(int32_t n, const int64_t* numel, const void* const* grad,
+                          const int32_t* grad_dtype, double max_norm,
+                          opt_norm_result* d_out, void* stream);
 
 /* ---- host-only helpers (no GPU needed) ----------------------------------- */
 

@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(_HERE, "_build", "libpsopt.so")
 
 # ------------------------------------------------------------------ constants
 OPT_OK, OPT_ENONFINITE = 0, 1
-OPT_EINVAL, OPT_EUNSUPPORTED, OPT_EALIGN, OPT_ECUDA, OPT_ENOMEM = -1, -2, -3, -4, -5
+OPT_EINVAL, OPT_EUNSUPPORTED, OPT_EALIGN, OPT_ECUDA, OPT_ENOMEM, OPT_ELIMIT = -1, -2, -3, -4, -5, -6
+OPT_NOALLOC_MAX_TENSORS, OPT_NOALLOC_MAX_CHUNKS = 8192, 262144
 OPT_F32, OPT_BF16, OPT_E4M3, OPT_E2M2 = 0, 1, 2, 3
 OPT_ROUND_NEAREST, OPT_ROUND_STOCHASTIC = 0, 1
 OPT_CHUNK_ELEMS = 32768
@@ -73,6 +74,8 @@ _SIGS = {
                                  _c.POINTER(_c.c_int64)]),
     "opt_plan_norm_buffer": (_vp, [_vp]),
     "opt_grad_norm": (_c.c_int, [_vp, _c.c_double, _vp, _c.POINTER(opt_norm_result), _vp]),
+    "opt_grad_norm_noalloc": (_c.c_int, [_c.c_int32, _c.POINTER(_c.c_int64), _c.POINTER(_vp),
+                                         _c.POINTER(_c.c_int32), _c.c_double, _vp, _vp]),
     "opt_adamw_step": (_c.c_int, [_vp, _c.POINTER(opt_hparams), _c.c_int64, _vp, _vp]),
     "opt_ademamix_step": (_c.c_int, [_vp, _c.POINTER(opt_hparams), _c.c_int64, _vp, _vp]),
     "opt_unchanged_count": (_c.c_int, [_vp, _c.POINTER(_c.c_uint64), _vp]),

@@ -20,6 +20,7 @@ const char* opt_strerror(int status) {
     case OPT_EALIGN: return "device pointer not 16-byte aligned";
     case OPT_ECUDA: return "CUDA runtime error";
     case OPT_ENOMEM: return "out of device memory";
+    case OPT_ELIMIT: return "list exceeds the no-allocation norm's fixed limits";
     default: return "unknown status";
   }
 }
