@@ -21,10 +21,17 @@
 // streaming loads and stores (p, m, v, m2: evict-first; g: read-only path).
 // The group start is a multiple of 8 elements and every base pointer is
 // 16-byte aligned, so each stream's vector is naturally aligned (E4M3: 8
-// bytes, E2M2: 4 bytes).  The one ragged group of a tensor is handled
-// element by element.  Stochastic-rounding draws: two Philox4x32-10 calls
-// per group (counters q = e0/4 and e0/4 + 1), so each draw depends only on
-// (seed, step, tensor, element).
+// bytes, E2M2: 4 bytes).  The one ragged group of a tensor is loaded and
+// stored element by element.
+//
+// The kernel is bound by HBM latency x bytes in flight, so each thread runs a
+// two-deep software pipeline: the raw words of its next group (possibly in
+// the CTA's next chunk) are requested before the current group is decoded,
+// updated, encoded and stored.
+//
+// Stochastic-rounding draws: two Philox4x32-10 calls per group (counters
+// q = e0/4 and e0/4 + 1), so each draw depends only on (seed, step, tensor,
+// element).
 #pragma once
 
 #include "common.cuh"
@@ -33,6 +40,7 @@
 namespace psopt {
 
 constexpr int kStepThreads = 256;
+constexpr int kStepMinBlocks = 2;    // 256 x 2 threads per SM, <= 128 registers
 
 template <int COMBO>
 struct Combo;
@@ -41,105 +49,114 @@ template <> struct Combo<SC_BF16_BF16> { static constexpr int M = OPT_BF16, V = 
 template <> struct Combo<SC_BF16_E4M3> { static constexpr int M = OPT_BF16, V = OPT_E4M3; };
 template <> struct Combo<SC_BF16_E2M2> { static constexpr int M = OPT_BF16, V = OPT_E2M2; };
 
-__device__ __forceinline__ void u4_to_f4(uint4 w, float* f) {
-  f[0] = u2f(w.x); f[1] = u2f(w.y); f[2] = u2f(w.z); f[3] = u2f(w.w);
+// Raw 32-bit words of one 8-element group, as they sit in memory.
+template <int GT, int COMBO, int ALGO>
+struct Frag {
+  static constexpr int MD = Combo<COMBO>::M, VD = Combo<COMBO>::V;
+  static constexpr int NG = GT == OPT_BF16 ? 4 : 8;
+  static constexpr int NM = MD == OPT_F32 ? 8 : 4;
+  static constexpr int NV = VD == OPT_F32 ? 8 : VD == OPT_BF16 ? 4 : VD == OPT_E4M3 ? 2 : 1;
+  static constexpr int NM2 = ALGO == ALGO_ADEMAMIX ? 8 : 1;
+  uint32_t p[8], g[NG], m[NM], v[NV], m2[NM2];
+};
+
+__device__ __forceinline__ void put4(uint32_t* w, uint4 x) { w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w; }
+
+// Element j of a word array holding `bits`-wide codes (16, 8 or 4 bits).
+template <int BITS>
+__device__ __forceinline__ uint32_t code_at(const uint32_t* w, int j) {
+  if constexpr (BITS == 32) {
+    return w[j];
+  } else {
+    constexpr int PER = 32 / BITS;
+    return (w[j / PER] >> (BITS * (j % PER))) & ((1u << BITS) - 1u);
+  }
 }
-__device__ __forceinline__ uint4 f4_to_u4(const float* f) {
-  return make_uint4(f2u(f[0]), f2u(f[1]), f2u(f[2]), f2u(f[3]));
+
+template <int GT, int COMBO, int ALGO>
+__device__ __forceinline__ void load_full(const TensorDesc& td, int64_t e0, Frag<GT, COMBO, ALGO>& f) {
+  using F = Frag<GT, COMBO, ALGO>;
+  put4(f.p, ld_cs_u4(td.p + e0));
+  put4(f.p + 4, ld_cs_u4(td.p + e0 + 4));
+  if constexpr (F::NG == 4) {
+    put4(f.g, ld_nc_u4(static_cast<const uint16_t*>(td.g) + e0));
+  } else {
+    put4(f.g, ld_nc_u4(static_cast<const float*>(td.g) + e0));
+    put4(f.g + 4, ld_nc_u4(static_cast<const float*>(td.g) + e0 + 4));
+  }
+  if constexpr (F::NM == 8) {
+    put4(f.m, ld_cs_u4(static_cast<const float*>(td.m) + e0));
+    put4(f.m + 4, ld_cs_u4(static_cast<const float*>(td.m) + e0 + 4));
+  } else {
+    put4(f.m, ld_cs_u4(static_cast<const uint16_t*>(td.m) + e0));
+  }
+  if constexpr (F::NV == 8) {
+    put4(f.v, ld_cs_u4(static_cast<const float*>(td.v) + e0));
+    put4(f.v + 4, ld_cs_u4(static_cast<const float*>(td.v) + e0 + 4));
+  } else if constexpr (F::NV == 4) {
+    put4(f.v, ld_cs_u4(static_cast<const uint16_t*>(td.v) + e0));
+  } else if constexpr (F::NV == 2) {
+    const uint2 w = ld_cs_u2(static_cast<const uint8_t*>(td.v) + e0);
+    f.v[0] = w.x;
+    f.v[1] = w.y;
+  } else {
+    f.v[0] = ld_cs_u1(static_cast<const uint8_t*>(td.v) + (e0 >> 1));
+  }
+  if constexpr (ALGO == ALGO_ADEMAMIX) {
+    put4(f.m2, ld_cs_u4(td.m2 + e0));
+    put4(f.m2 + 4, ld_cs_u4(td.m2 + e0 + 4));
+  }
 }
-__device__ __forceinline__ void bf16x8_to_f(uint4 w, float* f) {
-  const uint32_t a[4] = {w.x, w.y, w.z, w.w};
+
+// The ragged group of a tensor: element-wise loads packed into the same
+// words, zero past the end (an E2M2 byte is read whole: both nibbles belong
+// to the tensor's ceil(n/2) bytes).
+template <int GT, int COMBO, int ALGO>
+__device__ __forceinline__ void load_partial(const TensorDesc& td, int64_t e0, int cnt,
+                                             Frag<GT, COMBO, ALGO>& f) {
+  using F = Frag<GT, COMBO, ALGO>;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) { f[2 * k] = u2f(a[k] << 16); f[2 * k + 1] = u2f(a[k] & 0xFFFF0000u); }
+  for (int k = 0; k < 8; ++k) f.p[k] = 0u;
+#pragma unroll
+  for (int k = 0; k < F::NG; ++k) f.g[k] = 0u;
+#pragma unroll
+  for (int k = 0; k < F::NM; ++k) f.m[k] = 0u;
+#pragma unroll
+  for (int k = 0; k < F::NV; ++k) f.v[k] = 0u;
+#pragma unroll
+  for (int k = 0; k < F::NM2; ++k) f.m2[k] = 0u;
+  for (int j = 0; j < cnt; ++j) {
+    const int64_t e = e0 + j;
+    f.p[j] = f2u(td.p[e]);
+    if constexpr (F::NG == 8) f.g[j] = f2u(static_cast<const float*>(td.g)[e]);
+    else f.g[j >> 1] |= (uint32_t)static_cast<const uint16_t*>(td.g)[e] << (16 * (j & 1));
+    if constexpr (F::NM == 8) f.m[j] = f2u(static_cast<const float*>(td.m)[e]);
+    else f.m[j >> 1] |= (uint32_t)static_cast<const uint16_t*>(td.m)[e] << (16 * (j & 1));
+    if constexpr (F::NV == 8) {
+      f.v[j] = f2u(static_cast<const float*>(td.v)[e]);
+    } else if constexpr (F::NV == 4) {
+      f.v[j >> 1] |= (uint32_t)static_cast<const uint16_t*>(td.v)[e] << (16 * (j & 1));
+    } else if constexpr (F::NV == 2) {
+      f.v[j >> 2] |= (uint32_t)static_cast<const uint8_t*>(td.v)[e] << (8 * (j & 3));
+    } else if ((j & 1) == 0) {
+      uint32_t byte = static_cast<const uint8_t*>(td.v)[e >> 1];
+      if (j + 1 >= cnt) byte &= 0xFu;
+      f.v[0] |= byte << (4 * j);
+    }
+    if constexpr (ALGO == ALGO_ADEMAMIX) f.m2[j] = f2u(td.m2[e]);
+  }
 }
 
 template <int GT, int COMBO, int ALGO, bool SR>
-__device__ __forceinline__ uint32_t step_group(const TensorDesc& td, int64_t e0, int cnt,
-                                               float coef, const opt_step_scalars& sc,
-                                               uint32_t tensor, uint32_t seed_lo,
-                                               uint32_t seed_hi, uint32_t step32) {
-  constexpr int MD = Combo<COMBO>::M, VD = Combo<COMBO>::V;
+__device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e0, int cnt,
+                                                 const Frag<GT, COMBO, ALGO>& f, float coef,
+                                                 const opt_step_scalars& sc, uint32_t tensor,
+                                                 uint32_t seed_lo, uint32_t seed_hi, uint32_t step32) {
+  using F = Frag<GT, COMBO, ALGO>;
+  constexpr int MD = F::MD, VD = F::VD;
   constexpr bool LOWP = COMBO != SC_F32;
-  const bool full = cnt == 8;
+  constexpr int VBITS = VD == OPT_F32 ? 32 : VD == OPT_BF16 ? 16 : VD == OPT_E4M3 ? 8 : 4;
 
-  float p[8], g[8], m[8], v[8], m2[8];
-  uint32_t vold[8];
-
-  // ------------------------------------------------------------- loads
-  if (full) {
-    u4_to_f4(ld_cs_u4(td.p + e0), p);
-    u4_to_f4(ld_cs_u4(td.p + e0 + 4), p + 4);
-    if (GT == OPT_BF16) {
-      bf16x8_to_f(ld_nc_u4(static_cast<const uint16_t*>(td.g) + e0), g);
-    } else {
-      u4_to_f4(ld_nc_u4(static_cast<const float*>(td.g) + e0), g);
-      u4_to_f4(ld_nc_u4(static_cast<const float*>(td.g) + e0 + 4), g + 4);
-    }
-    if (MD == OPT_F32) {
-      u4_to_f4(ld_cs_u4(static_cast<float*>(td.m) + e0), m);
-      u4_to_f4(ld_cs_u4(static_cast<float*>(td.m) + e0 + 4), m + 4);
-    } else {
-      bf16x8_to_f(ld_cs_u4(static_cast<uint16_t*>(td.m) + e0), m);
-    }
-    if (VD == OPT_F32) {
-      const uint4 a = ld_cs_u4(static_cast<float*>(td.v) + e0);
-      const uint4 b = ld_cs_u4(static_cast<float*>(td.v) + e0 + 4);
-      vold[0] = a.x; vold[1] = a.y; vold[2] = a.z; vold[3] = a.w;
-      vold[4] = b.x; vold[5] = b.y; vold[6] = b.z; vold[7] = b.w;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = u2f(vold[j]);
-    } else if (VD == OPT_BF16) {
-      const uint4 w = ld_cs_u4(static_cast<uint16_t*>(td.v) + e0);
-      const uint32_t a[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) { vold[2 * k] = a[k] & 0xFFFFu; vold[2 * k + 1] = a[k] >> 16; }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = bf16_dec(vold[j]);
-    } else if (VD == OPT_E4M3) {
-      const uint2 w = ld_cs_u2(static_cast<uint8_t*>(td.v) + e0);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) { vold[j] = (w.x >> (8 * j)) & 0xFFu; vold[4 + j] = (w.y >> (8 * j)) & 0xFFu; }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = e4m3_dec(vold[j]);
-    } else {
-      const uint32_t w = ld_cs_u1(static_cast<uint8_t*>(td.v) + (e0 >> 1));
-#pragma unroll
-      for (int j = 0; j < 8; ++j) vold[j] = (w >> (4 * j)) & 0xFu;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = e2m2_dec(vold[j]);
-    }
-    if (ALGO == ALGO_ADEMAMIX) {
-      u4_to_f4(ld_cs_u4(td.m2 + e0), m2);
-      u4_to_f4(ld_cs_u4(td.m2 + e0 + 4), m2 + 4);
-    }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const bool in = j < cnt;
-      const int64_t e = e0 + j;
-      p[j] = in ? td.p[e] : 0.0f;
-      g[j] = !in ? 0.0f
-                 : (GT == OPT_BF16 ? bf16_dec(static_cast<const uint16_t*>(td.g)[e])
-                                   : static_cast<const float*>(td.g)[e]);
-      m[j] = !in ? 0.0f
-                 : (MD == OPT_F32 ? static_cast<const float*>(td.m)[e]
-                                  : bf16_dec(static_cast<const uint16_t*>(td.m)[e]));
-      uint32_t code = 0;
-      if (in) {
-        if (VD == OPT_F32) code = f2u(static_cast<const float*>(td.v)[e]);
-        else if (VD == OPT_BF16) code = static_cast<const uint16_t*>(td.v)[e];
-        else if (VD == OPT_E4M3) code = static_cast<const uint8_t*>(td.v)[e];
-        else code = (static_cast<const uint8_t*>(td.v)[e >> 1] >> (4 * (e & 1))) & 0xFu;
-      }
-      vold[j] = code;
-      v[j] = VD == OPT_F32 ? u2f(code)
-           : VD == OPT_BF16 ? bf16_dec(code)
-           : VD == OPT_E4M3 ? e4m3_dec(code) : e2m2_dec(code);
-      if (ALGO == ALGO_ADEMAMIX) m2[j] = in ? td.m2[e] : 0.0f;
-    }
-  }
-
-  // ------------------------------------------------------------- draws
   uint32_t words[8];
   if (LOWP && SR) {
     const uint4 d0 = draw_words((uint64_t)e0 >> 2, tensor, step32, seed_lo, seed_hi);
@@ -148,34 +165,39 @@ __device__ __forceinline__ uint32_t step_group(const TensorDesc& td, int64_t e0,
     words[4] = d1.x; words[5] = d1.y; words[6] = d1.z; words[7] = d1.w;
   }
 
-  // ----------------------------------------------------------- compute
-  uint32_t mcode[8], vcode[8];
+  float pn[8], mnv[8], vnv[8], m2n[8];
+  uint32_t mcode[8], vcode[8], vold[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const float ge = __fmul_rn(g[j], coef);
-    const float mn = __fadd_rn(__fmul_rn(sc.beta1, m[j]), __fmul_rn(sc.omb1, ge));
-    const float vn = __fadd_rn(__fmul_rn(sc.beta2, v[j]), __fmul_rn(sc.omb2, __fmul_rn(ge, ge)));
+    const float g = GT == OPT_BF16 ? bf16_dec(code_at<16>(f.g, j)) : u2f(f.g[j]);
+    const float m = MD == OPT_F32 ? u2f(f.m[j]) : bf16_dec(code_at<16>(f.m, j));
+    vold[j] = VBITS == 32 ? f.v[j] : code_at<VBITS>(f.v, j);
+    const float v = VD == OPT_F32 ? u2f(vold[j])
+                  : VD == OPT_BF16 ? bf16_dec(vold[j])
+                  : VD == OPT_E4M3 ? e4m3_dec(vold[j]) : e2m2_dec(vold[j]);
+    const float ge = __fmul_rn(g, coef);
+    const float mn = __fadd_rn(__fmul_rn(sc.beta1, m), __fmul_rn(sc.omb1, ge));
+    const float vn = __fadd_rn(__fmul_rn(sc.beta2, v), __fmul_rn(sc.omb2, __fmul_rn(ge, ge)));
     float num = __fmul_rn(mn, sc.inv_bc1);
     if (ALGO == ALGO_ADEMAMIX) {
-      const float m2n = __fadd_rn(__fmul_rn(sc.beta3, m2[j]), __fmul_rn(sc.omb3, ge));
-      num = __fadd_rn(num, __fmul_rn(sc.alpha, m2n));
-      m2[j] = m2n;
+      m2n[j] = __fadd_rn(__fmul_rn(sc.beta3, u2f(f.m2[j])), __fmul_rn(sc.omb3, ge));
+      num = __fadd_rn(num, __fmul_rn(sc.alpha, m2n[j]));
     }
     const float den = __fadd_rn(__fsqrt_rn(__fmul_rn(vn, sc.inv_bc2)), sc.eps);
     const float u = __fdiv_rn(num, den);
-    p[j] = __fsub_rn(__fmul_rn(p[j], sc.decay), __fmul_rn(sc.lr, u));
-    if (MD == OPT_F32) m[j] = mn;
-    else mcode[j] = bf16_enc<SR>(mn, SR ? (words[j] & 0xFFFFu) : 0u);
-    if (VD == OPT_F32) { v[j] = vn; vcode[j] = f2u(vn); }
+    pn[j] = __fsub_rn(__fmul_rn(u2f(f.p[j]), sc.decay), __fmul_rn(sc.lr, u));
+    mnv[j] = mn;
+    vnv[j] = vn;
+    if (MD == OPT_BF16) mcode[j] = bf16_enc<SR>(mn, SR ? (words[j] & 0xFFFFu) : 0u);
+    if (VD == OPT_F32) vcode[j] = f2u(vn);
     else if (VD == OPT_BF16) vcode[j] = bf16_enc<SR>(vn, SR ? (words[j] >> 16) : 0u);
     else if (VD == OPT_E2M2) vcode[j] = e2m2_enc<SR>(vn, SR ? (words[j] >> 16) : 0u);
     else if (SR) vcode[j] = e4m3_enc_sr(vn, words[j] >> 16);
-    else v[j] = vn;   // E4M3 nearest: converted in pairs below
   }
   if (VD == OPT_E4M3 && !SR) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint32_t pair = e4m3x2_rn(v[2 * k], v[2 * k + 1]);
+      const uint32_t pair = e4m3x2_rn(vnv[2 * k], vnv[2 * k + 1]);
       vcode[2 * k] = pair & 0xFFu;
       vcode[2 * k + 1] = pair >> 8;
     }
@@ -184,21 +206,21 @@ __device__ __forceinline__ uint32_t step_group(const TensorDesc& td, int64_t e0,
 #pragma unroll
   for (int j = 0; j < 8; ++j) same += (j < cnt && vcode[j] == vold[j]) ? 1u : 0u;
 
-  // ------------------------------------------------------------ stores
-  if (full) {
-    st_cs_u4(td.p + e0, f4_to_u4(p));
-    st_cs_u4(td.p + e0 + 4, f4_to_u4(p + 4));
+  if (cnt == 8) {
+    st_cs_u4(td.p + e0, make_uint4(f2u(pn[0]), f2u(pn[1]), f2u(pn[2]), f2u(pn[3])));
+    st_cs_u4(td.p + e0 + 4, make_uint4(f2u(pn[4]), f2u(pn[5]), f2u(pn[6]), f2u(pn[7])));
     if (MD == OPT_F32) {
-      st_cs_u4(static_cast<float*>(td.m) + e0, f4_to_u4(m));
-      st_cs_u4(static_cast<float*>(td.m) + e0 + 4, f4_to_u4(m + 4));
+      st_cs_u4(static_cast<float*>(td.m) + e0, make_uint4(f2u(mnv[0]), f2u(mnv[1]), f2u(mnv[2]), f2u(mnv[3])));
+      st_cs_u4(static_cast<float*>(td.m) + e0 + 4,
+               make_uint4(f2u(mnv[4]), f2u(mnv[5]), f2u(mnv[6]), f2u(mnv[7])));
     } else {
       st_cs_u4(static_cast<uint16_t*>(td.m) + e0,
                make_uint4(mcode[0] | (mcode[1] << 16), mcode[2] | (mcode[3] << 16),
                           mcode[4] | (mcode[5] << 16), mcode[6] | (mcode[7] << 16)));
     }
     if (VD == OPT_F32) {
-      st_cs_u4(static_cast<float*>(td.v) + e0, f4_to_u4(v));
-      st_cs_u4(static_cast<float*>(td.v) + e0 + 4, f4_to_u4(v + 4));
+      st_cs_u4(static_cast<float*>(td.v) + e0, make_uint4(vcode[0], vcode[1], vcode[2], vcode[3]));
+      st_cs_u4(static_cast<float*>(td.v) + e0 + 4, make_uint4(vcode[4], vcode[5], vcode[6], vcode[7]));
     } else if (VD == OPT_BF16) {
       st_cs_u4(static_cast<uint16_t*>(td.v) + e0,
                make_uint4(vcode[0] | (vcode[1] << 16), vcode[2] | (vcode[3] << 16),
@@ -214,21 +236,21 @@ __device__ __forceinline__ uint32_t step_group(const TensorDesc& td, int64_t e0,
       st_cs_u1(static_cast<uint8_t*>(td.v) + (e0 >> 1), w);
     }
     if (ALGO == ALGO_ADEMAMIX) {
-      st_cs_u4(td.m2 + e0, f4_to_u4(m2));
-      st_cs_u4(td.m2 + e0 + 4, f4_to_u4(m2 + 4));
+      st_cs_u4(td.m2 + e0, make_uint4(f2u(m2n[0]), f2u(m2n[1]), f2u(m2n[2]), f2u(m2n[3])));
+      st_cs_u4(td.m2 + e0 + 4, make_uint4(f2u(m2n[4]), f2u(m2n[5]), f2u(m2n[6]), f2u(m2n[7])));
     }
   } else {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       if (j >= cnt) break;
       const int64_t e = e0 + j;
-      td.p[e] = p[j];
-      if (MD == OPT_F32) static_cast<float*>(td.m)[e] = m[j];
+      td.p[e] = pn[j];
+      if (MD == OPT_F32) static_cast<float*>(td.m)[e] = mnv[j];
       else static_cast<uint16_t*>(td.m)[e] = (uint16_t)mcode[j];
-      if (VD == OPT_F32) static_cast<float*>(td.v)[e] = v[j];
+      if (VD == OPT_F32) static_cast<float*>(td.v)[e] = vnv[j];
       else if (VD == OPT_BF16) static_cast<uint16_t*>(td.v)[e] = (uint16_t)vcode[j];
       else if (VD == OPT_E4M3) static_cast<uint8_t*>(td.v)[e] = (uint8_t)vcode[j];
-      if (ALGO == ALGO_ADEMAMIX) td.m2[e] = m2[j];
+      if (ALGO == ALGO_ADEMAMIX) td.m2[e] = m2n[j];
     }
     if (VD == OPT_E2M2) {
       // whole bytes: e0 is even, so byte k holds elements 2k and 2k+1 of the
@@ -244,23 +266,75 @@ __device__ __forceinline__ uint32_t step_group(const TensorDesc& td, int64_t e0,
   return same;
 }
 
+// A thread's walk over its groups: chunk c of the bucket (c = begin +
+// blockIdx.x + k * gridDim.x), group start `base` within the chunk.
+struct Cursor {
+  int64_t c;
+  int base;
+  opt_chunk ch;
+};
+
+__device__ __forceinline__ bool cursor_settle(Cursor& k, const StepArgs& a) {
+  while (k.base >= (int)k.ch.len) {
+    k.c += gridDim.x;
+    if (k.c >= a.chunk_end) return false;
+    k.ch = a.chunks[k.c];
+    k.base = threadIdx.x * 8;
+  }
+  return true;
+}
+
 template <int GT, int COMBO, int ALGO, bool SR>
-__global__ void __launch_bounds__(kStepThreads)
+__global__ void __launch_bounds__(kStepThreads, kStepMinBlocks)
 step_kernel(const StepArgs a) {
   float coef = 1.0f;
   if (a.d_norm != nullptr) {
     if (a.d_norm->status != OPT_OK) return;     // non-finite norm: leave all untouched
     coef = a.d_norm->clip_coef;
   }
+  Cursor k;
+  k.c = a.chunk_begin + blockIdx.x;
+  if (k.c >= a.chunk_end) return;
+  k.ch = a.chunks[k.c];
+  k.base = threadIdx.x * 8;
+  bool have = cursor_settle(k, a);
+
+  Frag<GT, COMBO, ALGO> cur, nxt;
+  TensorDesc ctd;
+  int64_t ce0 = 0;
+  int ccnt = 0;
+  uint32_t ctensor = 0;
+  if (have) {
+    ctd = a.tensors[k.ch.tensor];
+    ctensor = k.ch.tensor;
+    ce0 = k.ch.start + k.base;
+    ccnt = min(8, (int)k.ch.len - k.base);
+    if (ccnt == 8) load_full(ctd, ce0, cur);
+    else load_partial(ctd, ce0, ccnt, cur);
+  }
   uint32_t same = 0;
-  for (int64_t c = a.chunk_begin + blockIdx.x; c < a.chunk_end; c += gridDim.x) {
-    const opt_chunk ch = a.chunks[c];
-    const TensorDesc td = a.tensors[ch.tensor];
-    const int len = (int)ch.len;
-    for (int base = threadIdx.x * 8; base < len; base += kStepThreads * 8) {
-      same += step_group<GT, COMBO, ALGO, SR>(td, ch.start + base, min(8, len - base), coef, a.sc,
-                                              ch.tensor, a.seed_lo, a.seed_hi, a.step32);
+  while (have) {
+    // request the next group before working on the current one
+    k.base += kStepThreads * 8;
+    const bool have_next = cursor_settle(k, a);
+    TensorDesc ntd;
+    int64_t ne0 = 0;
+    int ncnt = 0;
+    if (have_next) {
+      ntd = a.tensors[k.ch.tensor];
+      ne0 = k.ch.start + k.base;
+      ncnt = min(8, (int)k.ch.len - k.base);
+      if (ncnt == 8) load_full(ntd, ne0, nxt);
+      else load_partial(ntd, ne0, ncnt, nxt);
     }
+    same += update_store<GT, COMBO, ALGO, SR>(ctd, ce0, ccnt, cur, coef, a.sc, ctensor, a.seed_lo,
+                                              a.seed_hi, a.step32);
+    cur = nxt;
+    ctd = ntd;
+    ce0 = ne0;
+    ccnt = ncnt;
+    ctensor = k.ch.tensor;
+    have = have_next;
   }
   if (a.unchanged != nullptr) {
     // integer sums: the total does not depend on the order of the atomics
@@ -276,15 +350,15 @@ cudaError_t launch_one(const StepArgs& a, int sm_count, cudaStream_t s) {
   const int64_t n = a.chunk_end - a.chunk_begin;
   if (n <= 0) return cudaSuccess;
   auto k = step_kernel<GT, COMBO, ALGO, SR>;
-  static int cached_grid_per_sm = 0;
-  if (cached_grid_per_sm == 0) {
+  static int cached_per_sm = 0;
+  if (cached_per_sm == 0) {
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kStepThreads, 0) != cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
-    cached_grid_per_sm = per_sm;
+    cached_per_sm = per_sm;
   }
-  const int64_t full = (int64_t)cached_grid_per_sm * sm_count;
+  const int64_t full = (int64_t)cached_per_sm * sm_count;
   const int grid = (int)(n < full ? n : full);
   k<<<grid, kStepThreads, 0, s>>>(a);
   return cudaGetLastError();
