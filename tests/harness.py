@@ -53,25 +53,100 @@ class GpuSide:
 
 
 class OracleSide:
-    """Host copies of the sampled tensors, stepped by the oracle."""
+    """Host copies of sampled tensors or slices, stepped by the oracle.
 
-    def __init__(self, gpu: GpuSide, indices):
+    `samples` holds tensor indices (the whole tensor) or (index, start, n)
+    slices; start must be even (E2M2 packs two codes per byte).  Element k of
+    a slice is element start + k of its tensor, which selects its
+    stochastic-rounding draws."""
+
+    def __init__(self, gpu: GpuSide, samples):
         self.w = gpu.w
-        self.idx = list(indices)
-        self.p = [W.to_numpy_codes(gpu.params[i]) for i in self.idx]
-        self.m = [W.to_numpy_codes(gpu.m[i]) for i in self.idx]
-        self.v = [W.to_numpy_codes(gpu.v[i]) for i in self.idx]
-        self.m2 = ([W.to_numpy_codes(gpu.m2[i]) for i in self.idx] if gpu.m2 is not None else None)
+        self.samples = [(s, 0, gpu.w.sizes[s]) if isinstance(s, int) else tuple(s) for s in samples]
+        self.idx = [i for i, _, _ in self.samples]
+        self.p = [W.to_numpy_codes(self.cut(gpu.params, k, "f32")) for k in range(len(self.samples))]
+        self.m = [W.to_numpy_codes(self.cut(gpu.m, k, self.w.m_dtype)) for k in range(len(self.samples))]
+        self.v = [W.to_numpy_codes(self.cut(gpu.v, k, self.w.v_dtype)) for k in range(len(self.samples))]
+        self.m2 = ([W.to_numpy_codes(self.cut(gpu.m2, k, self.w.m_dtype)) for k in range(len(self.samples))]
+                   if gpu.m2 is not None else None)
+
+    def cut(self, tensors, k, dtype):
+        """The part of tensor list `tensors` that sample k covers."""
+        i, start, n = self.samples[k]
+        t = tensors[i]
+        if dtype == "e2m2":
+            assert start % 2 == 0
+            return t[start // 2:(start + n + 1) // 2]
+        return t[start:start + n]
+
+    def grads(self, gpu_grads):
+        return [W.to_numpy_codes(self.cut(gpu_grads, k, "grad")) for k in range(len(self.samples))]
 
     def step(self, t: int, grads_np, ohp, coef: float, stochastic: bool, seed: int):
-        """grads_np: host gradient arrays for the sampled tensors (same order)."""
+        """grads_np: host gradient arrays for the samples (same order)."""
         unchanged = 0
-        for k, i in enumerate(self.idx):
+        for k, (i, start, n) in enumerate(self.samples):
             unchanged += oracle.adam_tensor(
                 ALGO[self.w.algo], self.p[k], grads_np[k], self.m[k], self.v[k], ohp, t,
                 m2=None if self.m2 is None else self.m2[k], m_dtype=self.w.m_dtype,
-                v_dtype=self.w.v_dtype, coef=coef, stochastic=stochastic, seed=seed, tensor_index=i)
+                v_dtype=self.w.v_dtype, coef=coef, stochastic=stochastic, seed=seed, tensor_index=i,
+                index_base=start)
         return unchanged
+
+    def compare(self, gpu: GpuSide, tol: float, exact_codes: bool):
+        """FP32 values within tol (1+|x|); low-precision codes identical
+        (exact_codes) or >= 99.99 % identical and one step off."""
+        w = self.w
+        for k, (i, start, n) in enumerate(self.samples):
+            what = f"tensor {i} [{start}:{start + n}]"
+            assert_close_scaled(W.to_numpy_codes(self.cut(gpu.params, k, "f32")), self.p[k], tol, "p " + what)
+            gm = W.to_numpy_codes(self.cut(gpu.m, k, w.m_dtype))
+            gv = W.to_numpy_codes(self.cut(gpu.v, k, w.v_dtype))
+            if w.m_dtype == "f32":
+                assert_close_scaled(gm, self.m[k], tol, "m " + what)
+                assert_close_scaled(gv, self.v[k], tol, "v " + what)
+            else:
+                compare_codes(gm, self.m[k], "bf16", n, exact=exact_codes, what="m " + what)
+                compare_codes(gv, self.v[k], w.v_dtype, n, exact=exact_codes, what="v " + what)
+            if self.m2 is not None:
+                assert_close_scaled(W.to_numpy_codes(self.cut(gpu.m2, k, w.m_dtype)), self.m2[k], tol,
+                                    "m2 " + what)
+
+
+def run_lockstep(w, steps, tol, samples=None, rounding="nearest", seed=0, hp_seed=77, count=False,
+                 checkpoints=(), norm_threads=16, gpu=None):
+    """Run `steps` steps of workload `w` on the GPU (whole list, clip from the
+    GPU's own norm when w.max_norm > 0) and on the oracle (its own norm over
+    every gradient, the step on `samples`), comparing the norms every step and
+    the sampled states at each checkpoint and at the end."""
+    gpu = gpu or GpuSide(w, seed=seed)
+    orc = OracleSide(gpu, range(len(w.sizes)) if samples is None else samples)
+    ghp, ohp = hp_for(w, rounding=rounding, seed=hp_seed, count=count)
+    sr = rounding == "stochastic"
+    clip = w.max_norm > 0
+    counts = []
+    for t in range(1, steps + 1):
+        W.fill_grads(w, gpu.grads, t, seed)
+        coef = 1.0
+        if clip:
+            all_np = [W.to_numpy_codes(g) for g in gpu.grads]
+            want = oracle_norm_parallel(all_np, w.max_norm, norm_threads)
+            got = gpu.plan.grad_norm(w.max_norm)
+            assert rel_err(got.norm2, want["norm2"]) <= 1e-12, (t, got.norm2, want["norm2"])
+            assert got.clip_coef == want["clip_coef"], t
+            coef = want["clip_coef"]
+            del all_np
+        g_np = orc.grads(gpu.grads)
+        gpu.step(t, ghp, clip)
+        same = orc.step(t, g_np, ohp, coef, sr, hp_seed)
+        if count:
+            counts.append((gpu.plan.unchanged_count(), same))
+        if t in checkpoints:
+            torch.cuda.synchronize()
+            orc.compare(gpu, tol, sr)
+    torch.cuda.synchronize()
+    orc.compare(gpu, tol, sr)
+    return gpu, orc, counts
 
 
 def oracle_norm_parallel(grads_np, max_norm: float, threads: int = 16) -> dict:

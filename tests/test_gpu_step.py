@@ -10,46 +10,20 @@ import torch
 import oracle
 import precision_states_gb300 as ps
 import workloads as W
-from harness import (GpuSide, OracleSide, assert_close_scaled, compare_codes, decode, hp_for)
+from harness import GpuSide, hp_for, run_lockstep
 
 pytestmark = pytest.mark.gpu
 
 
 def run_parity(w, steps, tol, rounding="nearest", clip=True, seed=0, count=False, check_every=None):
-    gpu = GpuSide(w, seed=seed)
-    orc = OracleSide(gpu, range(len(w.sizes)))
-    ghp, ohp = hp_for(w, rounding=rounding, seed=77, count=count)
-    sr = rounding == "stochastic"
-    for t in range(1, steps + 1):
-        W.fill_grads(w, gpu.grads, t, seed)
-        g_np = [W.to_numpy_codes(g) for g in gpu.grads]
-        coef = 1.0
-        if clip and w.max_norm > 0:
-            coef = oracle.grad_norm(g_np, w.max_norm)["clip_coef"]
-        gpu.step(t, ghp, clip and w.max_norm > 0)
-        same = orc.step(t, g_np, ohp, coef, sr, 77)
-        if count:
-            assert gpu.plan.unchanged_count() == same
-        if check_every and t % check_every == 0:
-            compare(gpu, orc, w, tol, sr)
-    torch.cuda.synchronize()
-    compare(gpu, orc, w, tol, sr)
+    if not clip:
+        w.max_norm = 0.0
+    checkpoints = range(check_every, steps + 1, check_every) if check_every else ()
+    gpu, orc, counts = run_lockstep(w, steps, tol, rounding=rounding, seed=seed, count=count,
+                                    checkpoints=checkpoints)
+    for got, want in counts:
+        assert got == want
     return gpu, orc
-
-
-def compare(gpu, orc, w, tol, sr):
-    for k, i in enumerate(orc.idx):
-        n = w.sizes[i]
-        assert_close_scaled(W.to_numpy_codes(gpu.params[i]), orc.p[k], tol, f"p[{i}]")
-        gm, gv = W.to_numpy_codes(gpu.m[i]), W.to_numpy_codes(gpu.v[i])
-        if w.m_dtype == "f32":
-            assert_close_scaled(gm, orc.m[k], tol, f"m[{i}]")
-            assert_close_scaled(gv, orc.v[k], tol, f"v[{i}]")
-        else:
-            compare_codes(gm, orc.m[k], "bf16", n, exact=sr, what=f"m[{i}]")
-            compare_codes(gv, orc.v[k], w.v_dtype, n, exact=sr, what=f"v[{i}]")
-        if orc.m2 is not None:
-            assert_close_scaled(W.to_numpy_codes(gpu.m2[i]), orc.m2[k], tol, f"m2[{i}]")
 
 
 @pytest.mark.parametrize("algo", ["adamw", "ademamix"])
