@@ -31,9 +31,16 @@ sys.path.insert(0, ROOT)
 
 METRIC = "optimizer-step Gparams/s and HBM GB/s (% of ~8 TB/s peak), 1×GB300"
 UNIT = "Gparams/s"
-# algorithmic bytes per parameter: step = p r+w (8) + g r (2) + m r+w (8) + v r+w (8)
-STEP_BYTES_PER_PARAM = {"bf16": 26, "f32": 28}
-NORM_BYTES_PER_PARAM = {"bf16": 2, "f32": 4}
+ELEM_BYTES = {"f32": 4, "bf16": 2, "e4m3": 1, "e2m2": 0.5}
+
+
+def step_bytes_per_param(w) -> float:
+    """Algorithmic bytes per parameter of one fused step: p read + write,
+    g read, m (and m2) read + write, v read + write."""
+    b = 8 + ELEM_BYTES[w.grad_dtype] + 2 * ELEM_BYTES[w.m_dtype] + 2 * ELEM_BYTES[w.v_dtype]
+    if w.algo == "ademamix":
+        b += 2 * ELEM_BYTES[w.m_dtype]
+    return b
 
 
 def parse():
@@ -43,6 +50,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama3_8b")
+    ap.add_argument("--v-dtype", default=None, choices=["f32", "bf16", "e4m3", "e2m2"],
+                    help="override the state dtypes: f32 = f32 m and v; otherwise bf16 m and this v")
+    ap.add_argument("--rounding", default="nearest", choices=["nearest", "stochastic"])
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -131,49 +141,76 @@ def traffic_for(kernel_key: str, params: int):
 
 
 # ----------------------------------------------------------- cpu baseline
-def cpu_baseline(w, seconds: float):
-    """Time the CPU oracle (as it stands, single-threaded) on a bounded sample
-    of the workload: norm + AdamW step over a growing prefix of the list's
-    sampled tensors until about `seconds` of CPU time."""
-    import numpy as np
-    import torch
+class OracleSample:
+    """A bounded, deterministic sample of the workload for the CPU oracle:
+    tensors in list order (the embedding and head last), as many as fit a
+    budget of about `seconds` of single-threaded oracle time per step."""
 
-    import oracle
-    import workloads as W
+    def __init__(self, w, seconds: float, stochastic: bool = False):
+        import numpy as np
 
-    order = sorted(range(len(w.sizes)), key=lambda i: (w.sizes[i] > 50_000_000, i))
-    # deterministic sample: tensors in list order, skipping the embedding and
-    # head, cut to a budget measured on a first small tensor
-    ohp = oracle.hparams(**{k: v for k, v in {**dict(beta1=0.9, beta2=0.999), **w.hp}.items()})
-    probe = order[1]
-    n_probe = min(w.sizes[probe], 2_000_000)
-    p = np.zeros(n_probe, np.float32)
-    g = W.make_grads(W.Workload("probe", [n_probe], w.grad_dtype), "cpu", 1, 0)[0]
-    g = W.to_numpy_codes(g)
-    t0 = time.perf_counter()
-    oracle.grad_norm([g], w.max_norm)
-    oracle.adam_tensor(oracle.ADAMW, p, g, np.zeros(n_probe, np.float32), np.zeros(n_probe, np.float32),
-                       ohp, 1)
-    per_elem = (time.perf_counter() - t0) / n_probe
-    budget = int(seconds / max(per_elem, 1e-10))
-    idx, total = [], 0
-    for i in order:
-        if total + w.sizes[i] > budget and idx:
-            break
-        idx.append(i)
-        total += w.sizes[i]
-    grads = [W.to_numpy_codes(t) for t in W.make_grads(w, "cpu", 1, 0, idx)]
-    params = [W.to_numpy_codes(t) for t in W.make_params(w, "cpu", 0, idx)]
-    ms = [np.zeros(w.sizes[i], np.float32) for i in idx]
-    vs = [np.zeros(w.sizes[i], np.float32) for i in idx]
-    t0 = time.perf_counter()
-    r = oracle.grad_norm(grads, w.max_norm)
-    for k in range(len(idx)):
-        oracle.adam_tensor(oracle.ADAMW, params[k], grads[k], ms[k], vs[k], ohp, 1, coef=r["clip_coef"])
-    dt = time.perf_counter() - t0
-    return {"value": total / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{len(idx)} of {len(w.sizes)} tensors ({total:,} params, {total / w.numel:.2%} of the "
-                      f"list): norm + one AdamW step, single-threaded C oracle, {dt:.1f} s"}
+        import oracle
+        import workloads as W
+
+        self.w = w
+        self.ohp = oracle.hparams(**{**dict(beta1=0.9, beta2=0.999), **w.hp})
+        order = sorted(range(len(w.sizes)), key=lambda i: (w.sizes[i] > 50_000_000, i))
+        # calibrate: oracle time per element on a probe tensor
+        n_probe = min(2_000_000, max(w.sizes))
+        pw = W.Workload("probe", [n_probe], w.grad_dtype)
+        g = W.to_numpy_codes(W.make_grads(pw, "cpu", 1, 0)[0])
+        p = np.zeros(n_probe, np.float32)
+        t0 = time.perf_counter()
+        oracle.grad_norm([g], w.max_norm)
+        oracle.adam_tensor(oracle.ADAMW, p, g, np.zeros(n_probe, np.float32), np.zeros(n_probe, np.float32),
+                           self.ohp, 1)
+        per_elem = (time.perf_counter() - t0) / n_probe
+        budget = max(1, int(seconds / max(per_elem, 1e-10)))
+        self.idx, total = [], 0
+        for i in order:
+            if total + w.sizes[i] > budget and self.idx:
+                break
+            self.idx.append(i)
+            total += w.sizes[i]
+        self.numel = total
+        self.grads = [W.to_numpy_codes(t) for t in W.make_grads(w, "cpu", 1, 0, self.idx)]
+        self.params = [W.to_numpy_codes(t) for t in W.make_params(w, "cpu", 0, self.idx)]
+        self.m = [W.to_numpy_codes(W.state_storage(w.m_dtype, w.sizes[i], "cpu")) for i in self.idx]
+        self.v = [W.to_numpy_codes(W.state_storage(w.v_dtype, w.sizes[i], "cpu")) for i in self.idx]
+        self.m2 = ([W.to_numpy_codes(W.state_storage(w.m_dtype, w.sizes[i], "cpu")) for i in self.idx]
+                   if w.algo == "ademamix" else None)
+        self.stochastic = stochastic
+        self.t = 0
+
+    def step(self) -> float:
+        """One oracle step over the sample (norm + update); returns seconds."""
+        import oracle
+        self.t += 1
+        algo = oracle.ADEMAMIX if self.w.algo == "ademamix" else oracle.ADAMW
+        t0 = time.perf_counter()
+        coef = 1.0
+        if self.w.max_norm > 0:
+            coef = oracle.grad_norm(self.grads, self.w.max_norm)["clip_coef"]
+        for k in range(len(self.idx)):
+            oracle.adam_tensor(algo, self.params[k], self.grads[k], self.m[k], self.v[k], self.ohp, self.t,
+                               m2=None if self.m2 is None else self.m2[k], m_dtype=self.w.m_dtype,
+                               v_dtype=self.w.v_dtype, coef=coef, stochastic=self.stochastic, seed=1234,
+                               tensor_index=self.idx[k])
+        return time.perf_counter() - t0
+
+    def describe(self, dt: float) -> str:
+        return (f"{len(self.idx)} of {len(self.w.sizes)} tensors ({self.numel:,} params, "
+                f"{self.numel / self.w.numel:.2%} of the list): norm + one step per timed step, "
+                f"single-threaded C oracle, {dt:.2f} s per step")
+
+
+def cpu_baseline(w, seconds: float, stochastic: bool = False):
+    """The CPU oracle as it stands, timed on the machine's host cores (one
+    thread) over a bounded sample of the same workload."""
+    smp = OracleSample(w, seconds, stochastic)
+    dt = smp.step()
+    return {"value": smp.numel / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": smp.describe(dt)}
 
 
 # ---------------------------------------------------------------- our arm
@@ -192,13 +229,15 @@ def run_ours(args, rank, local_rank, world):
         pg = dist
 
     w = W.workload(args.workload)
+    if args.v_dtype:
+        w.m_dtype, w.v_dtype = ("f32", "f32") if args.v_dtype == "f32" else ("bf16", args.v_dtype)
     params = W.make_params(w, dev, seed=rank)
     grads = W.make_grads(w, dev, step=1, seed=rank)
     m = [W.state_storage(w.m_dtype, n, dev) for n in w.sizes]
     v = [W.state_storage(w.v_dtype, n, dev) for n in w.sizes]
     m2 = [W.state_storage(w.m_dtype, n, dev) for n in w.sizes] if w.algo == "ademamix" else None
     plan = ps.Plan(params, grads, m, v, m2, m_dtype=w.m_dtype, v_dtype=w.v_dtype)
-    hp = ps.hparams(**{**dict(beta1=0.9, beta2=0.999), **w.hp})
+    hp = ps.hparams(rounding=args.rounding, seed=1234, **{**dict(beta1=0.9, beta2=0.999), **w.hp})
     stream = torch.cuda.current_stream(dev)
     clip = w.max_norm > 0
     d_norm = plan.norm_buffer() if clip else None
@@ -281,27 +320,29 @@ def run_ours(args, rank, local_rank, world):
         del host
 
     peak, peak_src = measured_peak()
-    step_bytes = STEP_BYTES_PER_PARAM[w.grad_dtype] * params_per_step
-    norm_bytes = NORM_BYTES_PER_PARAM[w.grad_dtype] * params_per_step
+    bpp = step_bytes_per_param(w)
+    step_bytes = int(bpp * params_per_step)
+    norm_bytes = int(ELEM_BYTES[w.grad_dtype] * params_per_step) if clip else 0
     step_avg = sum(step_ms) / len(step_ms)
     norm_avg = sum(norm_ms) / len(norm_ms)
     achieved = step_bytes / (step_avg / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": "step_kernel<bf16 grads, f32 states, AdamW>",
+    kname = f"step_kernel<{w.grad_dtype} grads, {w.m_dtype} m, {w.v_dtype} v, {w.algo}, {args.rounding}>"
+    roofline = {"bound": "hbm", "kernel": kname,
                 "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic_for("adamw_step_f32_bf16grad",
-                                                                          params_per_step),
+                "frac": round(achieved / peak, 4), "traffic": traffic_for(kname, params_per_step),
                 "peak_source": peak_src, "bytes_per_launch": step_bytes,
-                "bytes_per_param": STEP_BYTES_PER_PARAM[w.grad_dtype], "ms_per_launch": round(step_avg, 4),
-                "norm": {"achieved": round(norm_bytes / (norm_avg / 1e3) / 1e9, 1), "ms_per_launch_pair":
-                         round(norm_avg, 4), "bytes_per_launch": norm_bytes,
-                         "frac": round(norm_bytes / (norm_avg / 1e3) / 1e9 / peak, 4)}}
+                "bytes_per_param": bpp, "ms_per_launch": round(step_avg, 4)}
+    if clip:
+        roofline["norm"] = {"achieved": round(norm_bytes / (norm_avg / 1e3) / 1e9, 1),
+                            "ms_per_launch_pair": round(norm_avg, 4), "bytes_per_launch": norm_bytes,
+                            "frac": round(norm_bytes / (norm_avg / 1e3) / 1e9 / peak, 4)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         del params, grads, m, v, m2
         plan.close()
         torch.cuda.empty_cache()
-        cpu = cpu_baseline(w, args.cpu_sample_seconds)
+        cpu = cpu_baseline(w, args.cpu_sample_seconds, args.rounding == "stochastic")
 
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
@@ -309,6 +350,7 @@ def run_ours(args, rank, local_rank, world):
             "data": "synthetic",
             "config": {"workload": w.name, "tensors": len(w.sizes), "params_per_gpu": params_per_step,
                        "grad_dtype": w.grad_dtype, "m_dtype": w.m_dtype, "v_dtype": w.v_dtype,
+                       "rounding": args.rounding, "algo": w.algo,
                        "clip_max_norm": w.max_norm, "parallelism": f"replicas{world}",
                        "l2": "inputs larger than L2 (%.0f GB streamed per step)" % ((step_bytes + norm_bytes) / 1e9)},
             "hbm_gbs": round((step_bytes + norm_bytes) / (total_ms / args.steps / 1e3) / 1e9, 1),
@@ -323,27 +365,31 @@ def run_ours(args, rank, local_rank, world):
 
 # ---------------------------------------------------------- reference arm
 def run_reference(args, rank, world):
-    """The CPU oracle as the reference arm: each step is a bounded sample of
-    the workload (norm + AdamW step over the sampled tensors)."""
+    """The CPU oracle as the reference arm: each step is the oracle's norm +
+    step over a bounded sample of the workload (rank 0 only)."""
     if rank != 0:
         return
     import workloads as W
     w = W.workload(args.workload)
-    per_step = max(1.0, min(6.0, 90.0 / max(1, args.steps + args.warmup)))
-    vals = []
-    cb = None
-    for k in range(args.warmup + args.steps):
-        cb = cpu_baseline(w, per_step)
-        if k >= args.warmup:
-            vals.append(cb["value"])
-    value = statistics.median(vals)
-    cb["value"] = value
+    if args.v_dtype:
+        w.m_dtype, w.v_dtype = ("f32", "f32") if args.v_dtype == "f32" else ("bf16", args.v_dtype)
+    per_step = max(0.5, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
+    smp = OracleSample(w, per_step, args.rounding == "stochastic")
+    for _ in range(args.warmup):
+        smp.step()
+    times = [smp.step() for _ in range(args.steps)]
+    total = sum(times)
+    value = smp.numel * args.steps / total / 1e9
+    cb = {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+          "sample": smp.describe(total / args.steps)}
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
             "config": {"workload": w.name, "tensors": len(w.sizes), "params_per_gpu": w.numel,
                        "grad_dtype": w.grad_dtype, "m_dtype": w.m_dtype, "v_dtype": w.v_dtype,
-                       "clip_max_norm": w.max_norm, "parallelism": "replicas1"},
+                       "clip_max_norm": w.max_norm, "parallelism": "replicas1",
+                       "sampled_params_per_step": smp.numel},
             "cpu_baseline": cb,
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

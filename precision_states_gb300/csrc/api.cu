@@ -19,17 +19,20 @@ struct opt_plan {
   int32_t n = 0;
   int64_t total_numel = 0;
   int64_t n_chunks = 0;
-  int64_t bucket_begin[3] = {0, 0, 0};
+  int64_t bucket_begin[3] = {0, 0, 0};       // norm chunks per gradient-dtype bucket
+  int64_t n_tiles = 0;
+  int64_t tile_begin[3] = {0, 0, 0};         // step tiles per bucket
   int32_t m_dtype = OPT_F32, v_dtype = OPT_F32;
   int combo = SC_F32;
   bool has_m2 = false;
   std::vector<void*> grad_dev;          // per tensor, for opt_grads_upload
   std::vector<int64_t> grad_bytes;
-  // one device allocation: tensors | chunks | slots | result | counter
+  // one device allocation: tensors | chunks | tiles | slots | result | counter
   void* d_mem = nullptr;
   int64_t d_bytes = 0;
   TensorDesc* d_tensors = nullptr;
   opt_chunk* d_chunks = nullptr;
+  opt_chunk* d_tiles = nullptr;
   NormSlot* d_slots = nullptr;
   opt_norm_result* d_result = nullptr;
   unsigned long long* d_unchanged = nullptr;
@@ -129,6 +132,10 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
   std::vector<opt_chunk> chunks((size_t)nch);
   opt_chunk_table(L->n, L->numel, L->grad_dtype, chunks.data(), nch, P->bucket_begin);
   P->n_chunks = nch;
+  const int64_t ntl = build_table(L->n, L->numel, L->grad_dtype, kTileElems, nullptr, 0, P->tile_begin);
+  std::vector<opt_chunk> tiles((size_t)ntl);
+  build_table(L->n, L->numel, L->grad_dtype, kTileElems, tiles.data(), ntl, P->tile_begin);
+  P->n_tiles = ntl;
 
   std::vector<TensorDesc> tds((size_t)L->n);
   P->grad_dev.resize((size_t)L->n);
@@ -154,7 +161,8 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
 
   const int64_t off_t = 0;
   const int64_t off_c = align_up(off_t + (int64_t)sizeof(TensorDesc) * L->n, 256);
-  const int64_t off_s = align_up(off_c + (int64_t)sizeof(opt_chunk) * nch, 256);
+  const int64_t off_l = align_up(off_c + (int64_t)sizeof(opt_chunk) * nch, 256);
+  const int64_t off_s = align_up(off_l + (int64_t)sizeof(opt_chunk) * ntl, 256);
   const int64_t off_r = align_up(off_s + (int64_t)sizeof(NormSlot) * 2 * OPT_NORM_SLOTS, 256);
   const int64_t off_u = align_up(off_r + (int64_t)sizeof(opt_norm_result), 256);
   P->d_bytes = align_up(off_u + 8, 256);
@@ -163,6 +171,7 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
   char* base = static_cast<char*>(P->d_mem);
   P->d_tensors = reinterpret_cast<TensorDesc*>(base + off_t);
   P->d_chunks = reinterpret_cast<opt_chunk*>(base + off_c);
+  P->d_tiles = reinterpret_cast<opt_chunk*>(base + off_l);
   P->d_slots = reinterpret_cast<NormSlot*>(base + off_s);
   P->d_result = reinterpret_cast<opt_norm_result*>(base + off_r);
   P->d_unchanged = reinterpret_cast<unsigned long long*>(base + off_u);
@@ -172,6 +181,8 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
     e = cudaMemcpy(P->d_tensors, tds.data(), sizeof(TensorDesc) * (size_t)L->n, cudaMemcpyHostToDevice);
   if (e == cudaSuccess && nch > 0)
     e = cudaMemcpy(P->d_chunks, chunks.data(), sizeof(opt_chunk) * (size_t)nch, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && ntl > 0)
+    e = cudaMemcpy(P->d_tiles, tiles.data(), sizeof(opt_chunk) * (size_t)ntl, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) {
     cudaFree(P->d_mem);
     delete P;
@@ -252,7 +263,7 @@ static int do_step(opt_plan* P, const opt_hparams* hp, int64_t step, const opt_n
   int st = opt_step_scalars_compute(hp, step, &a.sc);
   if (st != OPT_OK) return st;
   a.tensors = P->d_tensors;
-  a.chunks = P->d_chunks;
+  a.tiles = P->d_tiles;
   a.seed_lo = (uint32_t)hp->seed;
   a.seed_hi = (uint32_t)(hp->seed >> 32);
   a.step32 = (uint32_t)step;
@@ -264,9 +275,9 @@ static int do_step(opt_plan* P, const opt_hparams* hp, int64_t step, const opt_n
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
-    a.chunk_begin = P->bucket_begin[b];
-    a.chunk_end = P->bucket_begin[b + 1];
-    if (a.chunk_end <= a.chunk_begin) continue;
+    a.tile_begin = P->tile_begin[b];
+    a.tile_end = P->tile_begin[b + 1];
+    if (a.tile_end <= a.tile_begin) continue;
     const int dt = b == 0 ? OPT_F32 : OPT_BF16;
     if (P->combo == SC_F32) e = launch_step_fp32_states(dt, algo, a, P->sm_count, s);
     else e = launch_step_lowp_states(dt, P->combo, hp->rounding == OPT_ROUND_STOCHASTIC, a,

@@ -37,8 +37,8 @@ static_assert(sizeof(NormSlot) == 32, "NormSlot layout");
 // Everything a step kernel needs besides the tables.
 struct StepArgs {
   const TensorDesc* tensors;
-  const opt_chunk* chunks;
-  int64_t chunk_begin, chunk_end;     // this bucket's range of the chunk table
+  const opt_chunk* tiles;             // the step's work table (kTileElems per entry)
+  int64_t tile_begin, tile_end;       // this bucket's range of it
   opt_step_scalars sc;
   uint32_t seed_lo, seed_hi, step32;
   const opt_norm_result* d_norm;      // NULL: no clipping
@@ -100,46 +100,45 @@ __device__ __forceinline__ uint32_t bf16_enc(float x, uint32_t r16) {
 }
 
 // ------------------------------------------------- small-grid rounding core
-// Rounds a >= 0 onto a grid with P fraction bits whose binades start at
-// 2^EMIN (spacing 2^(EMIN-P) below it), saturating at vmax.  With
-// ulp = 2^(e-P), t = a/ulp, k = floor(t): stochastic rounding takes k+1 iff
-// the first 16 fraction bits of t plus the draw carry past 2^16; nearest
-// takes k+1 iff frac(t) > 1/2, or = 1/2 with k odd.  Every operation below is
-// exact (power-of-two scalings, floor, and the subtraction of the floor).
+// Code of a >= 0 (finite, below the grid's largest value) on a grid with P
+// fraction bits whose binades start at 2^EMIN (spacing 2^(EMIN-P) below
+// it).  With e = max(floor(log2 a), EMIN), t = a / 2^(e-P) lies in
+// [0, 2^(P+1)) and is exact (a power-of-two scaling); the code is
+// (e - EMIN) 2^P + r, where r is t rounded to an integer:
+//  * nearest: ties to even, by adding 2^23 in round-to-nearest (the sum's
+//    last bit is the units place, so the hardware rounding is the rounding
+//    we want, exactly);
+//  * stochastic: r = floor(t + r16 / 2^16), which takes the upper neighbour
+//    exactly when the first 16 fraction bits of t plus the draw carry past
+//    2^16 ("When Small Updates Disappear", sec. 6.1, applied at the target
+//    grid's spacing).  1 + r16/2^16 is built from bits; both additions round
+//    toward zero, which cannot move the sum across an integer, so the floor is
+//    exact.
+// A carry to 2^(P+1) lands on the next binade's first code, as it should.
 template <int P, int EMIN, bool SR>
-__device__ __forceinline__ float grid_round(float a, uint32_t r16, float vmax) {
-  if (a >= vmax) return vmax;
-  const int eb = (int)(f2u(a) >> 23);               // a >= 0: biased exponent
-  const int e = max(eb - 127, EMIN);
-  const float ulp = u2f((uint32_t)(e - P + 127) << 23);
-  const float inv_ulp = u2f((uint32_t)(P - e + 127) << 23);
-  const float t = __fmul_rn(a, inv_ulp);
-  const float k = floorf(t);
-  const float f = __fsub_rn(t, k);
-  uint32_t up;
+__device__ __forceinline__ uint32_t grid_code(float a, uint32_t r16) {
+  const int e = max((int)(f2u(a) >> 23) - 127, EMIN);
+  const float t = __fmul_rn(a, u2f((uint32_t)(P - e + 127) << 23));
+  uint32_t r;
   if (SR) {
-    const uint32_t l16 = __float2uint_rz(__fmul_rn(f, 65536.0f));
-    up = (l16 + r16) >> 16;
+    const float s = __fadd_rz(t, u2f(0x3F800000u | (r16 << 7)));   // t + 1 + r16 / 2^16
+    r = f2u(__fadd_rz(s, 8388608.0f)) - 0x4B000001u;                // floor(s) - 1
   } else {
-    up = (f > 0.5f || (f == 0.5f && (__float2uint_rz(k) & 1u))) ? 1u : 0u;
+    r = f2u(__fadd_rn(t, 8388608.0f)) - 0x4B000000u;                // nearest integer
   }
-  return fminf(__fmul_rn(__fadd_rn(k, (float)up), ulp), vmax);
+  return (uint32_t)(e - EMIN) * (1u << P) + r;
 }
 
 // ------------------------------------------------------- E4M3 (FP8) codec
+// Decode: as if normal with exponent field max(E, 1), minus 2^-6 for the
+// subnormal codes (E = 0), which gives k 2^-9 exactly.
 __device__ __forceinline__ float e4m3_dec(uint32_t c) {
   const uint32_t mag = c & 0x7Fu;
-  float r = (mag < 8u) ? __fmul_rn((float)mag, 0.001953125f)          // k * 2^-9
-                       : u2f((mag << 20) + (120u << 23));             // (1+k/8) 2^(e-7)
+  const uint32_t E = mag >> 3;
+  float r = u2f(((max(E, 1u) + 120u) << 23) | ((mag & 7u) << 20));
+  if (E == 0u) r = __fsub_rn(r, 0.015625f);
   if (mag == 0x7Fu) r = u2f(0x7FC00000u);
   return (c & 0x80u) ? -r : r;
-}
-
-// code of a magnitude that lies exactly on the E4M3 grid, 0 <= q <= 448
-__device__ __forceinline__ uint32_t e4m3_code_exact(float q) {
-  if (q < 0.015625f) return __float2uint_rz(__fmul_rn(q, 512.0f));   // 0..8
-  const uint32_t b = f2u(q);
-  return (((b >> 23) - 120u) << 3) | ((b >> 20) & 7u);
 }
 
 // Nearest (saturating) conversion of two values by the hardware converter:
@@ -150,29 +149,46 @@ __device__ __forceinline__ uint32_t e4m3x2_rn(float lo, float hi) {
   return (uint32_t)r;
 }
 
+// Stochastic: sign kept, magnitudes at or above 448 saturate, NaN stays NaN.
 __device__ __forceinline__ uint32_t e4m3_enc_sr(float x, uint32_t r16) {
   if (x != x) return 0x7Fu;
   const uint32_t sign = (f2u(x) >> 24) & 0x80u;
-  return sign | e4m3_code_exact(grid_round<3, -6, true>(fabsf(x), r16, 448.0f));
+  const float a = fabsf(x);
+  if (a >= 448.0f) return sign | 0x7Eu;
+  return sign | grid_code<3, -6, true>(a, r16);
 }
 
 // ------------------------------------------------ unsigned E2M2 (FP4) codec
+// Decode: codes 0-3 are k/4 = (1 + k/4) - 1; codes 4-15 are normal.
 __device__ __forceinline__ float e2m2_dec(uint32_t c) {
-  return (c < 4u) ? __fmul_rn((float)c, 0.25f)
-                  : u2f((((c >> 2) + 126u) << 23) | ((c & 3u) << 21));
+  const uint32_t E = c >> 2;
+  const float r = u2f(((max(E, 1u) + 126u) << 23) | ((c & 3u) << 21));
+  return E == 0u ? __fsub_rn(r, 1.0f) : r;
 }
 
-__device__ __forceinline__ uint32_t e2m2_code_exact(float q) {   // 0 <= q <= 7 on grid
-  if (q < 1.0f) return __float2uint_rz(__fmul_rn(q, 4.0f));      // 0..4
-  const uint32_t b = f2u(q);
-  return (((b >> 23) - 126u) << 2) | ((b >> 21) & 3u);
-}
-
+// Negative values store 0, NaN stores 7 (the largest code), values at or
+// above 7 saturate.
 template <bool SR>
 __device__ __forceinline__ uint32_t e2m2_enc(float x, uint32_t r16) {
   if (x != x) return 15u;
   if (!(x > 0.0f)) return 0u;
-  return e2m2_code_exact(grid_round<2, 0, SR>(x, r16, 7.0f));
+  if (x >= 7.0f) return 15u;
+  return grid_code<2, 0, SR>(x, r16);
+}
+
+// ------------------------------------------ arithmetic for the update term
+// The parameter update is not a stored code, so it may use the hardware
+// approximations (relative error about 2^-22, far inside the tolerance the
+// update is checked to); the moments, which are, use exact fp32 operations.
+__device__ __forceinline__ float sqrt_approx(float x) {
+  float r;
+  asm("sqrt.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float div_full(float a, float b) {
+  float r;
+  asm("div.full.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
 }
 
 // -------------------------------------------------- streaming memory access

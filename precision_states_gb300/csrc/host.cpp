@@ -25,11 +25,16 @@ const char* opt_strerror(int status) {
   }
 }
 
-// Chunk table from sizes and gradient dtypes only ("perf(training): fused
-// multi-tensor gradient-norm reduction", 'Correctness properties': host-side
-// decomposition from sizes, no atomics; 'What': one launch per dtype bucket).
-int64_t opt_chunk_table(int32_t n, const int64_t* numel, const int32_t* grad_dtype,
-                        opt_chunk* out, int64_t cap, int64_t bucket_begin[3]) {
+}  // extern "C"
+
+namespace psopt {
+// A table of pieces of at most `elems` elements, from sizes and gradient
+// dtypes only ("perf(training): fused multi-tensor gradient-norm reduction",
+// 'Correctness properties': host-side decomposition from sizes, no atomics;
+// 'What': one launch per dtype bucket).  FP32-gradient tensors first, then
+// BF16; list order within a bucket; element order within a tensor.
+int64_t build_table(int32_t n, const int64_t* numel, const int32_t* grad_dtype, int64_t elems,
+                    opt_chunk* out, int64_t cap, int64_t bucket_begin[3]) {
   if (n < 0 || (n > 0 && (numel == nullptr || grad_dtype == nullptr))) return OPT_EINVAL;
   for (int32_t i = 0; i < n; ++i) {
     if (numel[i] < 0) return OPT_EINVAL;
@@ -41,11 +46,11 @@ int64_t opt_chunk_table(int32_t n, const int64_t* numel, const int32_t* grad_dty
     if (bucket_begin) bucket_begin[b] = count;
     for (int32_t i = 0; i < n; ++i) {
       if (grad_dtype[i] != buckets[b]) continue;
-      for (int64_t start = 0; start < numel[i]; start += OPT_CHUNK_ELEMS) {
+      for (int64_t start = 0; start < numel[i]; start += elems) {
         if (out != nullptr && count < cap) {
           const int64_t left = numel[i] - start;
           out[count].tensor = (uint32_t)i;
-          out[count].len = (uint32_t)(left < OPT_CHUNK_ELEMS ? left : OPT_CHUNK_ELEMS);
+          out[count].len = (uint32_t)(left < elems ? left : elems);
           out[count].start = start;
         }
         ++count;
@@ -54,6 +59,14 @@ int64_t opt_chunk_table(int32_t n, const int64_t* numel, const int32_t* grad_dty
   }
   if (bucket_begin) bucket_begin[2] = count;
   return count;
+}
+}  // namespace psopt
+
+extern "C" {
+
+int64_t opt_chunk_table(int32_t n, const int64_t* numel, const int32_t* grad_dtype,
+                        opt_chunk* out, int64_t cap, int64_t bucket_begin[3]) {
+  return psopt::build_table(n, numel, grad_dtype, OPT_CHUNK_ELEMS, out, cap, bucket_begin);
 }
 
 // Per-step scalars, formed in double and rounded once ("Investigate SM103

@@ -19,6 +19,15 @@ enum Algo { ALGO_ADAMW = 0, ALGO_ADEMAMIX = 1 };
 
 int state_combo(int32_t m_dtype, int32_t v_dtype);   // -1 if not built
 
+// Elements per tile of the step's work table: one 8-element group for each
+// of the step kernel's 256 threads.
+constexpr int64_t kTileElems = 2048;
+
+// Table of pieces of at most `elems` elements (the norm's chunks, the step's
+// tiles), bucketed by gradient dtype; see opt_chunk_table.
+int64_t build_table(int32_t n, const int64_t* numel, const int32_t* grad_dtype, int64_t elems,
+                    opt_chunk* out, int64_t cap, int64_t bucket_begin[3]);
+
 // gradient norm: pass 1 for one dtype bucket into slots[0 .. OPT_NORM_SLOTS)
 cudaError_t launch_norm_partials(int grad_dtype, const TensorDesc* tensors,
                                  const opt_chunk* chunks, int64_t chunk_begin,

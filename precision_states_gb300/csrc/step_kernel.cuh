@@ -16,8 +16,10 @@
 // and re-encoded with nearest or stochastic rounding, each tensor read and
 // written once ("When Small Updates Disappear", sec. 8.1).
 //
-// Layout: a persistent grid strides over the bucket's chunks; inside a chunk
-// each thread owns groups of 8 consecutive elements, moved with 16-byte
+// Layout: a persistent grid strides over the bucket's tiles of 2048 elements
+// (a finer table than the norm's chunks, so that short lists and lists of
+// uneven tensors still spread evenly over every SM); in a tile thread t owns
+// the 8 consecutive elements 8t .. 8t+7, moved with 16-byte
 // streaming loads and stores (p, m, v, m2: evict-first; g: read-only path).
 // The group start is a multiple of 8 elements and every base pointer is
 // 16-byte aligned, so each stream's vector is naturally aligned (E4M3: 8
@@ -25,9 +27,9 @@
 // stored element by element.
 //
 // The kernel is bound by HBM latency x bytes in flight, so each thread runs a
-// two-deep software pipeline: the raw words of its next group (possibly in
-// the CTA's next chunk) are requested before the current group is decoded,
-// updated, encoded and stored.
+// two-deep software pipeline: the raw words of its group in the CTA's next
+// tile are requested before the current group is decoded, updated, encoded
+// and stored.
 //
 // Stochastic-rounding draws: two Philox4x32-10 calls per group (counters
 // q = e0/4 and e0/4 + 1), so each draw depends only on (seed, step, tensor,
@@ -183,8 +185,8 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
       m2n[j] = __fadd_rn(__fmul_rn(sc.beta3, u2f(f.m2[j])), __fmul_rn(sc.omb3, ge));
       num = __fadd_rn(num, __fmul_rn(sc.alpha, m2n[j]));
     }
-    const float den = __fadd_rn(__fsqrt_rn(__fmul_rn(vn, sc.inv_bc2)), sc.eps);
-    const float u = __fdiv_rn(num, den);
+    const float den = __fadd_rn(sqrt_approx(__fmul_rn(vn, sc.inv_bc2)), sc.eps);
+    const float u = div_full(num, den);
     pn[j] = __fsub_rn(__fmul_rn(u2f(f.p[j]), sc.decay), __fmul_rn(sc.lr, u));
     mnv[j] = mn;
     vnv[j] = vn;
@@ -266,22 +268,15 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
   return same;
 }
 
-// A thread's walk over its groups: chunk c of the bucket (c = begin +
-// blockIdx.x + k * gridDim.x), group start `base` within the chunk.
-struct Cursor {
-  int64_t c;
-  int base;
-  opt_chunk ch;
-};
-
-__device__ __forceinline__ bool cursor_settle(Cursor& k, const StepArgs& a) {
-  while (k.base >= (int)k.ch.len) {
-    k.c += gridDim.x;
-    if (k.c >= a.chunk_end) return false;
-    k.ch = a.chunks[k.c];
-    k.base = threadIdx.x * 8;
+// The next tile (from index i, stepping by the grid) in which this thread
+// owns a group: thread t owns elements 8t .. 8t+7 of every tile; the last
+// tile of a tensor may be shorter than kTileElems.
+__device__ __forceinline__ bool next_tile(int64_t& i, const StepArgs& a, int off, opt_chunk& tl) {
+  for (; i < a.tile_end; i += gridDim.x) {
+    tl = a.tiles[i];
+    if (off < (int)tl.len) return true;
   }
-  return true;
+  return false;
 }
 
 template <int GT, int COMBO, int ALGO, bool SR>
@@ -292,12 +287,10 @@ step_kernel(const StepArgs a) {
     if (a.d_norm->status != OPT_OK) return;     // non-finite norm: leave all untouched
     coef = a.d_norm->clip_coef;
   }
-  Cursor k;
-  k.c = a.chunk_begin + blockIdx.x;
-  if (k.c >= a.chunk_end) return;
-  k.ch = a.chunks[k.c];
-  k.base = threadIdx.x * 8;
-  bool have = cursor_settle(k, a);
+  const int off = threadIdx.x * 8;
+  int64_t i = a.tile_begin + blockIdx.x;
+  opt_chunk tl;
+  bool have = next_tile(i, a, off, tl);
 
   Frag<GT, COMBO, ALGO> cur, nxt;
   TensorDesc ctd;
@@ -305,25 +298,26 @@ step_kernel(const StepArgs a) {
   int ccnt = 0;
   uint32_t ctensor = 0;
   if (have) {
-    ctd = a.tensors[k.ch.tensor];
-    ctensor = k.ch.tensor;
-    ce0 = k.ch.start + k.base;
-    ccnt = min(8, (int)k.ch.len - k.base);
+    ctd = a.tensors[tl.tensor];
+    ctensor = tl.tensor;
+    ce0 = tl.start + off;
+    ccnt = min(8, (int)tl.len - off);
     if (ccnt == 8) load_full(ctd, ce0, cur);
     else load_partial(ctd, ce0, ccnt, cur);
   }
   uint32_t same = 0;
   while (have) {
     // request the next group before working on the current one
-    k.base += kStepThreads * 8;
-    const bool have_next = cursor_settle(k, a);
+    int64_t j = i + gridDim.x;
+    opt_chunk ntl;
+    const bool have_next = next_tile(j, a, off, ntl);
     TensorDesc ntd;
     int64_t ne0 = 0;
     int ncnt = 0;
     if (have_next) {
-      ntd = a.tensors[k.ch.tensor];
-      ne0 = k.ch.start + k.base;
-      ncnt = min(8, (int)k.ch.len - k.base);
+      ntd = a.tensors[ntl.tensor];
+      ne0 = ntl.start + off;
+      ncnt = min(8, (int)ntl.len - off);
       if (ncnt == 8) load_full(ntd, ne0, nxt);
       else load_partial(ntd, ne0, ncnt, nxt);
     }
@@ -333,7 +327,8 @@ step_kernel(const StepArgs a) {
     ctd = ntd;
     ce0 = ne0;
     ccnt = ncnt;
-    ctensor = k.ch.tensor;
+    ctensor = ntl.tensor;
+    i = j;
     have = have_next;
   }
   if (a.unchanged != nullptr) {
@@ -344,10 +339,10 @@ step_kernel(const StepArgs a) {
 }
 
 // Persistent launch: as many CTAs as fit on the GPU at once (occupancy is
-// a property of the kernel, cached), but no more than there are chunks.
+// a property of the kernel, cached), but no more than there are tiles.
 template <int GT, int COMBO, int ALGO, bool SR>
 cudaError_t launch_one(const StepArgs& a, int sm_count, cudaStream_t s) {
-  const int64_t n = a.chunk_end - a.chunk_begin;
+  const int64_t n = a.tile_end - a.tile_begin;
   if (n <= 0) return cudaSuccess;
   auto k = step_kernel<GT, COMBO, ALGO, SR>;
   static int cached_per_sm = 0;
