@@ -11,12 +11,12 @@ namespace {
 
 constexpr int kCodecThreads = 256;
 
-template <int DT, bool SR>
-__device__ __forceinline__ uint32_t enc1(float x, uint32_t r16) {
-  if (DT == OPT_BF16) return bf16_enc<SR>(x, r16);
-  if (DT == OPT_E2M2) return e2m2_enc<SR>(x, r16);
-  if (SR) return e4m3_enc_sr(x, r16);
-  return e4m3x2_rn(x, 0.0f) & 0xFFu;
+// stochastic encoders (nearest goes through the paired hardware converters)
+template <int DT>
+__device__ __forceinline__ uint32_t enc_sr(float x, uint32_t r16) {
+  if (DT == OPT_BF16) return bf16_enc_sr(x, r16);
+  if (DT == OPT_E2M2) return e2m2_enc_sr(x, r16);
+  return e4m3_enc_sr(x, r16);
 }
 
 template <int DT, bool SR>
@@ -45,16 +45,20 @@ encode_kernel(const float* __restrict__ in, void* __restrict__ out, int64_t n, u
       r[4] = d1.x >> 16; r[5] = d1.y >> 16; r[6] = d1.z >> 16; r[7] = d1.w >> 16;
     }
     uint32_t c[8];
-    if (DT == OPT_E4M3 && !SR) {
+    if (SR) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) c[j] = enc_sr<DT>(x[j], r[j]);
+    } else if (DT == OPT_BF16) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) c[j] = bf16_enc_rn(x[j]);
+    } else {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint32_t pair = e4m3x2_rn(x[2 * k], x[2 * k + 1]);
+        const uint32_t pair = DT == OPT_E4M3 ? e4m3x2_rn(x[2 * k], x[2 * k + 1])
+                                             : e2m2x2_rn(x[2 * k], x[2 * k + 1]);
         c[2 * k] = pair & 0xFFu;
         c[2 * k + 1] = pair >> 8;
       }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) c[j] = enc1<DT, SR>(x[j], r[j]);
     }
     if (cnt == 8) {
       if (DT == OPT_BF16)

@@ -49,6 +49,41 @@ struct StepArgs {
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
+// ------------------------------------------------- packed f32x2 arithmetic
+// sm_100+ executes two independent IEEE fp32 operations per instruction on a
+// pair of lanes held in one 64-bit register; each lane rounds exactly as the
+// scalar operation would.
+typedef unsigned long long f2_t;   // two fp32 lanes in one 64-bit register
+
+__device__ __forceinline__ f2_t pk(float a, float b) {
+  f2_t r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpk(f2_t v, float& a, float& b) {
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ f2_t add2(f2_t a, f2_t b) {
+  f2_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2_t sub2(f2_t a, f2_t b) {
+  f2_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2_t mul2(f2_t a, f2_t b) {
+  f2_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2_t fma2(f2_t a, f2_t b, f2_t c) {
+  f2_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
 // ------------------------------------------------------------------ Philox
 // Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, "Parallel Random
 // Numbers: As Easy as 1, 2, 3", SC'11, sec. 3).  A round multiplies counter
@@ -100,33 +135,27 @@ __device__ __forceinline__ uint32_t bf16_enc(float x, uint32_t r16) {
 }
 
 // ------------------------------------------------- small-grid rounding core
-// Code of a >= 0 (finite, below the grid's largest value) on a grid with P
-// fraction bits whose binades start at 2^EMIN (spacing 2^(EMIN-P) below
-// it).  With e = max(floor(log2 a), EMIN), t = a / 2^(e-P) lies in
-// [0, 2^(P+1)) and is exact (a power-of-two scaling); the code is
-// (e - EMIN) 2^P + r, where r is t rounded to an integer:
-//  * nearest: ties to even, by adding 2^23 in round-to-nearest (the sum's
-//    last bit is the units place, so the hardware rounding is the rounding
-//    we want, exactly);
-//  * stochastic: r = floor(t + r16 / 2^16), which takes the upper neighbour
-//    exactly when the first 16 fraction bits of t plus the draw carry past
-//    2^16 ("When Small Updates Disappear", sec. 6.1, applied at the target
-//    grid's spacing).  1 + r16/2^16 is built from bits; both additions round
-//    toward zero, which cannot move the sum across an integer, so the floor is
-//    exact.
-// A carry to 2^(P+1) lands on the next binade's first code, as it should.
-template <int P, int EMIN, bool SR>
-__device__ __forceinline__ uint32_t grid_code(float a, uint32_t r16) {
-  const int e = max((int)(f2u(a) >> 23) - 127, EMIN);
-  const float t = __fmul_rn(a, u2f((uint32_t)(P - e + 127) << 23));
-  uint32_t r;
-  if (SR) {
-    const float s = __fadd_rz(t, u2f(0x3F800000u | (r16 << 7)));   // t + 1 + r16 / 2^16
-    r = f2u(__fadd_rz(s, 8388608.0f)) - 0x4B000001u;                // floor(s) - 1
-  } else {
-    r = f2u(__fadd_rn(t, 8388608.0f)) - 0x4B000000u;                // nearest integer
-  }
-  return (uint32_t)(e - EMIN) * (1u << P) + r;
+// Stochastic rounding of a (finite, 0 <= a below the grid's largest value)
+// onto a grid with P fraction bits whose binades start at 2^EMIN (constant
+// spacing 2^(EMIN-P) below it); returns the code (binade index << P | the P
+// fraction bits, counting the spacing below 2^EMIN as binade 0).
+// The rule ("When Small Updates Disappear", sec. 6.1, applied at the target
+// grid's spacing): round up iff the 16 bits just below the kept bits plus the
+// 16-bit draw carry past 2^16.  In the grid's normal range the kept bits are
+// the top P of the fp32 mantissa, so this is the BF16 bit trick at a shifted
+// position: add r16 << (7 - P) to the word and drop the low 23 - P bits (the
+// bits below the 16 examined cannot carry into them).  Below 2^EMIN the
+// spacing is constant: adding 2^EMIN with round-toward-zero moves a into the
+// first binade without disturbing any of the 16 examined bits (they all lie
+// at or above that binade's last place), and the same trick applies.
+template <int P, int EMIN>
+__device__ __forceinline__ uint32_t grid_code_sr(float a, uint32_t r16) {
+  constexpr uint32_t kMinNormal = (uint32_t)(EMIN + 127) << 23;   // the word of 2^EMIN
+  constexpr int kDrop = 23 - P;
+  const bool sub = f2u(a) < kMinNormal;
+  const float y = sub ? __fadd_rz(a, u2f(kMinNormal)) : a;
+  const uint32_t w = (f2u(y) + (r16 << (kDrop - 16))) >> kDrop;  // biased exponent << P | fraction
+  return w - ((uint32_t)(EMIN + 126) << P) - (sub ? (1u << P) : 0u);
 }
 
 // ------------------------------------------------------- E4M3 (FP8) codec
@@ -149,13 +178,28 @@ __device__ __forceinline__ uint32_t e4m3x2_rn(float lo, float hi) {
   return (uint32_t)r;
 }
 
-// Stochastic: sign kept, magnitudes at or above 448 saturate, NaN stays NaN.
+// Stochastic: sign kept, magnitudes at or above 448 (and Inf) saturate, NaN
+// stays NaN.  Branch-free: 448 itself lies on the grid, so clamping to it
+// yields its code whatever the draw.
 __device__ __forceinline__ uint32_t e4m3_enc_sr(float x, uint32_t r16) {
-  if (x != x) return 0x7Fu;
   const uint32_t sign = (f2u(x) >> 24) & 0x80u;
-  const float a = fabsf(x);
-  if (a >= 448.0f) return sign | 0x7Eu;
-  return sign | grid_code<3, -6, true>(a, r16);
+  const uint32_t code = sign | min(grid_code_sr<3, -6>(fminf(fabsf(x), 448.0f), r16), 0x7Eu);
+  return (x != x) ? 0x7Fu : code;
+}
+
+// Decode of two E4M3 codes (the low byte is the first element) by the
+// hardware converter to f16, then f16 to fp32; every E4M3 value, NaN
+// included, is an f16 value, so both steps are exact.
+__device__ __forceinline__ float h2f(unsigned short h) {
+  float f;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
+  return f;
+}
+__device__ __forceinline__ void e4m3x2_dec(uint32_t pair16, float& first, float& second) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)pair16));
+  first = h2f((unsigned short)(h2 & 0xFFFFu));
+  second = h2f((unsigned short)(h2 >> 16));
 }
 
 // ------------------------------------------------ unsigned E2M2 (FP4) codec
@@ -166,14 +210,39 @@ __device__ __forceinline__ float e2m2_dec(uint32_t c) {
   return E == 0u ? __fsub_rn(r, 1.0f) : r;
 }
 
-// Negative values store 0, NaN stores 7 (the largest code), values at or
-// above 7 saturate.
-template <bool SR>
-__device__ __forceinline__ uint32_t e2m2_enc(float x, uint32_t r16) {
-  if (x != x) return 15u;
-  if (!(x > 0.0f)) return 0u;
-  if (x >= 7.0f) return 15u;
-  return grid_code<2, 0, SR>(x, r16);
+// Decode of two E2M2 codes held in the low 4 bits of the two bytes of
+// pair16 (low byte first): as FP6 E3M2 codes (exponent field 0-3) they are
+// the E2M2 values over 4, which the hardware converts exactly to f16.
+__device__ __forceinline__ void e2m2x2_dec(uint32_t pair16, float& first, float& second) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e3m2x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)pair16));
+  first = __fmul_rn(h2f((unsigned short)(h2 & 0xFFFFu)), 4.0f);
+  second = __fmul_rn(h2f((unsigned short)(h2 >> 16)), 4.0f);
+}
+
+// The value handed to the converters: NaN stores 7 (the largest code),
+// negative values (and -0) store 0, values at or above 7 saturate.
+__device__ __forceinline__ float e2m2_clamp(float x) {
+  return (x != x) ? 7.0f : (x > 0.0f ? fminf(x, 7.0f) : 0.0f);
+}
+
+// Nearest, two values at a time: unsigned E2M2 is the FP6 E3M2 grid scaled
+// by 4 (E3M2 subnormals k/16 are E2M2's k/4 over 4; its binades with
+// exponent field 1-3 are E2M2's), so the hardware's nearest-even E3M2
+// conversion of x/4 (exact scaling), for 0 <= x <= 7, yields the E2M2 code
+// in the low bits of each byte (sign and exponent bits above are 0).  The
+// first operand lands in the upper byte.
+__device__ __forceinline__ uint32_t e2m2x2_rn(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e3m2x2.f32 %0, %1, %2;"
+      : "=h"(r) : "f"(__fmul_rn(e2m2_clamp(hi), 0.25f)), "f"(__fmul_rn(e2m2_clamp(lo), 0.25f)));
+  return (uint32_t)r;
+}
+
+// Stochastic, branch-free: 7 lies on the grid, so the clamped value 7 keeps
+// its code (15) whatever the draw.
+__device__ __forceinline__ uint32_t e2m2_enc_sr(float x, uint32_t r16) {
+  return min(grid_code_sr<2, 0>(e2m2_clamp(x), r16), 15u);
 }
 
 // ------------------------------------------ arithmetic for the update term

@@ -30,38 +30,6 @@ namespace {
 
 constexpr int kNormThreads = 256;
 
-// ---------------------------------------------------- packed f32x2 helpers
-typedef unsigned long long f2_t;   // two fp32 lanes in one 64-bit register
-
-__device__ __forceinline__ f2_t pk(float a, float b) {
-  f2_t r;
-  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ void unpk(f2_t v, float& a, float& b) {
-  asm("mov.b64 {%0,%1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-}
-__device__ __forceinline__ f2_t add2(f2_t a, f2_t b) {
-  f2_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ f2_t sub2(f2_t a, f2_t b) {
-  f2_t r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ f2_t mul2(f2_t a, f2_t b) {
-  f2_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ f2_t fma2(f2_t a, f2_t b, f2_t c) {
-  f2_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-
 // Two float-float accumulators (lane x, lane y): value = hi + lo per lane.
 struct FF2 {
   f2_t hi, lo;

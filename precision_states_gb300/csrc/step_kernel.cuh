@@ -153,65 +153,94 @@ template <int GT, int COMBO, int ALGO, bool SR>
 __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e0, int cnt,
                                                  const Frag<GT, COMBO, ALGO>& f, float coef,
                                                  const opt_step_scalars& sc, uint32_t tensor,
-                                                 uint32_t seed_lo, uint32_t seed_hi, uint32_t step32) {
+                                                 uint32_t seed_lo, uint32_t seed_hi, uint32_t step32,
+                                                 bool count) {
   using F = Frag<GT, COMBO, ALGO>;
   constexpr int MD = F::MD, VD = F::VD;
   constexpr bool LOWP = COMBO != SC_F32;
   constexpr int VBITS = VD == OPT_F32 ? 32 : VD == OPT_BF16 ? 16 : VD == OPT_E4M3 ? 8 : 4;
 
   uint32_t words[8];
-  if (LOWP && SR) {
+  if constexpr (LOWP && SR) {
     const uint4 d0 = draw_words((uint64_t)e0 >> 2, tensor, step32, seed_lo, seed_hi);
     const uint4 d1 = draw_words(((uint64_t)e0 >> 2) + 1, tensor, step32, seed_lo, seed_hi);
     words[0] = d0.x; words[1] = d0.y; words[2] = d0.z; words[3] = d0.w;
     words[4] = d1.x; words[5] = d1.y; words[6] = d1.z; words[7] = d1.w;
   }
 
-  float pn[8], mnv[8], vnv[8], m2n[8];
-  uint32_t mcode[8], vcode[8], vold[8];
+  // decode to fp32 (exact)
+  float g[8], m[8], v[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const float g = GT == OPT_BF16 ? bf16_dec(code_at<16>(f.g, j)) : u2f(f.g[j]);
-    const float m = MD == OPT_F32 ? u2f(f.m[j]) : bf16_dec(code_at<16>(f.m, j));
-    vold[j] = VBITS == 32 ? f.v[j] : code_at<VBITS>(f.v, j);
-    const float v = VD == OPT_F32 ? u2f(vold[j])
-                  : VD == OPT_BF16 ? bf16_dec(vold[j])
-                  : VD == OPT_E4M3 ? e4m3_dec(vold[j]) : e2m2_dec(vold[j]);
-    const float ge = __fmul_rn(g, coef);
-    const float mn = __fadd_rn(__fmul_rn(sc.beta1, m), __fmul_rn(sc.omb1, ge));
-    const float vn = __fadd_rn(__fmul_rn(sc.beta2, v), __fmul_rn(sc.omb2, __fmul_rn(ge, ge)));
-    float num = __fmul_rn(mn, sc.inv_bc1);
-    if (ALGO == ALGO_ADEMAMIX) {
-      m2n[j] = __fadd_rn(__fmul_rn(sc.beta3, u2f(f.m2[j])), __fmul_rn(sc.omb3, ge));
-      num = __fadd_rn(num, __fmul_rn(sc.alpha, m2n[j]));
-    }
-    const float den = __fadd_rn(sqrt_approx(__fmul_rn(vn, sc.inv_bc2)), sc.eps);
-    const float u = div_full(num, den);
-    pn[j] = __fsub_rn(__fmul_rn(u2f(f.p[j]), sc.decay), __fmul_rn(sc.lr, u));
-    mnv[j] = mn;
-    vnv[j] = vn;
-    if (MD == OPT_BF16) mcode[j] = bf16_enc<SR>(mn, SR ? (words[j] & 0xFFFFu) : 0u);
-    if (VD == OPT_F32) vcode[j] = f2u(vn);
-    else if (VD == OPT_BF16) vcode[j] = bf16_enc<SR>(vn, SR ? (words[j] >> 16) : 0u);
-    else if (VD == OPT_E2M2) vcode[j] = e2m2_enc<SR>(vn, SR ? (words[j] >> 16) : 0u);
-    else if (SR) vcode[j] = e4m3_enc_sr(vn, words[j] >> 16);
+    g[j] = GT == OPT_BF16 ? bf16_dec(code_at<16>(f.g, j)) : u2f(f.g[j]);
+    m[j] = MD == OPT_F32 ? u2f(f.m[j]) : bf16_dec(code_at<16>(f.m, j));
+    if constexpr (VD == OPT_F32) v[j] = u2f(f.v[j]);
+    if constexpr (VD == OPT_BF16) v[j] = bf16_dec(code_at<16>(f.v, j));
   }
-  if (VD == OPT_E4M3 && !SR) {
+  if constexpr (VD == OPT_E4M3) {
+    // byte pairs straight from the loaded words
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      e4m3x2_dec((k & 1) ? (f.v[k >> 1] >> 16) : (f.v[k >> 1] & 0xFFFFu), v[2 * k], v[2 * k + 1]);
+  }
+  if constexpr (VD == OPT_E2M2) {
+    // spread the nibbles into bytes: even elements, odd elements
+    const uint32_t even = f.v[0] & 0x0F0F0F0Fu, odd = (f.v[0] >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      e2m2x2_dec(__byte_perm(even, odd, (uint32_t)k | ((uint32_t)(4 + k) << 4)), v[2 * k], v[2 * k + 1]);
+  }
+  // the update, two elements per packed instruction, in the order of the
+  // definition (each lane is one IEEE fp32 operation, no contraction)
+  // the moments: scalar IEEE fp32 operations in the order of the definition
+  // (no contraction), so the values before rounding match bit for bit
+  float pn[8], mnv[8], vnv[8], m2n[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float ge = __fmul_rn(g[j], coef);
+    mnv[j] = __fadd_rn(__fmul_rn(sc.beta1, m[j]), __fmul_rn(sc.omb1, ge));
+    vnv[j] = __fadd_rn(__fmul_rn(sc.beta2, v[j]), __fmul_rn(sc.omb2, __fmul_rn(ge, ge)));
+    if constexpr (ALGO == ALGO_ADEMAMIX)
+      m2n[j] = __fadd_rn(__fmul_rn(sc.beta3, u2f(f.m2[j])), __fmul_rn(sc.omb3, ge));
+  }
+  // the update term (not a stored code)
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float num = __fmul_rn(mnv[j], sc.inv_bc1);
+    if constexpr (ALGO == ALGO_ADEMAMIX) num = __fadd_rn(num, __fmul_rn(sc.alpha, m2n[j]));
+    const float den = __fadd_rn(sqrt_approx(__fmul_rn(vnv[j], sc.inv_bc2)), sc.eps);
+    pn[j] = __fsub_rn(__fmul_rn(u2f(f.p[j]), sc.decay), __fmul_rn(sc.lr, div_full(num, den)));
+  }
+  uint32_t mcode[8], vcode[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if constexpr (MD == OPT_BF16) mcode[j] = bf16_enc<SR>(mnv[j], SR ? (words[j] & 0xFFFFu) : 0u);
+    if constexpr (VD == OPT_F32) vcode[j] = f2u(vnv[j]);
+    else if constexpr (VD == OPT_BF16) vcode[j] = bf16_enc<SR>(vnv[j], SR ? (words[j] >> 16) : 0u);
+    else if constexpr (VD == OPT_E2M2 && SR) vcode[j] = e2m2_enc_sr(vnv[j], words[j] >> 16);
+    else if constexpr (VD == OPT_E4M3 && SR) vcode[j] = e4m3_enc_sr(vnv[j], words[j] >> 16);
+  }
+  if constexpr ((VD == OPT_E4M3 || VD == OPT_E2M2) && !SR) {
+    // nearest: the hardware converters, two values per instruction
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint32_t pair = e4m3x2_rn(vnv[2 * k], vnv[2 * k + 1]);
+      const uint32_t pair = VD == OPT_E4M3 ? e4m3x2_rn(vnv[2 * k], vnv[2 * k + 1])
+                                           : e2m2x2_rn(vnv[2 * k], vnv[2 * k + 1]);
       vcode[2 * k] = pair & 0xFFu;
       vcode[2 * k + 1] = pair >> 8;
     }
   }
   uint32_t same = 0;
+  if (count) {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) same += (j < cnt && vcode[j] == vold[j]) ? 1u : 0u;
+    for (int j = 0; j < 8; ++j)
+      same += (j < cnt && vcode[j] == (VBITS == 32 ? f.v[j] : code_at<VBITS>(f.v, j))) ? 1u : 0u;
+  }
 
   if (cnt == 8) {
     st_cs_u4(td.p + e0, make_uint4(f2u(pn[0]), f2u(pn[1]), f2u(pn[2]), f2u(pn[3])));
     st_cs_u4(td.p + e0 + 4, make_uint4(f2u(pn[4]), f2u(pn[5]), f2u(pn[6]), f2u(pn[7])));
-    if (MD == OPT_F32) {
+    if constexpr (MD == OPT_F32) {
       st_cs_u4(static_cast<float*>(td.m) + e0, make_uint4(f2u(mnv[0]), f2u(mnv[1]), f2u(mnv[2]), f2u(mnv[3])));
       st_cs_u4(static_cast<float*>(td.m) + e0 + 4,
                make_uint4(f2u(mnv[4]), f2u(mnv[5]), f2u(mnv[6]), f2u(mnv[7])));
@@ -220,14 +249,14 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
                make_uint4(mcode[0] | (mcode[1] << 16), mcode[2] | (mcode[3] << 16),
                           mcode[4] | (mcode[5] << 16), mcode[6] | (mcode[7] << 16)));
     }
-    if (VD == OPT_F32) {
+    if constexpr (VD == OPT_F32) {
       st_cs_u4(static_cast<float*>(td.v) + e0, make_uint4(vcode[0], vcode[1], vcode[2], vcode[3]));
       st_cs_u4(static_cast<float*>(td.v) + e0 + 4, make_uint4(vcode[4], vcode[5], vcode[6], vcode[7]));
-    } else if (VD == OPT_BF16) {
+    } else if constexpr (VD == OPT_BF16) {
       st_cs_u4(static_cast<uint16_t*>(td.v) + e0,
                make_uint4(vcode[0] | (vcode[1] << 16), vcode[2] | (vcode[3] << 16),
                           vcode[4] | (vcode[5] << 16), vcode[6] | (vcode[7] << 16)));
-    } else if (VD == OPT_E4M3) {
+    } else if constexpr (VD == OPT_E4M3) {
       st_cs_u2(static_cast<uint8_t*>(td.v) + e0,
                make_uint2(vcode[0] | (vcode[1] << 8) | (vcode[2] << 16) | (vcode[3] << 24),
                           vcode[4] | (vcode[5] << 8) | (vcode[6] << 16) | (vcode[7] << 24)));
@@ -237,7 +266,7 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
       for (int j = 0; j < 8; ++j) w |= vcode[j] << (4 * j);
       st_cs_u1(static_cast<uint8_t*>(td.v) + (e0 >> 1), w);
     }
-    if (ALGO == ALGO_ADEMAMIX) {
+    if constexpr (ALGO == ALGO_ADEMAMIX) {
       st_cs_u4(td.m2 + e0, make_uint4(f2u(m2n[0]), f2u(m2n[1]), f2u(m2n[2]), f2u(m2n[3])));
       st_cs_u4(td.m2 + e0 + 4, make_uint4(f2u(m2n[4]), f2u(m2n[5]), f2u(m2n[6]), f2u(m2n[7])));
     }
@@ -247,14 +276,14 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
       if (j >= cnt) break;
       const int64_t e = e0 + j;
       td.p[e] = pn[j];
-      if (MD == OPT_F32) static_cast<float*>(td.m)[e] = mnv[j];
+      if constexpr (MD == OPT_F32) static_cast<float*>(td.m)[e] = mnv[j];
       else static_cast<uint16_t*>(td.m)[e] = (uint16_t)mcode[j];
-      if (VD == OPT_F32) static_cast<float*>(td.v)[e] = vnv[j];
-      else if (VD == OPT_BF16) static_cast<uint16_t*>(td.v)[e] = (uint16_t)vcode[j];
-      else if (VD == OPT_E4M3) static_cast<uint8_t*>(td.v)[e] = (uint8_t)vcode[j];
-      if (ALGO == ALGO_ADEMAMIX) td.m2[e] = m2n[j];
+      if constexpr (VD == OPT_F32) static_cast<float*>(td.v)[e] = vnv[j];
+      else if constexpr (VD == OPT_BF16) static_cast<uint16_t*>(td.v)[e] = (uint16_t)vcode[j];
+      else if constexpr (VD == OPT_E4M3) static_cast<uint8_t*>(td.v)[e] = (uint8_t)vcode[j];
+      if constexpr (ALGO == ALGO_ADEMAMIX) td.m2[e] = m2n[j];
     }
-    if (VD == OPT_E2M2) {
+    if constexpr (VD == OPT_E2M2) {
       // whole bytes: e0 is even, so byte k holds elements 2k and 2k+1 of the
       // group; an element past the end contributes a zero nibble
 #pragma unroll
@@ -287,6 +316,7 @@ step_kernel(const StepArgs a) {
     if (a.d_norm->status != OPT_OK) return;     // non-finite norm: leave all untouched
     coef = a.d_norm->clip_coef;
   }
+  const bool count = a.unchanged != nullptr;
   const int off = threadIdx.x * 8;
   int64_t i = a.tile_begin + blockIdx.x;
   opt_chunk tl;
@@ -315,14 +345,17 @@ step_kernel(const StepArgs a) {
     int64_t ne0 = 0;
     int ncnt = 0;
     if (have_next) {
-      ntd = a.tensors[ntl.tensor];
+      // consecutive tiles usually share a tensor; reusing its descriptor pays
+      // off where the ALU is busy (low-precision states), not elsewhere
+      if constexpr (COMBO != SC_F32) ntd = ntl.tensor == ctensor ? ctd : a.tensors[ntl.tensor];
+      else ntd = a.tensors[ntl.tensor];
       ne0 = ntl.start + off;
       ncnt = min(8, (int)ntl.len - off);
       if (ncnt == 8) load_full(ntd, ne0, nxt);
       else load_partial(ntd, ne0, ncnt, nxt);
     }
     same += update_store<GT, COMBO, ALGO, SR>(ctd, ce0, ccnt, cur, coef, a.sc, ctensor, a.seed_lo,
-                                              a.seed_hi, a.step32);
+                                              a.seed_hi, a.step32, count);
     cur = nxt;
     ctd = ntd;
     ce0 = ne0;
