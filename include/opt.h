@@ -98,7 +98,15 @@ typedef enum { OPT_ROUND_NEAREST = 0, OPT_ROUND_STOCHASTIC = 1 } opt_round;
  * used only by opt_ademamix_step (FP32 states only); pass NULL otherwise.
  * Every non-NULL pointer must be 16-byte aligned.  Tensors with numel 0 may
  * have NULL pointers.  The plan copies what it needs: the arrays may be
- * freed after opt_plan_create returns. */
+ * freed after opt_plan_create returns.
+ *
+ * v_scale (optional, NULL = all 1): a per-tensor power of two s_i for a
+ * low-precision v.  The stored code then holds v / s_i, so a small second
+ * moment early in training is not flushed to 0 by a coarse grid ("When Small
+ * Updates Disappear", sec. 2.3 and 5: FP8/FP4 states stall and lose small
+ * values).  Both scalings are exact, so the rounding is the same rule on the
+ * grid scaled by s_i.  Values that are not positive finite powers of two
+ * are rejected (OPT_EINVAL). */
 typedef struct opt_tensor_list {
   int32_t n;
   const int64_t* numel;
@@ -111,6 +119,7 @@ typedef struct opt_tensor_list {
   int32_t param_dtype;
   int32_t m_dtype;             /* also the dtype of m2 */
   int32_t v_dtype;
+  const float* v_scale;        /* per tensor, power of two; NULL = 1 */
 } opt_tensor_list;
 
 /* ---- hyperparameters ----------------------------------------------------
@@ -131,8 +140,18 @@ typedef struct opt_hparams {
   uint64_t seed;             /* stochastic-rounding key */
   int32_t count_unchanged;   /* nonzero: also count v codes left unchanged
                                 (read with opt_unchanged_count) */
-  int32_t reserved;          /* must be 0 */
+  int32_t flags;             /* OPT_STEP_* bits; others must be 0 */
 } opt_hparams;
+
+/* Periodic state reset ("When Small Updates Disappear", sec. 5: resetting
+ * the moments to zero restarts the cycle in which small updates get through,
+ * every ~1000 / 300 / 200 steps for BF16 / FP8 / FP4 states).  With this flag
+ * the step starts from m = v = 0 (and m2 = 0) instead of the stored states,
+ * which it does not read.  Pass step = 1 on the reset step and count up from
+ * there, as for a fresh optimizer, so that the bias corrections restart too.
+ * With count_unchanged, the reset step compares the new v codes with code 0
+ * (the state it started from). */
+#define OPT_STEP_RESET_STATES 1
 
 /* ---- norm result (48 bytes, written by opt_grad_norm) -------------------
  * sumsq    sum of squares of all finite gradient elements (fp64)
@@ -216,7 +235,7 @@ int opt_decode(const void* d_in, float* d_out, int64_t n, int32_t dtype, void* s
  * cudaMalloc, cudaFree or allocating library routine, and no host heap.  The
  * pages describe no such variant; it has no counterpart there.
  *
- * Scratch: one fixed device array inside the library (4,927,488 bytes, held
+ * Scratch: one fixed device array inside the library (5,058,560 bytes, held
  * by every GPU that loads the library until the process exits), large enough
  * for OPT_NOALLOC_MAX_TENSORS tensors and OPT_NOALLOC_MAX_CHUNKS chunks of
  * OPT_CHUNK_ELEMS elements (about 8.6e9 elements).  Larger lists are rejected

@@ -105,7 +105,7 @@ def lib():
             L.oracle_adam_tensor.argtypes = [
                 ctypes.c_int, i64, vp, ctypes.c_int, vp, ctypes.c_int, vp, vp, ctypes.c_int,
                 vp, ctypes.c_int, ctypes.POINTER(HParams), i64, f32, ctypes.c_int, u64, u32,
-                i64, ctypes.c_int, ctypes.POINTER(i64)]
+                i64, f64, ctypes.c_int, ctypes.POINTER(i64)]
             L.oracle_adam_tensor.restype = ctypes.c_int
             _lib = L
     return _lib
@@ -201,7 +201,8 @@ def hparams(lr=1e-3, beta1=0.9, beta2=0.999, beta3=0.9999, alpha=5.0, eps=1e-8,
 def adam_tensor(algo: int, p: np.ndarray, g: np.ndarray, m: np.ndarray, v: np.ndarray,
                 hp: HParams, step: int, *, m2: np.ndarray | None = None, m_dtype="f32",
                 v_dtype="f32", coef: float = 1.0, stochastic: bool = False, seed: int = 0,
-                tensor_index: int = 0, index_base: int = 0, decay_after: bool = False) -> int:
+                tensor_index: int = 0, index_base: int = 0, v_scale: float = 1.0,
+                decay_after: bool = False) -> int:
     """One step on one tensor, in place.  p: float32 (or float64 with every
     other array float64).  g: float32 or uint16 BF16 codes.  m/m2: float32 or
     uint16 BF16 codes.  v: float32, uint16 BF16, uint8 E4M3 codes, or uint8
@@ -219,7 +220,8 @@ def adam_tensor(algo: int, p: np.ndarray, g: np.ndarray, m: np.ndarray, v: np.nd
         algo, n, p.ctypes.data, p_dt, g.ctypes.data, g_dt, m.ctypes.data,
         None if m2 is None else m2.ctypes.data, _DT[m_dtype] if p_dt != F64 else F64,
         v.ctypes.data, _DT[v_dtype] if p_dt != F64 else F64, ctypes.byref(hp), int(step),
-        float(coef), int(stochastic), int(seed), int(tensor_index), int(index_base), int(decay_after),
+        float(coef), int(stochastic), int(seed), int(tensor_index), int(index_base), float(v_scale),
+        int(decay_after),
         ctypes.byref(unchanged))
     if rc != 0:
         raise ValueError("unsupported oracle combination")

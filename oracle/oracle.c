@@ -355,7 +355,8 @@ int oracle_adam_tensor(int algo, int64_t n,
                        void* v, int v_dtype,
                        const oracle_hparams* hp, int64_t step, float coef,
                        int stochastic, uint64_t seed, uint32_t tensor_index,
-                       int64_t index_base, int decay_after, int64_t* unchanged) {
+                       int64_t index_base, double v_scale, int decay_after,
+                       int64_t* unchanged) {
   if (step < 1 || index_base < 0) return -1;
   if (v_dtype == ORC_E2M2 && (index_base & 1)) return -1;
   if (algo == ORC_ADEMAMIX && m2 == 0) return -1;
@@ -367,6 +368,7 @@ int oracle_adam_tensor(int algo, int64_t n,
   int lowp = (m_dtype == ORC_BF16) || (v_dtype == ORC_BF16) ||
              (v_dtype == ORC_E4M3) || (v_dtype == ORC_E2M2);
   if (algo == ORC_ADEMAMIX && lowp) return -1;   /* AdEMAMix: FP32 states only */
+  if (!(v_scale > 0.0) || (!lowp && v_scale != 1.0)) return -1;
 
   const double b1 = hp->beta1, b2 = hp->beta2, b3 = hp->beta3;
   const double lr = hp->lr, wd = hp->weight_decay, eps = hp->eps, alpha = hp->alpha;
@@ -395,7 +397,8 @@ int oracle_adam_tensor(int algo, int64_t n,
     } else {
       float ge = (float)gi * coef;
       float md = (float)load_state(m, m_dtype, i);
-      float vd = (float)load_state(v, v_dtype, i);
+      /* a scaled low-precision v code holds v / v_scale (a power of two) */
+      float vd = (float)(load_state(v, v_dtype, i) * v_scale);
       float t1 = b1f * md;
       float t2 = omb1f * ge;
       float mf = t1 + t2;
@@ -416,7 +419,7 @@ int oracle_adam_tensor(int algo, int64_t n,
     if (wide) ((double*)p)[i] = pn;
     else      ((float*)p)[i] = (float)pn;
     store_state(m, m_dtype, i, n, m_new, stochastic, r16_m);
-    uint32_t new_code = store_state(v, v_dtype, i, n, v_new, stochastic, r16_v);
+    uint32_t new_code = store_state(v, v_dtype, i, n, lowp ? v_new / v_scale : v_new, stochastic, r16_v);
     if (algo == ORC_ADEMAMIX)
       store_state(m2, m_dtype, i, n, m2_new, stochastic, r16_m);
     if (!wide && new_code == old_code) ++same;

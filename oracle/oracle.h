@@ -88,7 +88,11 @@ enum { ORC_ADAMW = 0, ORC_ADEMAMIX = 1 };
  * or e2m2 (two codes per byte, low nibble = even element).  `coef` is the
  * clip coefficient (1 = none).  Element i of the arrays is element
  * index_base + i of the tensor (it selects the stochastic-rounding draws; it
- * must be even for E2M2).  `decay_after` != 0 selects the wrong,
+ * must be even for E2M2).  v_scale (1 unless v is low precision): the v
+ * code holds v / v_scale ("When Small Updates Disappear", sec. 2.3 and 5:
+ * a coarse grid flushes a small second moment; a power-of-two scale moves v
+ * onto the grid without changing the rounding rule).  `decay_after` != 0
+ * selects the wrong,
  * decay-after ordering; it exists only so tests can show that the pins catch
  * it.  *unchanged (if non-NULL) receives the count of v codes (or f32 words)
  * left bitwise unchanged by this step.  Returns 0, or -1 on an unsupported
@@ -100,7 +104,8 @@ int oracle_adam_tensor(int algo, int64_t n,
                        void* v, int v_dtype,
                        const oracle_hparams* hp, int64_t step, float coef,
                        int stochastic, uint64_t seed, uint32_t tensor_index,
-                       int64_t index_base, int decay_after, int64_t* unchanged);
+                       int64_t index_base, double v_scale, int decay_after,
+                       int64_t* unchanged);
 
 #ifdef __cplusplus
 }

@@ -22,6 +22,7 @@ OPT_EINVAL, OPT_EUNSUPPORTED, OPT_EALIGN, OPT_ECUDA, OPT_ENOMEM, OPT_ELIMIT = -1
 OPT_NOALLOC_MAX_TENSORS, OPT_NOALLOC_MAX_CHUNKS = 8192, 262144
 OPT_F32, OPT_BF16, OPT_E4M3, OPT_E2M2 = 0, 1, 2, 3
 OPT_ROUND_NEAREST, OPT_ROUND_STOCHASTIC = 0, 1
+OPT_STEP_RESET_STATES = 1
 OPT_CHUNK_ELEMS = 32768
 OPT_NORM_SLOTS = 1216
 
@@ -36,14 +37,14 @@ class opt_tensor_list(_c.Structure):
                 ("param", _c.POINTER(_vp)), ("grad", _c.POINTER(_vp)),
                 ("m", _c.POINTER(_vp)), ("v", _c.POINTER(_vp)), ("m2", _c.POINTER(_vp)),
                 ("grad_dtype", _c.POINTER(_c.c_int32)), ("param_dtype", _c.c_int32),
-                ("m_dtype", _c.c_int32), ("v_dtype", _c.c_int32)]
+                ("m_dtype", _c.c_int32), ("v_dtype", _c.c_int32), ("v_scale", _c.POINTER(_c.c_float))]
 
 
 class opt_hparams(_c.Structure):
     _fields_ = [("lr", _c.c_float), ("beta1", _c.c_float), ("beta2", _c.c_float),
                 ("beta3", _c.c_float), ("alpha", _c.c_float), ("eps", _c.c_float),
                 ("weight_decay", _c.c_float), ("rounding", _c.c_int32), ("seed", _c.c_uint64),
-                ("count_unchanged", _c.c_int32), ("reserved", _c.c_int32)]
+                ("count_unchanged", _c.c_int32), ("flags", _c.c_int32)]
 
 
 class opt_norm_result(_c.Structure):
@@ -136,10 +137,10 @@ def opt_strerror(status: int) -> str:
 
 
 def hparams(lr=1e-3, beta1=0.9, beta2=0.999, beta3=0.9999, alpha=5.0, eps=1e-8, weight_decay=0.0,
-            rounding="nearest", seed=0, count_unchanged=False) -> opt_hparams:
+            rounding="nearest", seed=0, count_unchanged=False, reset_states=False) -> opt_hparams:
     r = OPT_ROUND_STOCHASTIC if rounding in ("stochastic", "sr", OPT_ROUND_STOCHASTIC) else OPT_ROUND_NEAREST
     return opt_hparams(lr, beta1, beta2, beta3, alpha, eps, weight_decay, r, seed,
-                       1 if count_unchanged else 0, 0)
+                       1 if count_unchanged else 0, OPT_STEP_RESET_STATES if reset_states else 0)
 
 
 def opt_chunk_table(numel, grad_dtype):
@@ -199,7 +200,7 @@ class Plan:
     storage of the chosen state dtypes (float32, or raw code tensors such as
     int16/uint8 for BF16/E4M3/E2M2 -- only their data pointers are used)."""
 
-    def __init__(self, params, grads, m, v, m2=None, m_dtype="f32", v_dtype="f32"):
+    def __init__(self, params, grads, m, v, m2=None, m_dtype="f32", v_dtype="f32", v_scale=None):
         import torch
         n = len(params)
         if not (len(grads) == len(m) == len(v) == n) or (m2 is not None and len(m2) != n):
@@ -221,10 +222,11 @@ class Plan:
         arr = lambda ts: (_vp * max(n, 1))(*[t.data_ptr() for t in ts])
         self._arrays = dict(numel=(_c.c_int64 * max(n, 1))(*self.numel), param=arr(params),
                             grad=arr(grads), m=arr(m), v=arr(v), m2=arr(m2) if m2 else None,
-                            gd=(_c.c_int32 * max(n, 1))(*gd))
+                            gd=(_c.c_int32 * max(n, 1))(*gd),
+                            vs=(_c.c_float * max(n, 1))(*v_scale) if v_scale is not None else None)
         a = self._arrays
         tl = opt_tensor_list(n, a["numel"], a["param"], a["grad"], a["m"], a["v"], a["m2"], a["gd"],
-                             OPT_F32, DTYPES[m_dtype], DTYPES[v_dtype])
+                             OPT_F32, DTYPES[m_dtype], DTYPES[v_dtype], a["vs"])
         h = _vp()
         _check(lib().opt_plan_create(_c.byref(tl), _c.byref(h)), "opt_plan_create")
         self.handle = h

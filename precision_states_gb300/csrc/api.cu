@@ -3,6 +3,7 @@
 // fused steps, and the standalone codecs.  Every argument is checked on the
 // host before anything is launched; failures return a status and launch
 // nothing.
+#include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <new>
@@ -84,6 +85,14 @@ struct DeviceGuard {
   }
 };
 
+// A usable v scale: a positive power of two whose reciprocal is also a
+// normal float, so both scalings are exact.
+bool valid_scale(float s) {
+  if (!(s > 0.0f) || !std::isfinite(s)) return false;
+  int e = 0;
+  return std::frexp(s, &e) == 0.5f && e >= -100 && e <= 100;
+}
+
 int validate_list(const opt_tensor_list* L) {
   if (L == nullptr || L->n < 0) return OPT_EINVAL;
   if (L->n > 0 && (L->numel == nullptr || L->param == nullptr || L->grad == nullptr ||
@@ -93,6 +102,8 @@ int validate_list(const opt_tensor_list* L) {
   if (state_combo(L->m_dtype, L->v_dtype) < 0) return OPT_EUNSUPPORTED;
   for (int32_t i = 0; i < L->n; ++i) {
     if (L->numel[i] < 0) return OPT_EINVAL;
+    if (L->v_scale != nullptr && !valid_scale(L->v_scale[i])) return OPT_EINVAL;
+    if (L->v_scale != nullptr && L->v_dtype == OPT_F32 && L->v_scale[i] != 1.0f) return OPT_EINVAL;
     if (L->grad_dtype[i] != OPT_F32 && L->grad_dtype[i] != OPT_BF16) return OPT_EUNSUPPORTED;
     if (L->numel[i] == 0) continue;
     const void* ptrs[5] = {L->param[i], L->grad[i], L->m[i], L->v[i],
@@ -148,6 +159,9 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
     t.v = L->v[i];
     t.m2 = P->has_m2 ? static_cast<float*>(L->m2[i]) : nullptr;
     t.numel = L->numel[i];
+    t.v_scale = L->v_scale ? L->v_scale[i] : 1.0f;
+    t.v_inv_scale = 1.0f / t.v_scale;     // exact for a power of two
+    t.pad = 0;
     P->total_numel += L->numel[i];
     P->grad_dev[(size_t)i] = const_cast<void*>(L->grad[i]);
     P->grad_bytes[(size_t)i] = state_bytes(L->grad_dtype[i], L->numel[i]);
@@ -251,7 +265,8 @@ int opt_grad_norm(opt_plan* P, double max_norm, opt_norm_result* d_out, opt_norm
 
 static int do_step(opt_plan* P, const opt_hparams* hp, int64_t step, const opt_norm_result* d_norm,
                    void* stream, int algo) {
-  if (P == nullptr || hp == nullptr || step < 1 || hp->reserved != 0) return OPT_EINVAL;
+  if (P == nullptr || hp == nullptr || step < 1) return OPT_EINVAL;
+  if ((hp->flags & ~OPT_STEP_RESET_STATES) != 0) return OPT_EINVAL;
   if (hp->rounding != OPT_ROUND_NEAREST && hp->rounding != OPT_ROUND_STOCHASTIC) return OPT_EINVAL;
   if (d_norm != nullptr && ((uintptr_t)d_norm & 7u)) return OPT_EALIGN;
   if (algo == ALGO_ADEMAMIX) {
@@ -269,6 +284,7 @@ static int do_step(opt_plan* P, const opt_hparams* hp, int64_t step, const opt_n
   a.step32 = (uint32_t)step;
   a.d_norm = d_norm;
   a.unchanged = hp->count_unchanged ? P->d_unchanged : nullptr;
+  a.reset = (hp->flags & OPT_STEP_RESET_STATES) ? 1 : 0;
 
   DeviceGuard g(P->device);
   if (!g.ok) return OPT_ECUDA;

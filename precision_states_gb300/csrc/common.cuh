@@ -19,8 +19,11 @@ struct TensorDesc {
   void* v;
   float* m2;
   int64_t numel;
+  float v_scale;       // stored v code holds v / v_scale (power of two)
+  float v_inv_scale;   // 1 / v_scale, exact
+  uint64_t pad;
 };
-static_assert(sizeof(TensorDesc) == 48, "TensorDesc layout");
+static_assert(sizeof(TensorDesc) == 64, "TensorDesc layout");
 static_assert(sizeof(opt_chunk) == 16, "opt_chunk layout");
 
 // One fixed slot of the gradient-norm pass: the slot's chunks are
@@ -43,6 +46,7 @@ struct StepArgs {
   uint32_t seed_lo, seed_hi, step32;
   const opt_norm_result* d_norm;      // NULL: no clipping
   unsigned long long* unchanged;      // NULL: do not count
+  int reset;                          // nonzero: start from zero moments
 };
 
 // ------------------------------------------------------------- bit views

@@ -44,7 +44,7 @@ constexpr int64_t kOffGrad = 0;                                            // co
 constexpr int64_t kOffNumel = align256(kOffGrad + 8 * kMaxTensors);        // int64[T]
 constexpr int64_t kOffDtype = align256(kOffNumel + 8 * kMaxTensors);       // int32[T]
 constexpr int64_t kOffDesc = align256(kOffDtype + 4 * kMaxTensors);        // TensorDesc[T]
-constexpr int64_t kOffOrder = align256(kOffDesc + 48 * kMaxTensors);       // int32[T]: bucket-major order
+constexpr int64_t kOffOrder = align256(kOffDesc + (int64_t)sizeof(TensorDesc) * kMaxTensors);  // int32[T]
 constexpr int64_t kOffBase = align256(kOffOrder + 4 * kMaxTensors);        // int64[T]: first chunk, in that order
 constexpr int64_t kOffChunks = align256(kOffBase + 8 * kMaxTensors);       // opt_chunk[C]
 constexpr int64_t kOffSlots = align256(kOffChunks + 16 * kMaxChunks);      // NormSlot[2 * OPT_NORM_SLOTS]
@@ -121,6 +121,7 @@ noalloc_prep_kernel(unsigned char* scratch, int n) {
     const int b = dtype[t] == OPT_BF16 ? 1 : 0;
     TensorDesc d;
     d.p = nullptr; d.g = grad[t]; d.m = nullptr; d.v = nullptr; d.m2 = nullptr; d.numel = numel[t];
+    d.v_scale = 1.0f; d.v_inv_scale = 1.0f; d.pad = 0;
     desc[t] = d;
     order[pos[b]] = t;
     base[pos[b]] = next[b];

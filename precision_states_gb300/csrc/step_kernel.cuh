@@ -75,8 +75,11 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t* w, int j) {
   }
 }
 
+// Loads the group's words; with `reset` the moments are not read: they
+// start from zero (every format's code 0 is the value 0).
 template <int GT, int COMBO, int ALGO>
-__device__ __forceinline__ void load_full(const TensorDesc& td, int64_t e0, Frag<GT, COMBO, ALGO>& f) {
+__device__ __forceinline__ void load_full(const TensorDesc& td, int64_t e0, bool reset,
+                                          Frag<GT, COMBO, ALGO>& f) {
   using F = Frag<GT, COMBO, ALGO>;
   put4(f.p, ld_cs_u4(td.p + e0));
   put4(f.p + 4, ld_cs_u4(td.p + e0 + 4));
@@ -85,6 +88,15 @@ __device__ __forceinline__ void load_full(const TensorDesc& td, int64_t e0, Frag
   } else {
     put4(f.g, ld_nc_u4(static_cast<const float*>(td.g) + e0));
     put4(f.g + 4, ld_nc_u4(static_cast<const float*>(td.g) + e0 + 4));
+  }
+  if (reset) {
+#pragma unroll
+    for (int k = 0; k < F::NM; ++k) f.m[k] = 0u;
+#pragma unroll
+    for (int k = 0; k < F::NV; ++k) f.v[k] = 0u;
+#pragma unroll
+    for (int k = 0; k < F::NM2; ++k) f.m2[k] = 0u;
+    return;
   }
   if constexpr (F::NM == 8) {
     put4(f.m, ld_cs_u4(static_cast<const float*>(td.m) + e0));
@@ -114,7 +126,7 @@ __device__ __forceinline__ void load_full(const TensorDesc& td, int64_t e0, Frag
 // words, zero past the end (an E2M2 byte is read whole: both nibbles belong
 // to the tensor's ceil(n/2) bytes).
 template <int GT, int COMBO, int ALGO>
-__device__ __forceinline__ void load_partial(const TensorDesc& td, int64_t e0, int cnt,
+__device__ __forceinline__ void load_partial(const TensorDesc& td, int64_t e0, int cnt, bool reset,
                                              Frag<GT, COMBO, ALGO>& f) {
   using F = Frag<GT, COMBO, ALGO>;
 #pragma unroll
@@ -132,6 +144,7 @@ __device__ __forceinline__ void load_partial(const TensorDesc& td, int64_t e0, i
     f.p[j] = f2u(td.p[e]);
     if constexpr (F::NG == 8) f.g[j] = f2u(static_cast<const float*>(td.g)[e]);
     else f.g[j >> 1] |= (uint32_t)static_cast<const uint16_t*>(td.g)[e] << (16 * (j & 1));
+    if (reset) continue;
     if constexpr (F::NM == 8) f.m[j] = f2u(static_cast<const float*>(td.m)[e]);
     else f.m[j >> 1] |= (uint32_t)static_cast<const uint16_t*>(td.m)[e] << (16 * (j & 1));
     if constexpr (F::NV == 8) {
@@ -192,6 +205,11 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
   }
   // the update, two elements per packed instruction, in the order of the
   // definition (each lane is one IEEE fp32 operation, no contraction)
+  // a low-precision v code holds v / v_scale (a power of two: exact)
+  if constexpr (VD != OPT_F32) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], td.v_scale);
+  }
   // the moments: scalar IEEE fp32 operations in the order of the definition
   // (no contraction), so the values before rounding match bit for bit
   float pn[8], mnv[8], vnv[8], m2n[8];
@@ -212,20 +230,23 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
     pn[j] = __fsub_rn(__fmul_rn(u2f(f.p[j]), sc.decay), __fmul_rn(sc.lr, div_full(num, den)));
   }
   uint32_t mcode[8], vcode[8];
+  float vs[8];   // the value the v code stores: v / v_scale, exact
+#pragma unroll
+  for (int j = 0; j < 8; ++j) vs[j] = VD == OPT_F32 ? vnv[j] : __fmul_rn(vnv[j], td.v_inv_scale);
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     if constexpr (MD == OPT_BF16) mcode[j] = bf16_enc<SR>(mnv[j], SR ? (words[j] & 0xFFFFu) : 0u);
     if constexpr (VD == OPT_F32) vcode[j] = f2u(vnv[j]);
-    else if constexpr (VD == OPT_BF16) vcode[j] = bf16_enc<SR>(vnv[j], SR ? (words[j] >> 16) : 0u);
-    else if constexpr (VD == OPT_E2M2 && SR) vcode[j] = e2m2_enc_sr(vnv[j], words[j] >> 16);
-    else if constexpr (VD == OPT_E4M3 && SR) vcode[j] = e4m3_enc_sr(vnv[j], words[j] >> 16);
+    else if constexpr (VD == OPT_BF16) vcode[j] = bf16_enc<SR>(vs[j], SR ? (words[j] >> 16) : 0u);
+    else if constexpr (VD == OPT_E2M2 && SR) vcode[j] = e2m2_enc_sr(vs[j], words[j] >> 16);
+    else if constexpr (VD == OPT_E4M3 && SR) vcode[j] = e4m3_enc_sr(vs[j], words[j] >> 16);
   }
   if constexpr ((VD == OPT_E4M3 || VD == OPT_E2M2) && !SR) {
     // nearest: the hardware converters, two values per instruction
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint32_t pair = VD == OPT_E4M3 ? e4m3x2_rn(vnv[2 * k], vnv[2 * k + 1])
-                                           : e2m2x2_rn(vnv[2 * k], vnv[2 * k + 1]);
+      const uint32_t pair = VD == OPT_E4M3 ? e4m3x2_rn(vs[2 * k], vs[2 * k + 1])
+                                           : e2m2x2_rn(vs[2 * k], vs[2 * k + 1]);
       vcode[2 * k] = pair & 0xFFu;
       vcode[2 * k + 1] = pair >> 8;
     }
@@ -317,6 +338,7 @@ step_kernel(const StepArgs a) {
     coef = a.d_norm->clip_coef;
   }
   const bool count = a.unchanged != nullptr;
+  const bool reset = a.reset != 0;
   const int off = threadIdx.x * 8;
   int64_t i = a.tile_begin + blockIdx.x;
   opt_chunk tl;
@@ -332,8 +354,8 @@ step_kernel(const StepArgs a) {
     ctensor = tl.tensor;
     ce0 = tl.start + off;
     ccnt = min(8, (int)tl.len - off);
-    if (ccnt == 8) load_full(ctd, ce0, cur);
-    else load_partial(ctd, ce0, ccnt, cur);
+    if (ccnt == 8) load_full(ctd, ce0, reset, cur);
+    else load_partial(ctd, ce0, ccnt, reset, cur);
   }
   uint32_t same = 0;
   while (have) {
@@ -351,8 +373,8 @@ step_kernel(const StepArgs a) {
       else ntd = a.tensors[ntl.tensor];
       ne0 = ntl.start + off;
       ncnt = min(8, (int)ntl.len - off);
-      if (ncnt == 8) load_full(ntd, ne0, nxt);
-      else load_partial(ntd, ne0, ncnt, nxt);
+      if (ncnt == 8) load_full(ntd, ne0, reset, nxt);
+      else load_partial(ntd, ne0, ncnt, reset, nxt);
     }
     same += update_store<GT, COMBO, ALGO, SR>(ctd, ce0, ccnt, cur, coef, a.sc, ctensor, a.seed_lo,
                                               a.seed_hi, a.step32, count);

@@ -27,8 +27,9 @@ def hp_for(w: W.Workload, rounding="nearest", seed=1234, count=False):
 class GpuSide:
     """The workload's tensors on the GPU and a plan over them."""
 
-    def __init__(self, w: W.Workload, seed: int = 0, device="cuda"):
+    def __init__(self, w: W.Workload, seed: int = 0, device="cuda", v_scale=None):
         self.w, self.seed = w, seed
+        self.v_scale = v_scale
         self.params = W.make_params(w, device, seed)
         self.grads = W.make_grads(w, device, 1, seed)
         self.m = [W.state_storage(w.m_dtype, n, device) for n in w.sizes]
@@ -36,7 +37,7 @@ class GpuSide:
         self.m2 = ([W.state_storage(w.m_dtype, n, device) for n in w.sizes]
                    if w.algo == "ademamix" else None)
         self.plan = ps.Plan(self.params, self.grads, self.m, self.v, self.m2,
-                            m_dtype=w.m_dtype, v_dtype=w.v_dtype)
+                            m_dtype=w.m_dtype, v_dtype=w.v_dtype, v_scale=v_scale)
 
     def norm(self, max_norm: float):
         return self.plan.grad_norm(max_norm)
@@ -62,6 +63,7 @@ class OracleSide:
 
     def __init__(self, gpu: GpuSide, samples):
         self.w = gpu.w
+        self.v_scale = gpu.v_scale
         self.samples = [(s, 0, gpu.w.sizes[s]) if isinstance(s, int) else tuple(s) for s in samples]
         self.idx = [i for i, _, _ in self.samples]
         self.p = [W.to_numpy_codes(self.cut(gpu.params, k, "f32")) for k in range(len(self.samples))]
@@ -90,7 +92,7 @@ class OracleSide:
                 ALGO[self.w.algo], self.p[k], grads_np[k], self.m[k], self.v[k], ohp, t,
                 m2=None if self.m2 is None else self.m2[k], m_dtype=self.w.m_dtype,
                 v_dtype=self.w.v_dtype, coef=coef, stochastic=stochastic, seed=seed, tensor_index=i,
-                index_base=start)
+                index_base=start, v_scale=1.0 if self.v_scale is None else self.v_scale[i])
         return unchanged
 
     def compare(self, gpu: GpuSide, tol: float, exact_codes: bool):

@@ -132,7 +132,7 @@ def _tensor_list(n=1, numel=(8,), ptr=0x10000, dtype_p=0, m_dt=0, v_dt=0, gd=0):
     a = dict(numel=(ctypes.c_int64 * n)(*numel), ptrs=(ctypes.c_void_p * n)(*([ptr] * n)),
              gd=(ctypes.c_int32 * n)(*([gd] * n)))
     tl = ps.opt_tensor_list(n, a["numel"], a["ptrs"], a["ptrs"], a["ptrs"], a["ptrs"], None, a["gd"],
-                            dtype_p, m_dt, v_dt)
+                            dtype_p, m_dt, v_dt, None)
     return tl, a
 
 
@@ -182,3 +182,12 @@ def test_codec_entry_validation():
     assert L.opt_encode(0x10004, 0x10000, 4, ps.OPT_BF16, 0, 0, 0, 0, None) == ps.OPT_EALIGN
     assert L.opt_encode(None, None, 0, ps.OPT_BF16, 0, 0, 0, 0, None) == ps.OPT_OK
     assert L.opt_decode(None, None, 4, 9, None) == ps.OPT_EUNSUPPORTED
+
+
+@pytest.mark.parametrize("scale", [3.0, 0.0, -2.0, float("inf"), float("nan"), 2.0 ** -120])
+def test_plan_create_rejects_bad_v_scale(scale):
+    tl, keep = _tensor_list(m_dt=ps.OPT_BF16, v_dt=ps.OPT_E4M3)
+    sc = (ctypes.c_float * 1)(scale)
+    tl.v_scale = sc
+    h = ctypes.c_void_p()
+    assert ps.lib().opt_plan_create(ctypes.byref(tl), ctypes.byref(h)) == ps.OPT_EINVAL

@@ -10,7 +10,7 @@ import torch
 import oracle
 import precision_states_gb300 as ps
 import workloads as W
-from harness import GpuSide, hp_for, run_lockstep
+from harness import GpuSide, OracleSide, hp_for, run_lockstep
 
 pytestmark = pytest.mark.gpu
 
@@ -127,3 +127,68 @@ def test_invalid_arguments():
         ps.Plan([p[:8]], [torch.zeros(8, dtype=torch.float8_e4m3fn, device="cuda")],
                 [torch.zeros(8, device="cuda")], [torch.zeros(8, device="cuda")])
     assert e.value.status == ps.OPT_EUNSUPPORTED
+
+
+@pytest.mark.parametrize("v_dtype", ["bf16", "e4m3", "e2m2"])
+@pytest.mark.parametrize("rounding", ["nearest", "stochastic"])
+def test_scaled_v_codes(v_dtype, rounding):
+    """Per-tensor power-of-two v scales: the stored codes hold v / scale and
+    match the oracle's exactly (stochastic) or to one step (nearest)."""
+    w = W.workload("sweep", m_dtype="bf16", v_dtype=v_dtype, hp=dict(lr=1e-3, weight_decay=0.1),
+                   sigma_decay_steps=8)
+    scales = [2.0 ** k for k in ([-8, -4, 0, 3, -12] * 5)[:len(w.sizes)]]
+    gpu = GpuSide(w, seed=2, v_scale=scales)
+    _, _, counts = run_lockstep(w, 8, 1e-6, rounding=rounding, count=True, gpu=gpu, checkpoints=(1, 4))
+    assert all(got == want for got, want in counts)
+
+
+@pytest.mark.parametrize("v_dtype", ["f32", "bf16", "e2m2"])
+def test_reset_step_starts_from_zero_states(v_dtype):
+    """"When Small Updates Disappear" sec. 5: a reset step starts from zero
+    moments.  It must equal (bitwise) a step at t = 1 after zeroing the
+    states by hand, and match the oracle run from zeroed states."""
+    md = "f32" if v_dtype == "f32" else "bf16"
+    w = W.workload("sweep", m_dtype=md, v_dtype=v_dtype, hp=dict(lr=1e-2, weight_decay=0.1))
+    w.max_norm = 0.0
+    a, b = GpuSide(w, seed=4), GpuSide(w, seed=4)
+    ghp, ohp = hp_for(w)
+    for t in (1, 2, 3):                       # both accumulate the same states
+        for side in (a, b):
+            W.fill_grads(w, side.grads, t, 4)
+            side.step(t, ghp, clip=False)
+    for side in (a, b):
+        W.fill_grads(w, side.grads, 4, 4)
+    orc = OracleSide(b, range(len(w.sizes)))  # the states the reset discards
+    g_np = orc.grads(b.grads)
+    for x in b.m + b.v:
+        x.zero_()
+    b.step(1, ghp, clip=False)
+    rhp = hp_for(w)[0]
+    rhp.flags = ps.OPT_STEP_RESET_STATES
+    a.step(1, rhp, clip=False)
+    torch.cuda.synchronize()
+    for x, y in zip(a.params + a.m + a.v, b.params + b.m + b.v):
+        assert torch.equal(x, y)
+    for k in range(len(orc.samples)):
+        orc.m[k][...] = 0
+        orc.v[k][...] = 0
+    orc.step(1, g_np, ohp, 1.0, False, 77)
+    orc.compare(a, 1e-6, False)
+
+
+def test_invalid_flags_and_scales():
+    w = W.workload("sweep")
+    gpu = GpuSide(w)
+    bad = ps.hparams()
+    bad.flags = 2
+    with pytest.raises(ps.OptError) as e:
+        gpu.plan.adamw_step(bad, 1)
+    assert e.value.status == ps.OPT_EINVAL
+    x = [torch.zeros(8, device="cuda")]
+    with pytest.raises(ps.OptError):          # not a power of two
+        ps.Plan(x, [torch.zeros(8, device="cuda")], [torch.zeros(8, dtype=torch.int16, device="cuda")],
+                [torch.zeros(8, dtype=torch.uint8, device="cuda")], m_dtype="bf16", v_dtype="e4m3",
+                v_scale=[3.0])
+    with pytest.raises(ps.OptError):          # FP32 v takes no scale
+        ps.Plan(x, [torch.zeros(8, device="cuda")], [torch.zeros(8, device="cuda")],
+                [torch.zeros(8, device="cuda")], v_scale=[2.0])

@@ -345,3 +345,55 @@ def test_sr_state_update_unbiased_on_average():
     mean = acc.mean() / seeds
     ulp = 2.0 ** -8  # spacing just below 1.0
     assert abs(mean - float(target)) < 0.05 * ulp + 3 * ulp / math.sqrt(n * seeds)
+
+
+# ------------------------------------------------------------- scaled v
+@pytest.mark.parametrize("v_dtype", ["e4m3", "e2m2"])
+@pytest.mark.parametrize("stochastic", [False, True])
+def test_scaled_v_gradient_scale_invariance(v_dtype, stochastic):
+    """With every gradient multiplied by 2^j and v_scale = 2^(2j), the v codes
+    are those of the unscaled run, the BF16 m values are exactly 2^j times
+    theirs, and p moves the same way up to eps (u is scale-free).  A scale
+    applied on the wrong side of the codec, or squared wrongly, breaks it."""
+    rng = np.random.default_rng(30)
+    n, j = 512, 6
+    hp = oracle.hparams(lr=1e-3, beta2=0.999, weight_decay=0.1, eps=1e-30)
+    runs = []
+    for scale_pow in (0, j):
+        p = f32arr(rng.standard_normal(n) * 0) + np.float32(0.5)
+        m = bf16(np.zeros(n))
+        v = lp_state(v_dtype, np.zeros(n))
+        grng = np.random.default_rng(31)
+        for t in range(1, 9):
+            g = bf16(grng.standard_normal(n) * 4.0 * 2.0 ** scale_pow)
+            oracle.adam_tensor(ADAMW, p, g, m, v, hp, t, m_dtype="bf16", v_dtype=v_dtype,
+                               stochastic=stochastic, seed=5, v_scale=2.0 ** (2 * scale_pow))
+        runs.append((p.copy(), bf16_val(m).astype(np.float64), v.copy()))
+    (p0, m0, v0), (p1, m1, v1) = runs
+    assert np.array_equal(v0, v1)
+    assert np.array_equal(m1, m0 * 2.0 ** j)
+    assert np.max(np.abs(p1 - p0)) < 1e-6
+
+
+def test_scaled_v_keeps_small_second_moment():
+    """"When Small Updates Disappear", sec. 2.3 / 5: on the E2M2 grid a second
+    moment of ~1e-3 is flushed to 0; a power-of-two scale keeps it."""
+    n = 64
+    hp = oracle.hparams(lr=1e-3, beta2=0.999)
+    g = bf16(np.full(n, 1.0))
+    flushed = lp_state("e2m2", np.zeros(n))
+    oracle.adam_tensor(ADAMW, f32arr(np.zeros(n)), g, bf16(np.zeros(n)), flushed, hp, 1,
+                       m_dtype="bf16", v_dtype="e2m2")
+    assert np.all(lp_decode("e2m2", flushed, n) == 0.0)
+    kept = lp_state("e2m2", np.zeros(n))
+    oracle.adam_tensor(ADAMW, f32arr(np.zeros(n)), g, bf16(np.zeros(n)), kept, hp, 1,
+                       m_dtype="bf16", v_dtype="e2m2", v_scale=2.0 ** -8)
+    v = lp_decode("e2m2", kept, n) * 2.0 ** -8
+    assert np.allclose(v, 1e-3, rtol=0.25)
+
+
+def test_scaled_v_rejected_for_fp32_states():
+    n = 8
+    with pytest.raises(ValueError):
+        oracle.adam_tensor(ADAMW, f32arr(np.zeros(n)), f32arr(np.ones(n)), f32arr(np.zeros(n)),
+                           f32arr(np.zeros(n)), oracle.hparams(), 1, v_scale=2.0)
