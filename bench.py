@@ -57,6 +57,12 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-seconds", type=float, default=12.0)
+    ap.add_argument("--stall-curve", action="store_true",
+                    help="instead of timing: the fraction of v codes left unchanged per step, every state "
+                         "mode, over the low-precision workload's steps (one JSON line per mode)")
+    ap.add_argument("--curve-steps", type=int, default=1000)
+    ap.add_argument("--constant-sigma", action="store_true", help="stall curve with a fixed gradient scale")
+    ap.add_argument("--reset-every", type=int, default=0, help="stall curve with periodic state resets")
     return ap.parse_args()
 
 
@@ -135,7 +141,7 @@ def traffic_for(kernel_key: str, params: int):
     except (OSError, KeyError, ValueError):
         return None
     from precision_states_gb300 import build as b
-    if d.get("source_stamp") != b._stamp():
+    if d.get("source_stamp") != b.source_stamp(b.STEP_KERNEL_SOURCES):
         return None
     return d["dram_bytes_per_param"] * params
 
@@ -395,9 +401,64 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_stall_curve(args):
+    """The low-precision workload's report: for each state mode, the fraction
+    of v coordinates whose stored code a step left unchanged ("When Small
+    Updates Disappear", sec. 1.1 and 4), every step, over the whole GPT-2
+    list.  Gradients are drawn fresh every step with the workload's scale
+    schedule (or a fixed scale), optionally with periodic resets (sec. 5).
+    The model's stationary prediction is printed beside each mode."""
+    import torch
+
+    import precision_states_gb300 as ps
+    import workloads as W
+    from oracle import stall_model
+
+    dev = torch.device("cuda", 0)
+    modes = [("f32", "nearest"), ("bf16", "nearest"), ("bf16", "stochastic"), ("e4m3", "nearest"),
+             ("e4m3", "stochastic"), ("e2m2", "nearest"), ("e2m2", "stochastic")]
+    T = args.curve_steps
+    for vd, rnd in modes:
+        w = W.workload("lowp_gpt2", sigma_decay_steps=0 if args.constant_sigma else T)
+        w.m_dtype, w.v_dtype = ("f32", "f32") if vd == "f32" else ("bf16", vd)
+        params = W.make_params(w, dev, 0)
+        grads = [torch.empty(n, dtype=torch.bfloat16, device=dev) for n in w.sizes]
+        m = [W.state_storage(w.m_dtype, n, dev) for n in w.sizes]
+        v = [W.state_storage(w.v_dtype, n, dev) for n in w.sizes]
+        plan = ps.Plan(params, grads, m, v, m_dtype=w.m_dtype, v_dtype=w.v_dtype)
+        frac, t_local = [], 0
+        for t in range(1, T + 1):
+            W.fill_grads(w, grads, t, 0)
+            reset = args.reset_every > 0 and t > 1 and (t - 1) % args.reset_every == 0
+            t_local = 1 if reset else t_local + 1
+            hp = ps.hparams(rounding=rnd, seed=99, count_unchanged=True, reset_states=reset,
+                            **{**dict(beta1=0.9, beta2=0.999), **w.hp})
+            plan.adamw_step(hp, t_local)
+            frac.append(plan.unchanged_count() / w.numel)
+        plan.close()
+        del params, grads, m, v
+        torch.cuda.empty_cache()
+        p = stall_model.FRACTION_BITS.get(vd)
+        model = None if p is None else {
+            "nearest": round(stall_model.stall_nearest(0.999, p), 4) if rnd == "nearest" else None,
+            "stochastic": round(stall_model.stall_stochastic(0.999, p), 4) if rnd == "stochastic" else None}
+        pick = [s for s in (1, 2, 5, 10, 20, 50, 100, 200, 300, 500, 700, 1000) if s <= T]
+        print(json.dumps({"report": "unchanged-v fraction per step", "workload": w.name, "params": w.numel,
+                          "v_dtype": vd, "m_dtype": w.m_dtype, "rounding": rnd, "beta2": 0.999, "steps": T,
+                          "grad_scale": "constant 1" if args.constant_sigma else f"1 -> 0.1 linearly over {T}",
+                          "reset_every": args.reset_every or None,
+                          "at_step": {str(s): round(frac[s - 1], 5) for s in pick},
+                          "mean_last_100": round(sum(frac[-100:]) / min(100, T), 5),
+                          "model_stationary": model}), flush=True)
+
+
 def main():
     args = parse()
     rank, local_rank, world = dist_env()
+    if args.stall_curve:
+        if rank == 0:
+            run_stall_curve(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:

@@ -35,6 +35,23 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libpsopt.so")
 
 
+# the sources that make up the fused step kernel (for the profile stamp)
+STEP_KERNEL_SOURCES = ["step_kernel.cuh", "common.cuh", "internal.h", "step_f32.cu", "step_lowp.cu",
+                       "../../include/opt.h"]
+
+
+def source_stamp(files) -> str:
+    """SHA-256 over the named sources (paths relative to csrc/) and the flags."""
+    h = hashlib.sha256()
+    for f in files:
+        path = os.path.normpath(os.path.join(CSRC, f))
+        h.update(f.encode())
+        with open(path, "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join(NVCC_FLAGS).encode())
+    return h.hexdigest()
+
+
 def _stamp() -> str:
     h = hashlib.sha256()
     files = sorted(os.listdir(CSRC)) + ["../../include/opt.h"]
