@@ -292,14 +292,27 @@ def run_ours(args, rank, local_rank, world):
     params_per_step = w.numel
     value = params_per_step * world * args.steps / (total_ms / 1e3) / 1e9
 
-    # end-to-end through the C ABI with host buffers: per step, H2D of the
-    # gradients from pinned memory, norm + step, D2H of the norm result
+    # end-to-end through the C ABI with host buffers.  Every step copies its
+    # gradients from pinned host memory (opt_grads_upload) and reads its norm
+    # result back to pinned host memory.  Two device gradient buffers, each
+    # with a plan over the same p, m, v, let step k+1's copy (copy stream)
+    # overlap step k (compute stream); events order the reuse of a buffer.
     e2e = None
     if not args.no_e2e:
         host = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in grads]
         for h, g in zip(host, grads):
             h.copy_(g)
         ke = args.e2e_steps or args.steps
+        grads_b = [torch.empty_like(g) for g in grads]
+        plan_b = ps.Plan(params, grads_b, m, v, m2, m_dtype=w.m_dtype, v_dtype=w.v_dtype)
+        plans = [plan, plan_b]
+        steps_of = [plan.ademamix_step if w.algo == "ademamix" else plan.adamw_step,
+                    plan_b.ademamix_step if w.algo == "ademamix" else plan_b.adamw_step]
+        copy_stream = torch.cuda.Stream(dev)
+        res_dev = torch.zeros((ke, 6), dtype=torch.float64, device=dev)      # 48 B per step
+        res_host = torch.zeros((ke, 6), dtype=torch.float64, pin_memory=True)
+        up_done = [torch.cuda.Event(), torch.cuda.Event()]
+        step_done = [torch.cuda.Event(), torch.cuda.Event()]
         h2d = sum(g.numel() * g.element_size() for g in grads)
         torch.cuda.synchronize()
         if pg:
@@ -307,23 +320,39 @@ def run_ours(args, rank, local_rank, world):
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(ke):
+        copy_stream.wait_event(e0)
+        plans[0].grads_upload(host, stream=copy_stream)
+        up_done[0].record(copy_stream)
+        for k in range(ke):
+            b = k % 2
+            if k + 1 < ke:                          # prefetch the next step's gradients
+                if k >= 1:
+                    copy_stream.wait_event(step_done[1 - b])
+                plans[1 - b].grads_upload(host, stream=copy_stream)
+                up_done[1 - b].record(copy_stream)
+            stream.wait_event(up_done[b])
             t += 1
-            plan.grads_upload(host, stream=stream)
-            r = plan.grad_norm(w.max_norm, sync=True, stream=stream)   # D2H of the 48-byte result
-            step_fn(hp, t, d_norm, stream=stream)
+            d_res = res_dev[k].data_ptr()
+            plans[b].grad_norm(w.max_norm, d_out=d_res, sync=False, stream=stream)
+            steps_of[b](hp, t, d_res if clip else None, stream=stream)
+            res_host[k].copy_(res_dev[k], non_blocking=True)                 # D2H of the result
+            step_done[b].record(stream)
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1)
+        finite = all(int(res_host[k].view(torch.int32)[11]) == 0 for k in range(ke))
         if pg:
             tt = torch.tensor([e_ms], device=dev)
             pg.all_reduce(tt, op=pg.ReduceOp.MAX)
             e_ms = float(tt.item())
         e2e = {"value": params_per_step * world * ke / (e_ms / 1e3) / 1e9, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 48, "steps": ke,
-               "note": "per step: opt_grads_upload from pinned host memory (one cudaMemcpyAsync per "
-                       "tensor), opt_grad_norm with a host copy of the result, opt_adamw_step"}
-        del host
+               "ms_per_step": round(e_ms / ke, 3), "all_norms_finite": finite,
+               "note": "per step: opt_grads_upload of the step's gradients from pinned host memory (one "
+                       "cudaMemcpyAsync per tensor, copy stream, double-buffered), opt_grad_norm, the step, "
+                       "and a copy of the 48-byte norm result to pinned host memory"}
+        plan_b.close()
+        del host, grads_b
 
     peak, peak_src = measured_peak()
     bpp = step_bytes_per_param(w)

@@ -48,7 +48,8 @@ def source_stamp(files) -> str:
         h.update(f.encode())
         with open(path, "rb") as fh:
             h.update(fh.read())
-    h.update(" ".join(NVCC_FLAGS).encode())
+    # flags without machine-specific paths, so the stamp is the same wherever the tree sits
+    h.update(" ".join(f for f in NVCC_FLAGS if not os.path.isabs(f)).encode())
     return h.hexdigest()
 
 
