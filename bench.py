@@ -40,6 +40,8 @@ def step_bytes_per_param(w) -> float:
     b = 8 + ELEM_BYTES[w.grad_dtype] + 2 * ELEM_BYTES[w.m_dtype] + 2 * ELEM_BYTES[w.v_dtype]
     if w.algo == "ademamix":
         b += 2 * ELEM_BYTES[w.m_dtype]
+    if w.algo == "lamb":      # second pass: p read + write, m and v read again
+        b += 4 + ELEM_BYTES[w.m_dtype] + ELEM_BYTES[w.v_dtype]
     return b
 
 
@@ -53,6 +55,8 @@ def parse():
     ap.add_argument("--v-dtype", default=None, choices=["f32", "bf16", "e4m3", "e2m2"],
                     help="override the state dtypes: f32 = f32 m and v; otherwise bf16 m and this v")
     ap.add_argument("--rounding", default="nearest", choices=["nearest", "stochastic"])
+    ap.add_argument("--lamb", type=float, default=None, metavar="MAX_UNORM",
+                    help="time the update-norm clipping (LAMB) step with this bound instead of AdamW")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -152,7 +156,7 @@ class OracleSample:
     tensors in list order (the embedding and head last), as many as fit a
     budget of about `seconds` of single-threaded oracle time per step."""
 
-    def __init__(self, w, seconds: float, stochastic: bool = False):
+    def __init__(self, w, seconds: float, stochastic: bool = False, max_unorm: float = 0.0):
         import numpy as np
 
         import oracle
@@ -186,6 +190,7 @@ class OracleSample:
         self.m2 = ([W.to_numpy_codes(W.state_storage(w.m_dtype, w.sizes[i], "cpu")) for i in self.idx]
                    if w.algo == "ademamix" else None)
         self.stochastic = stochastic
+        self.max_unorm = max_unorm
         self.t = 0
 
     def step(self) -> float:
@@ -198,6 +203,10 @@ class OracleSample:
         if self.w.max_norm > 0:
             coef = oracle.grad_norm(self.grads, self.w.max_norm)["clip_coef"]
         for k in range(len(self.idx)):
+            if self.w.algo == "lamb":
+                oracle.lamb_tensor(self.params[k], self.grads[k], self.m[k], self.v[k], self.ohp, self.t,
+                                   self.max_unorm, coef)
+                continue
             oracle.adam_tensor(algo, self.params[k], self.grads[k], self.m[k], self.v[k], self.ohp, self.t,
                                m2=None if self.m2 is None else self.m2[k], m_dtype=self.w.m_dtype,
                                v_dtype=self.w.v_dtype, coef=coef, stochastic=self.stochastic, seed=1234,
@@ -210,10 +219,10 @@ class OracleSample:
                 f"single-threaded C oracle, {dt:.2f} s per step")
 
 
-def cpu_baseline(w, seconds: float, stochastic: bool = False):
+def cpu_baseline(w, seconds: float, stochastic: bool = False, max_unorm: float = 0.0):
     """The CPU oracle as it stands, timed on the machine's host cores (one
     thread) over a bounded sample of the same workload."""
-    smp = OracleSample(w, seconds, stochastic)
+    smp = OracleSample(w, seconds, stochastic, max_unorm)
     dt = smp.step()
     return {"value": smp.numel / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": smp.describe(dt)}
@@ -248,7 +257,10 @@ def run_ours(args, rank, local_rank, world):
     clip = w.max_norm > 0
     d_norm = plan.norm_buffer() if clip else None
     step_fn = plan.ademamix_step if w.algo == "ademamix" else plan.adamw_step
-    launches_per_step = (2 if clip else 0) + 1   # norm partials + finish, fused step (one dtype bucket)
+    if args.lamb is not None:
+        w.algo = "lamb"
+        step_fn = lambda hp_, t_, dn_, stream=None: plan.lamb_step(hp_, t_, args.lamb, dn_, stream=stream)
+    launches_per_step = (2 if clip else 0) + (3 if args.lamb is not None else 1)
 
     def one_step(t, ev=None):
         if ev is not None:
@@ -306,8 +318,11 @@ def run_ours(args, rank, local_rank, world):
         grads_b = [torch.empty_like(g) for g in grads]
         plan_b = ps.Plan(params, grads_b, m, v, m2, m_dtype=w.m_dtype, v_dtype=w.v_dtype)
         plans = [plan, plan_b]
-        steps_of = [plan.ademamix_step if w.algo == "ademamix" else plan.adamw_step,
-                    plan_b.ademamix_step if w.algo == "ademamix" else plan_b.adamw_step]
+        def stepper(pl):
+            if args.lamb is not None:
+                return lambda hp_, t_, dn_, stream=None: pl.lamb_step(hp_, t_, args.lamb, dn_, stream=stream)
+            return pl.ademamix_step if w.algo == "ademamix" else pl.adamw_step
+        steps_of = [stepper(plan), stepper(plan_b)]
         copy_stream = torch.cuda.Stream(dev)
         res_dev = torch.zeros((ke, 6), dtype=torch.float64, device=dev)      # 48 B per step
         res_host = torch.zeros((ke, 6), dtype=torch.float64, pin_memory=True)
@@ -377,7 +392,8 @@ def run_ours(args, rank, local_rank, world):
         del params, grads, m, v, m2
         plan.close()
         torch.cuda.empty_cache()
-        cpu = cpu_baseline(w, args.cpu_sample_seconds, args.rounding == "stochastic")
+        cpu = cpu_baseline(w, args.cpu_sample_seconds, args.rounding == "stochastic",
+                           args.lamb if args.lamb is not None else 0.0)
 
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),

@@ -205,6 +205,20 @@ int opt_adamw_step(opt_plan* plan, const opt_hparams* hp, int64_t step,
 int opt_ademamix_step(opt_plan* plan, const opt_hparams* hp, int64_t step,
                       const opt_norm_result* d_norm, void* stream);
 
+/* Update-norm clipping, the LAMB / max_unorm path ("Investigate SM103
+ * bias-correction broadcast in 32-bit optimizers", 'Problem' and 'B300
+ * result': the norm of each tensor's whole update is measured before it is
+ * applied; there a cross-CTA atomicAdd made it differ run to run).  With the
+ * AdamW direction u = m_hat / (sqrt(v_hat) + eps) of every element and |.| the
+ * 2-norm over a tensor, ratio = max_unorm |p| / |u| when |u| > max_unorm |p|
+ * (p before the step), else 1; then p <- p (1 - lr wd) - lr ratio u.  The norms
+ * come from fixed per-tile slots reduced per tensor in a fixed order: the
+ * result is bit-identical run to run.  max_unorm = 0 disables the clipping
+ * (the AdamW step, in three passes).  FP32 states only; hp->flags must be 0.
+ * The first call allocates a workspace of 16 bytes per 2048 elements. */
+int opt_lamb_step(opt_plan* plan, const opt_hparams* hp, int64_t step, float max_unorm,
+                  const opt_norm_result* d_norm, void* stream);
+
 /* Number of v codes (FP32 words for FP32 v) the last step with
  * count_unchanged set left bitwise unchanged ("stalled", "When Small Updates
  * Disappear" sec. 1.1).  Copies to host and synchronises the stream; resets

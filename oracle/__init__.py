@@ -107,6 +107,9 @@ def lib():
                 vp, ctypes.c_int, ctypes.POINTER(HParams), i64, f32, ctypes.c_int, u64, u32,
                 i64, f64, ctypes.c_int, ctypes.POINTER(i64)]
             L.oracle_adam_tensor.restype = ctypes.c_int
+            L.oracle_lamb_tensor.argtypes = [i64, vp, vp, ctypes.c_int, vp, vp, ctypes.POINTER(HParams),
+                                             i64, f32, f32, ctypes.POINTER(f64)]
+            L.oracle_lamb_tensor.restype = ctypes.c_int
             _lib = L
     return _lib
 
@@ -226,3 +229,19 @@ def adam_tensor(algo: int, p: np.ndarray, g: np.ndarray, m: np.ndarray, v: np.nd
     if rc != 0:
         raise ValueError("unsupported oracle combination")
     return unchanged.value
+
+
+def lamb_tensor(p: np.ndarray, g: np.ndarray, m: np.ndarray, v: np.ndarray, hp: HParams, step: int,
+                max_unorm: float, coef: float = 1.0) -> float:
+    """LAMB-style update-norm clipping step on one tensor (FP32 p, m, v; g
+    float32 or uint16 BF16 codes), in place.  Returns the ratio applied."""
+    for a in (p, m, v):
+        if a.dtype != np.float32 or not a.flags["C_CONTIGUOUS"]:
+            raise ValueError("p, m, v must be contiguous float32")
+    ratio = ctypes.c_double()
+    rc = lib().oracle_lamb_tensor(p.size, p.ctypes.data, g.ctypes.data, _grad_dtype(g), m.ctypes.data,
+                                  v.ctypes.data, ctypes.byref(hp), int(step), float(coef),
+                                  float(max_unorm), ctypes.byref(ratio))
+    if rc != 0:
+        raise ValueError("unsupported oracle combination")
+    return ratio.value

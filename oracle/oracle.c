@@ -427,3 +427,50 @@ int oracle_adam_tensor(int algo, int64_t n,
   if (unchanged) *unchanged = same;
   return 0;
 }
+
+/* ======================================================================
+ * LAMB-style update-norm clipping ("Investigate SM103 bias-correction
+ * broadcast in 32-bit optimizers", 'Problem' and 'B300 result': the 2-state
+ * optimizers' max_unorm > 0 path measures the norm of the whole update of a
+ * tensor before applying it).  Reading (the pages give no formula): with the
+ * AdamW direction u of every element of the tensor (computed from the new
+ * moments as in oracle_adam_tensor, FP32 states), ratio = max_unorm |p| / |u|
+ * when |u| > max_unorm |p| (norms over the tensor, |p| of the parameters
+ * before the step), else 1; then p <- p (1 - lr wd) - lr ratio u, decay-first.
+ * Norms are summed in double with Neumaier's compensation.
+ * ====================================================================== */
+int oracle_lamb_tensor(int64_t n, float* p, const void* g, int g_dtype, float* m,
+                       float* v, const oracle_hparams* hp, int64_t step, float coef,
+                       float max_unorm, double* ratio_out) {
+  if (step < 1 || n < 0) return -1;
+  if (g_dtype != ORC_F32 && g_dtype != ORC_BF16) return -1;
+  const double b1 = hp->beta1, b2 = hp->beta2;
+  const double lr = hp->lr, wd = hp->weight_decay, eps = hp->eps;
+  const double bc1 = 1.0 - pow(b1, (double)step);
+  const double bc2 = 1.0 - pow(b2, (double)step);
+  const double decay = 1.0 - lr * wd;
+  double su = 0.0, cu = 0.0, sp = 0.0, cp = 0.0;
+  /* first pass: the new moments (stored as FP32, as the buffers hold) and
+     the norms of the update and of the old parameters */
+  for (int64_t i = 0; i < n; ++i) {
+    double ge = load_grad(g, g_dtype, i) * (double)coef;
+    float mf = (float)(b1 * (double)m[i] + (1.0 - b1) * ge);
+    float vf = (float)(b2 * (double)v[i] + (1.0 - b2) * ge * ge);
+    m[i] = mf;
+    v[i] = vf;
+    double u = ((double)mf / bc1) / (sqrt((double)vf / bc2) + eps);
+    neumaier_add(&su, &cu, u * u);
+    neumaier_add(&sp, &cp, (double)p[i] * (double)p[i]);
+  }
+  const double un = sqrt(su + cu), pn = sqrt(sp + cp);
+  double ratio = 1.0;
+  if (max_unorm > 0.0f && un > (double)max_unorm * pn && un > 0.0)
+    ratio = (double)max_unorm * pn / un;
+  /* second pass: the update from the stored moments */
+  for (int64_t i = 0; i < n; ++i) {
+    double u = ((double)m[i] / bc1) / (sqrt((double)v[i] / bc2) + eps);
+    p[i] = (float)((double)p[i] * decay - lr * ratio * u);
+  }
+  if (ratio_out) *ratio_out = ratio;
+  return 0;
+}

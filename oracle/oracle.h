@@ -107,6 +107,14 @@ int oracle_adam_tensor(int algo, int64_t n,
                        int64_t index_base, double v_scale, int decay_after,
                        int64_t* unchanged);
 
+/* LAMB-style update-norm clipping of one tensor (FP32 states), in place:
+ * the new moments, u = m_hat / (sqrt(v_hat) + eps) per element,
+ * ratio = min(1, max_unorm |p| / |u|) over the tensor (1 when max_unorm <= 0),
+ * p <- p (1 - lr wd) - lr ratio u.  *ratio_out receives the ratio. */
+int oracle_lamb_tensor(int64_t n, float* p, const void* g, int g_dtype, float* m,
+                       float* v, const oracle_hparams* hp, int64_t step, float coef,
+                       float max_unorm, double* ratio_out);
+
 #ifdef __cplusplus
 }
 #endif

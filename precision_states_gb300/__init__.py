@@ -79,6 +79,7 @@ _SIGS = {
                                          _c.POINTER(_c.c_int32), _c.c_double, _vp, _vp]),
     "opt_adamw_step": (_c.c_int, [_vp, _c.POINTER(opt_hparams), _c.c_int64, _vp, _vp]),
     "opt_ademamix_step": (_c.c_int, [_vp, _c.POINTER(opt_hparams), _c.c_int64, _vp, _vp]),
+    "opt_lamb_step": (_c.c_int, [_vp, _c.POINTER(opt_hparams), _c.c_int64, _c.c_float, _vp, _vp]),
     "opt_unchanged_count": (_c.c_int, [_vp, _c.POINTER(_c.c_uint64), _vp]),
     "opt_grads_upload": (_c.c_int, [_vp, _c.POINTER(_vp), _vp]),
     "opt_encode": (_c.c_int, [_vp, _vp, _c.c_int64, _c.c_int32, _c.c_int32, _c.c_uint64,
@@ -266,6 +267,11 @@ class Plan:
     def ademamix_step(self, hp: opt_hparams, step: int, d_norm: int | None = None, stream=None):
         _check(lib().opt_ademamix_step(self.handle, _c.byref(hp), step, d_norm, _stream_ptr(stream)),
                "opt_ademamix_step")
+
+    def lamb_step(self, hp: opt_hparams, step: int, max_unorm: float, d_norm: int | None = None,
+                  stream=None):
+        _check(lib().opt_lamb_step(self.handle, _c.byref(hp), step, max_unorm, d_norm, _stream_ptr(stream)),
+               "opt_lamb_step")
 
     def unchanged_count(self, stream=None) -> int:
         out = _c.c_uint64()

@@ -37,6 +37,13 @@ struct opt_plan {
   NormSlot* d_slots = nullptr;
   opt_norm_result* d_result = nullptr;
   unsigned long long* d_unchanged = nullptr;
+  // update-norm clipping (LAMB) workspace, allocated on first use
+  std::vector<int64_t> tile_first, tile_count;   // per tensor, in the tile table
+  void* d_lamb = nullptr;
+  void* d_lamb_sums = nullptr;
+  int64_t* d_tile_first = nullptr;
+  int64_t* d_tile_count = nullptr;
+  float* d_ratio = nullptr;
 };
 
 namespace psopt {
@@ -147,6 +154,12 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
   std::vector<opt_chunk> tiles((size_t)ntl);
   build_table(L->n, L->numel, L->grad_dtype, kTileElems, tiles.data(), ntl, P->tile_begin);
   P->n_tiles = ntl;
+  P->tile_first.assign((size_t)L->n, 0);
+  P->tile_count.assign((size_t)L->n, 0);
+  for (int64_t k = ntl - 1; k >= 0; --k) {     // a tensor's tiles are contiguous
+    P->tile_first[tiles[(size_t)k].tensor] = k;
+    P->tile_count[tiles[(size_t)k].tensor] += 1;
+  }
 
   std::vector<TensorDesc> tds((size_t)L->n);
   P->grad_dev.resize((size_t)L->n);
@@ -212,6 +225,7 @@ void opt_plan_destroy(opt_plan* P) {
     DeviceGuard g(P->device);
     cudaDeviceSynchronize();
     cudaFree(P->d_mem);
+    if (P->d_lamb) cudaFree(P->d_lamb);
   }
   delete P;
 }
@@ -298,6 +312,53 @@ static int do_step(opt_plan* P, const opt_hparams* hp, int64_t step, const opt_n
     if (P->combo == SC_F32) e = launch_step_fp32_states(dt, algo, a, P->sm_count, s);
     else e = launch_step_lowp_states(dt, P->combo, hp->rounding == OPT_ROUND_STOCHASTIC, a,
                                      P->sm_count, s);
+  }
+  return cuda_status(e);
+}
+
+int opt_lamb_step(opt_plan* P, const opt_hparams* hp, int64_t step, float max_unorm,
+                  const opt_norm_result* d_norm, void* stream) {
+  if (P == nullptr || hp == nullptr || step < 1 || hp->flags != 0) return OPT_EINVAL;
+  if (!(max_unorm >= 0.0f) || !std::isfinite(max_unorm)) return OPT_EINVAL;
+  if (d_norm != nullptr && ((uintptr_t)d_norm & 7u)) return OPT_EALIGN;
+  if (P->combo != SC_F32) return OPT_EUNSUPPORTED;
+  StepArgs a;
+  std::memset(&a, 0, sizeof a);
+  int st = opt_step_scalars_compute(hp, step, &a.sc);
+  if (st != OPT_OK) return st;
+  a.tensors = P->d_tensors;
+  a.tiles = P->d_tiles;
+  a.d_norm = d_norm;
+  DeviceGuard g(P->device);
+  if (!g.ok) return OPT_ECUDA;
+  cudaError_t e = cudaSuccess;
+  if (P->d_lamb == nullptr && P->n > 0) {
+    // per tile: two doubles; per tensor: first tile, tile count, ratio
+    const int64_t off_f = align_up(16 * P->n_tiles, 256);
+    const int64_t off_c = align_up(off_f + 8 * (int64_t)P->n, 256);
+    const int64_t off_r = align_up(off_c + 8 * (int64_t)P->n, 256);
+    const int64_t bytes = align_up(off_r + 4 * (int64_t)P->n, 256);
+    e = cudaMalloc(&P->d_lamb, (size_t)bytes);
+    if (e != cudaSuccess) { P->d_lamb = nullptr; return cuda_status(e); }
+    char* base = static_cast<char*>(P->d_lamb);
+    P->d_lamb_sums = base;
+    P->d_tile_first = reinterpret_cast<int64_t*>(base + off_f);
+    P->d_tile_count = reinterpret_cast<int64_t*>(base + off_c);
+    P->d_ratio = reinterpret_cast<float*>(base + off_r);
+    e = cudaMemcpy(P->d_tile_first, P->tile_first.data(), 8 * (size_t)P->n, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+      e = cudaMemcpy(P->d_tile_count, P->tile_count.data(), 8 * (size_t)P->n, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int phase = 0; phase < 3 && e == cudaSuccess; ++phase) {
+    for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+      if (phase == 1 && b == 1) break;               // the ratios cover every tensor at once
+      a.tile_begin = P->tile_begin[b];
+      a.tile_end = P->tile_begin[b + 1];
+      e = launch_lamb(b == 0 ? OPT_F32 : OPT_BF16, a, P->d_lamb_sums, P->d_tile_first, P->d_tile_count, P->n,
+                      max_unorm, P->d_ratio, P->sm_count, s, phase);
+    }
   }
   return cuda_status(e);
 }

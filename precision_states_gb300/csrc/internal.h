@@ -42,6 +42,12 @@ cudaError_t launch_step_fp32_states(int grad_dtype, int algo, const StepArgs& ar
 cudaError_t launch_step_lowp_states(int grad_dtype, int combo, int stochastic, const StepArgs& args,
                                     int sm_count, cudaStream_t s);
 
+// update-norm clipping (LAMB / max_unorm): phase 0 = per-tile sums (one
+// bucket), 1 = per-tensor ratios (all tensors), 2 = apply (one bucket)
+cudaError_t launch_lamb(int grad_dtype, const StepArgs& args, void* tile_sums, const int64_t* tile_first,
+                        const int64_t* tile_count, int n_tensors, float max_unorm, float* ratio,
+                        int sm_count, cudaStream_t s, int phase);
+
 // standalone codecs
 cudaError_t launch_encode(const float* in, void* out, int64_t n, int dtype, int stochastic,
                           uint32_t seed_lo, uint32_t seed_hi, uint32_t tensor,

@@ -1,0 +1,237 @@
+// lamb.cu -- deterministic update-norm clipping (the LAMB / max_unorm path)
+// over a plan's tiles, FP32 states.
+//
+// "Investigate SM103 bias-correction broadcast in 32-bit optimizers",
+// 'Problem' and 'B300 result': the 2-state optimizers' max_unorm > 0 path
+// measures the norm of a tensor's whole update before applying it, and its
+// cross-CTA atomicAdd made that norm -- and every step after it -- differ from
+// run to run.  Here the norms come from fixed slots reduced in a fixed order,
+// so the result is bit-identical run to run:
+//   pass 1 (lamb_stats_kernel): per tile, update m and v (stored), form the
+//     AdamW direction u and write the tile's sums of u^2 and p^2 (old p) to
+//     the tile's own slot;
+//   pass 2 (lamb_ratio_kernel): one CTA per tensor sums its tiles' slots in
+//     order and sets ratio = max_unorm |p| / |u| when |u| > max_unorm |p|,
+//     else 1;
+//   pass 3 (lamb_apply_kernel): per element, u again from the stored m and v
+//     (the same operations, so the same bits), p <- p (1 - lr wd) - lr ratio u.
+// Traffic: pass 1 reads p, g, m, v and writes m, v; pass 3 reads p, m, v and
+// writes p: 38 B per parameter with BF16 gradients.
+#include "step_kernel.cuh"
+
+namespace psopt {
+namespace {
+
+constexpr int kLambThreads = kStepThreads;
+
+struct TileSums {
+  double su, sp;   // sum of u^2 and of p^2 over the tile
+};
+
+// the AdamW direction of one element from its new moments (shared by both passes)
+__device__ __forceinline__ float lamb_dir(float mn, float vn, const opt_step_scalars& sc) {
+  const float num = __fmul_rn(mn, sc.inv_bc1);
+  const float den = __fadd_rn(sqrt_approx(__fmul_rn(vn, sc.inv_bc2)), sc.eps);
+  return div_full(num, den);
+}
+
+template <int GT>
+__global__ void __launch_bounds__(kLambThreads, kStepMinBlocks)
+lamb_stats_kernel(const StepArgs a, TileSums* __restrict__ sums) {
+  float coef = 1.0f;
+  if (a.d_norm != nullptr) {
+    if (a.d_norm->status != OPT_OK) return;
+    coef = a.d_norm->clip_coef;
+  }
+  __shared__ float s_u[kLambThreads / 32], s_p[kLambThreads / 32];
+  const int off = threadIdx.x * 8;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int64_t i = a.tile_begin + blockIdx.x; i < a.tile_end; i += gridDim.x) {
+    const opt_chunk tl = a.tiles[i];
+    float su = 0.0f, sp = 0.0f;
+    if (off < (int)tl.len) {
+      const TensorDesc td = a.tensors[tl.tensor];
+      const int64_t e0 = tl.start + off;
+      const int cnt = min(8, (int)tl.len - off);
+      Frag<GT, SC_F32, ALGO_ADAMW> f;
+      if (cnt == 8) load_full(td, e0, false, f);
+      else load_partial(td, e0, cnt, false, f);
+      float mn[8], vn[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float g = GT == OPT_BF16 ? bf16_dec(code_at<16>(f.g, j)) : u2f(f.g[j]);
+        const float ge = __fmul_rn(g, coef);
+        mn[j] = __fadd_rn(__fmul_rn(a.sc.beta1, u2f(f.m[j])), __fmul_rn(a.sc.omb1, ge));
+        vn[j] = __fadd_rn(__fmul_rn(a.sc.beta2, u2f(f.v[j])), __fmul_rn(a.sc.omb2, __fmul_rn(ge, ge)));
+        if (j < cnt) {
+          const float u = lamb_dir(mn[j], vn[j], a.sc);
+          su = __fadd_rn(su, __fmul_rn(u, u));
+          sp = __fadd_rn(sp, __fmul_rn(u2f(f.p[j]), u2f(f.p[j])));
+        }
+      }
+      if (cnt == 8) {
+        st_cs_u4(static_cast<float*>(td.m) + e0, make_uint4(f2u(mn[0]), f2u(mn[1]), f2u(mn[2]), f2u(mn[3])));
+        st_cs_u4(static_cast<float*>(td.m) + e0 + 4,
+                 make_uint4(f2u(mn[4]), f2u(mn[5]), f2u(mn[6]), f2u(mn[7])));
+        st_cs_u4(static_cast<float*>(td.v) + e0, make_uint4(f2u(vn[0]), f2u(vn[1]), f2u(vn[2]), f2u(vn[3])));
+        st_cs_u4(static_cast<float*>(td.v) + e0 + 4,
+                 make_uint4(f2u(vn[4]), f2u(vn[5]), f2u(vn[6]), f2u(vn[7])));
+      } else {
+        for (int j = 0; j < cnt; ++j) {
+          static_cast<float*>(td.m)[e0 + j] = mn[j];
+          static_cast<float*>(td.v)[e0 + j] = vn[j];
+        }
+      }
+    }
+    // fixed-order reduction over the tile: warps, then the warp totals
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      su = __fadd_rn(su, __shfl_xor_sync(0xFFFFFFFFu, su, o));
+      sp = __fadd_rn(sp, __shfl_xor_sync(0xFFFFFFFFu, sp, o));
+    }
+    if (lane == 0) { s_u[warp] = su; s_p[warp] = sp; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      double tu = 0.0, tp = 0.0;
+      for (int w = 0; w < kLambThreads / 32; ++w) { tu += (double)s_u[w]; tp += (double)s_p[w]; }
+      TileSums r;
+      r.su = tu;
+      r.sp = tp;
+      sums[i] = r;
+    }
+    __syncthreads();
+  }
+}
+
+// One CTA per tensor: its tiles are contiguous in the table.
+__global__ void __launch_bounds__(kLambThreads)
+lamb_ratio_kernel(const TileSums* __restrict__ sums, const int64_t* __restrict__ tile_first,
+                  const int64_t* __restrict__ tile_count, int n, float max_unorm,
+                  const opt_norm_result* d_norm, float* __restrict__ ratio) {
+  if (d_norm != nullptr && d_norm->status != OPT_OK) return;
+  __shared__ double s_u[kLambThreads], s_p[kLambThreads];
+  for (int t = blockIdx.x; t < n; t += gridDim.x) {
+    const int64_t first = tile_first[t], count = tile_count[t];
+    double su = 0.0, sp = 0.0;
+    for (int64_t k = threadIdx.x; k < count; k += kLambThreads) {
+      su += sums[first + k].su;
+      sp += sums[first + k].sp;
+    }
+    s_u[threadIdx.x] = su;
+    s_p[threadIdx.x] = sp;
+    __syncthreads();
+    for (int w = kLambThreads / 2; w > 0; w >>= 1) {
+      if ((int)threadIdx.x < w) {
+        s_u[threadIdx.x] += s_u[threadIdx.x + w];
+        s_p[threadIdx.x] += s_p[threadIdx.x + w];
+      }
+      __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+      const double un = sqrt(s_u[0]), pn = sqrt(s_p[0]);
+      double r = 1.0;
+      if (max_unorm > 0.0f && un > (double)max_unorm * pn && un > 0.0) r = (double)max_unorm * pn / un;
+      ratio[t] = (float)r;
+    }
+    __syncthreads();
+  }
+}
+
+template <int GT>
+__global__ void __launch_bounds__(kLambThreads, kStepMinBlocks)
+lamb_apply_kernel(const StepArgs a, const float* __restrict__ ratio) {
+  if (a.d_norm != nullptr && a.d_norm->status != OPT_OK) return;
+  const int off = threadIdx.x * 8;
+  int64_t i = a.tile_begin + blockIdx.x;
+  opt_chunk tl;
+  while (next_tile(i, a, off, tl)) {
+    const TensorDesc td = a.tensors[tl.tensor];
+    const float r = ratio[tl.tensor];
+    const int64_t e0 = tl.start + off;
+    const int cnt = min(8, (int)tl.len - off);
+    float p[8], m[8], v[8];
+    if (cnt == 8) {
+      uint32_t w[8];
+      put4(w, ld_cs_u4(td.p + e0)); put4(w + 4, ld_cs_u4(td.p + e0 + 4));
+      for (int j = 0; j < 8; ++j) p[j] = u2f(w[j]);
+      put4(w, ld_cs_u4(static_cast<const float*>(td.m) + e0));
+      put4(w + 4, ld_cs_u4(static_cast<const float*>(td.m) + e0 + 4));
+      for (int j = 0; j < 8; ++j) m[j] = u2f(w[j]);
+      put4(w, ld_cs_u4(static_cast<const float*>(td.v) + e0));
+      put4(w + 4, ld_cs_u4(static_cast<const float*>(td.v) + e0 + 4));
+      for (int j = 0; j < 8; ++j) v[j] = u2f(w[j]);
+    } else {
+      for (int j = 0; j < 8; ++j) {
+        const bool in = j < cnt;
+        p[j] = in ? td.p[e0 + j] : 0.0f;
+        m[j] = in ? static_cast<const float*>(td.m)[e0 + j] : 0.0f;
+        v[j] = in ? static_cast<const float*>(td.v)[e0 + j] : 0.0f;
+      }
+    }
+    float pn[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float u = lamb_dir(m[j], v[j], a.sc);
+      pn[j] = __fsub_rn(__fmul_rn(p[j], a.sc.decay), __fmul_rn(a.sc.lr, __fmul_rn(r, u)));
+    }
+    if (cnt == 8) {
+      st_cs_u4(td.p + e0, make_uint4(f2u(pn[0]), f2u(pn[1]), f2u(pn[2]), f2u(pn[3])));
+      st_cs_u4(td.p + e0 + 4, make_uint4(f2u(pn[4]), f2u(pn[5]), f2u(pn[6]), f2u(pn[7])));
+    } else {
+      for (int j = 0; j < cnt; ++j) td.p[e0 + j] = pn[j];
+    }
+    i += gridDim.x;
+  }
+}
+
+// Persistent grid: CTAs resident at once (occupancy cached per kernel), at
+// most one per unit of work.
+template <typename K>
+int grid_for_kernel(K k, int sm_count, int64_t work) {
+  static int cached_per_sm = 0;
+  if (cached_per_sm == 0) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kLambThreads, 0) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    cached_per_sm = per_sm;
+  }
+  const int64_t full = (int64_t)cached_per_sm * sm_count;
+  return (int)(work < full ? work : full);
+}
+
+}  // namespace
+
+cudaError_t launch_lamb(int grad_dtype, const StepArgs& a, void* sums, const int64_t* tile_first,
+                        const int64_t* tile_count, int n_tensors, float max_unorm, float* ratio,
+                        int sm_count, cudaStream_t s, int phase) {
+  const int64_t tiles = a.tile_end - a.tile_begin;
+  TileSums* ts = static_cast<TileSums*>(sums);
+  if (phase == 0) {
+    if (tiles <= 0) return cudaSuccess;
+    if (grad_dtype == OPT_BF16) {
+      auto k = lamb_stats_kernel<OPT_BF16>;
+      k<<<grid_for_kernel(k, sm_count, tiles), kLambThreads, 0, s>>>(a, ts);
+    } else {
+      auto k = lamb_stats_kernel<OPT_F32>;
+      k<<<grid_for_kernel(k, sm_count, tiles), kLambThreads, 0, s>>>(a, ts);
+    }
+  } else if (phase == 1) {
+    if (n_tensors <= 0) return cudaSuccess;
+    const int grid = n_tensors < sm_count * 8 ? n_tensors : sm_count * 8;
+    lamb_ratio_kernel<<<grid, kLambThreads, 0, s>>>(ts, tile_first, tile_count, n_tensors, max_unorm,
+                                                    a.d_norm, ratio);
+  } else {
+    if (tiles <= 0) return cudaSuccess;
+    if (grad_dtype == OPT_BF16) {
+      auto k = lamb_apply_kernel<OPT_BF16>;
+      k<<<grid_for_kernel(k, sm_count, tiles), kLambThreads, 0, s>>>(a, ratio);
+    } else {
+      auto k = lamb_apply_kernel<OPT_F32>;
+      k<<<grid_for_kernel(k, sm_count, tiles), kLambThreads, 0, s>>>(a, ratio);
+    }
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace psopt

@@ -192,3 +192,70 @@ def test_invalid_flags_and_scales():
     with pytest.raises(ps.OptError):          # FP32 v takes no scale
         ps.Plan(x, [torch.zeros(8, device="cuda")], [torch.zeros(8, device="cuda")],
                 [torch.zeros(8, device="cuda")], v_scale=[2.0])
+
+
+def _lamb_run(w, seed, max_unorm, steps, with_oracle=True):
+    gpu = GpuSide(w, seed=seed)
+    orc = OracleSide(gpu, range(len(w.sizes))) if with_oracle else None
+    ghp, ohp = hp_for(w)
+    ratios = []
+    for t in range(1, steps + 1):
+        W.fill_grads(w, gpu.grads, t, seed)
+        coef = 1.0
+        d_norm = None
+        if w.max_norm > 0:
+            g_all = [W.to_numpy_codes(g) for g in gpu.grads]
+            coef = oracle.grad_norm(g_all, w.max_norm)["clip_coef"]
+            gpu.plan.grad_norm(w.max_norm, sync=False)
+            d_norm = gpu.plan.norm_buffer()
+        if orc is not None:
+            g_np = orc.grads(gpu.grads)
+            ratios.append([oracle.lamb_tensor(orc.p[k], g_np[k], orc.m[k], orc.v[k], ohp, t, max_unorm, coef)
+                           for k in range(len(orc.samples))])
+        gpu.plan.lamb_step(ghp, t, max_unorm, d_norm)
+    torch.cuda.synchronize()
+    return gpu, orc, ratios
+
+
+@pytest.mark.parametrize("gdt", ["bf16", "f32"])
+@pytest.mark.parametrize("max_unorm", [0.3, 100.0])
+def test_lamb_matches_oracle(gdt, max_unorm):
+    """Update-norm clipping ("Investigate SM103 bias-correction broadcast in
+    32-bit optimizers", 'B300 result'): the GPU's fixed-slot norms give the
+    oracle's ratios; p, m, v match within 1e-5 (1+|x|) after 5 steps."""
+    w = W.workload("sweep", grad_dtype=gdt, hp=dict(lr=1e-2, weight_decay=0.1))
+    gpu, orc, ratios = _lamb_run(w, 6, max_unorm, 5)
+    flat = [r for rs in ratios for r in rs]
+    if max_unorm < 1.0:
+        assert all(r < 1.0 for r in flat)          # |u| ~ |g|/|g| >> 0.3 |p| everywhere
+    else:
+        assert any(r == 1.0 for r in flat) and any(r < 1.0 for r in flat)   # tiny tensors still clip
+    orc.compare(gpu, 1e-5, False)
+
+
+def test_lamb_bitwise_repeatable_and_zero_bound_is_adamw():
+    w = W.workload("clip_740", steps=3)
+    a, _, _ = _lamb_run(w, 7, 0.5, 3, with_oracle=False)
+    b, _, _ = _lamb_run(w, 7, 0.5, 3, with_oracle=False)
+    for x, y in zip(a.params + a.m + a.v, b.params + b.m + b.v):
+        assert torch.equal(x, y)
+    del a, b
+    # max_unorm = 0: the AdamW step, bit for bit
+    ws = W.workload("sweep")
+    c, _, _ = _lamb_run(ws, 8, 0.0, 2, with_oracle=False)
+    d = GpuSide(ws, seed=8)
+    ghp, _ = hp_for(ws)
+    for t in (1, 2):
+        W.fill_grads(ws, d.grads, t, 8)
+        d.step(t, ghp, clip=True)
+    torch.cuda.synchronize()
+    for x, y in zip(c.params + c.m + c.v, d.params + d.m + d.v):
+        assert torch.equal(x, y)
+
+
+def test_lamb_rejects_low_precision_states():
+    w = W.workload("sweep", m_dtype="bf16", v_dtype="e4m3")
+    gpu = GpuSide(w)
+    with pytest.raises(ps.OptError) as e:
+        gpu.plan.lamb_step(ps.hparams(), 1, 1.0)
+    assert e.value.status == ps.OPT_EUNSUPPORTED
