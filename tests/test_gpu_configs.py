@@ -116,3 +116,30 @@ def test_llama3_8b_norm_and_step():
     assert again.as_dict() == got.as_dict()
     del gpu, orc
     free()
+
+
+def test_single_tensor_beyond_32bit_indexing():
+    """One tensor of 2^32 + 12 elements (BF16 grads, BF16 m and v, stochastic
+    rounding, clipped): element offsets past 2^31 and 2^32, the high word of
+    the Philox counter, and a ragged tail.  The oracle computes the full norm
+    and steps slices at the start, across 2^31, across 2^32 and at the end."""
+    n = (1 << 32) + 12
+    w = W.Workload("huge", [n], "bf16", m_dtype="bf16", v_dtype="bf16", steps=1, max_norm=1.0,
+                   p_std=0.02, grad_std=1e-3, hp=dict(lr=1e-3, weight_decay=0.1))
+    gpu = GpuSide(w, seed=9)
+    L = 4096
+    samples = [(0, 0, L), (0, (1 << 31) - L // 2, L), (0, (1 << 32) - L // 2, L), (0, n - L, L)]
+    orc = OracleSide(gpu, samples)
+    ghp, ohp = hp_for(w, rounding="stochastic", seed=2024)
+    got = gpu.plan.grad_norm(w.max_norm)
+    g_all = W.to_numpy_codes(gpu.grads[0])
+    want = oracle_norm_parallel([g_all[i:i + (1 << 28)] for i in range(0, n, 1 << 28)], w.max_norm)
+    del g_all
+    assert rel_err(got.norm2, want["norm2"]) <= 1e-12 and got.clip_coef == want["clip_coef"]
+    g_np = orc.grads(gpu.grads)
+    gpu.step(1, ghp, clip=True)
+    orc.step(1, g_np, ohp, want["clip_coef"], True, 2024)
+    torch.cuda.synchronize()
+    orc.compare(gpu, 1e-6, True)
+    del gpu, orc
+    free()
