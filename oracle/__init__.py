@@ -94,6 +94,8 @@ def lib():
             L.oracle_philox4x32_10.restype = None
             L.oracle_draws.argtypes = [u64, i64, u32, i64, ctypes.POINTER(u32), ctypes.POINTER(u32)]
             L.oracle_draws.restype = None
+            L.oracle_cast_draw.argtypes = [u64, i64, u32, i64]
+            L.oracle_cast_draw.restype = u32
             L.oracle_tensor_sumsq.argtypes = [i64, vp, ctypes.c_int, ctypes.POINTER(SumSq)]
             L.oracle_tensor_sumsq.restype = None
             L.oracle_norm_finish.argtypes = [i32, ctypes.POINTER(SumSq), f64, ctypes.POINTER(Norm)]
@@ -151,6 +153,11 @@ def draws(seed: int, step: int, tensor_index: int, index: int):
     a, b = ctypes.c_uint32(), ctypes.c_uint32()
     lib().oracle_draws(seed, step, tensor_index, index, ctypes.byref(a), ctypes.byref(b))
     return a.value, b.value
+
+
+def cast_draw(seed: int, step: int, tensor_index: int, index: int) -> int:
+    """The standalone cast's 16-bit draw for element `index`."""
+    return lib().oracle_cast_draw(seed, step, tensor_index, index)
 
 
 # ------------------------------------------------------------------ norm

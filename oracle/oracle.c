@@ -170,6 +170,23 @@ void oracle_draws(uint64_t seed, int64_t step, uint32_t tensor_index,
   *r16_v = word >> 16;
 }
 
+/* The standalone cast draws one 16-bit value per element and no more, so it
+ * uses every bit of each Philox output [SMALL sec. 7.3, the same generator
+ * and key]: counter = (element index / 8, tensor, step); element i takes
+ * word (i / 2) mod 4, its low half for an even i and its high half for an
+ * odd one. */
+uint32_t oracle_cast_draw(uint64_t seed, int64_t step, uint32_t tensor_index,
+                          int64_t index) {
+  uint64_t q = (uint64_t)index >> 3;
+  uint32_t ctr[4] = {(uint32_t)q, (uint32_t)(q >> 32), tensor_index,
+                     (uint32_t)step};
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  oracle_philox4x32_10(ctr, key, out);
+  uint32_t word = out[(index >> 1) & 3];
+  return (index & 1) ? (word >> 16) : (word & 0xFFFFu);
+}
+
 /* ======================================================================
  * Gradient norm [NORM "Correctness properties"]: every element is widened to
  * double (exact for BF16 and FP32, and so is its square), the finite squares

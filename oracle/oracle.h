@@ -51,6 +51,11 @@ void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2],
  * `tensor_index` at step `step` under `seed`. */
 void oracle_draws(uint64_t seed, int64_t step, uint32_t tensor_index,
                   int64_t index, uint32_t* r16_m, uint32_t* r16_v);
+/* The single 16-bit draw of element `index` in the standalone cast: eight
+ * elements per generator call (counter index / 8, word (index / 2) mod 4,
+ * low half for even index, high half for odd). */
+uint32_t oracle_cast_draw(uint64_t seed, int64_t step, uint32_t tensor_index,
+                          int64_t index);
 
 /* ---- gradient norm ---------------------------------------------------- */
 typedef struct {

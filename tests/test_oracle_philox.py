@@ -50,3 +50,26 @@ def test_draws_roughly_uniform():
     assert abs(r[:, 0].mean() - 32767.5) < 600
     assert abs(r[:, 1].mean() - 32767.5) < 600
     assert abs(np.corrcoef(r[:, 0], r[:, 1])[0, 1]) < 0.03
+
+
+def test_cast_draw_layout_uses_every_half_once():
+    """The standalone cast takes one 16-bit draw per element: counter
+    (index/8, tensor, step), word (index/2) mod 4, low half for even and high
+    half for odd indices, so the eight elements of a counter use its eight
+    halves exactly once each."""
+    seed, step, t = 0xFEDC_BA98_7654_3210, 12, 5
+    for base in (0, 8, 1 << 35):
+        q = base >> 3
+        words = oracle.philox4x32_10((q & 0xFFFFFFFF, q >> 32, t, step),
+                                     (seed & 0xFFFFFFFF, seed >> 32))
+        halves = [h for w in words for h in (w & 0xFFFF, w >> 16)]
+        got = [oracle.cast_draw(seed, step, t, base + j) for j in range(8)]
+        assert got == halves
+    assert oracle.cast_draw(seed, step, t, 8) != oracle.cast_draw(seed, step, t, 0) or \
+        oracle.cast_draw(seed, step, t, 9) != oracle.cast_draw(seed, step, t, 1)
+
+
+def test_cast_draws_roughly_uniform_and_uncorrelated():
+    r = np.array([oracle.cast_draw(3, 1, 0, i) for i in range(40000)], dtype=np.float64)
+    assert abs(r.mean() - 32767.5) < 600
+    assert abs(np.corrcoef(r[0::2], r[1::2])[0, 1]) < 0.03
