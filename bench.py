@@ -67,6 +67,10 @@ def parse():
     ap.add_argument("--curve-steps", type=int, default=1000)
     ap.add_argument("--constant-sigma", action="store_true", help="stall curve with a fixed gradient scale")
     ap.add_argument("--reset-every", type=int, default=0, help="stall curve with periodic state resets")
+    ap.add_argument("--cast", action="store_true",
+                    help="instead of the step: the standalone fp32 -> state-format cast (opt_encode) in every "
+                         "format and rounding mode beside torch's builtin RNE casts (one JSON line per mode)")
+    ap.add_argument("--cast-elems", type=int, default=(1 << 28) + 12)
     return ap.parse_args()
 
 
@@ -324,37 +328,47 @@ def run_ours(args, rank, local_rank, world):
             return pl.ademamix_step if w.algo == "ademamix" else pl.adamw_step
         steps_of = [stepper(plan), stepper(plan_b)]
         copy_stream = torch.cuda.Stream(dev)
-        res_dev = torch.zeros((ke, 6), dtype=torch.float64, device=dev)      # 48 B per step
-        res_host = torch.zeros((ke, 6), dtype=torch.float64, pin_memory=True)
+        res_dev = torch.zeros((max(ke, 2), 6), dtype=torch.float64, device=dev)   # 48 B per step
+        res_host = torch.zeros((max(ke, 2), 6), dtype=torch.float64, pin_memory=True)
         up_done = [torch.cuda.Event(), torch.cuda.Event()]
         step_done = [torch.cuda.Event(), torch.cuda.Event()]
         h2d = sum(g.numel() * g.element_size() for g in grads)
+
+        def e2e_loop(nsteps, t):
+            """nsteps uploads + norms + steps; returns (elapsed ms, last step)."""
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            copy_stream.wait_event(e0)
+            plans[0].grads_upload(host, stream=copy_stream)
+            up_done[0].record(copy_stream)
+            for k in range(nsteps):
+                b = k % 2
+                stream.wait_event(up_done[b])
+                t += 1
+                d_res = res_dev[k].data_ptr()
+                plans[b].grad_norm(w.max_norm, d_out=d_res, sync=False, stream=stream)
+                steps_of[b](hp, t, d_res if clip else None, stream=stream)
+                res_host[k].copy_(res_dev[k], non_blocking=True)             # D2H of the result
+                step_done[b].record(stream)
+                # prefetch the next step's gradients into the other buffer once
+                # the step that last read it (k - 1) is done.  Issued after
+                # step k so that a host call that blocks on the copy queue
+                # cannot hold back step k's launch.
+                if k + 1 < nsteps:
+                    if k >= 1:
+                        copy_stream.wait_event(step_done[1 - b])
+                    plans[1 - b].grads_upload(host, stream=copy_stream)
+                    up_done[1 - b].record(copy_stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            return e0.elapsed_time(e1), t
+
+        _, t = e2e_loop(2, t)                           # untimed: both buffers and plans warm
         torch.cuda.synchronize()
         if pg:
             pg.barrier()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        copy_stream.wait_event(e0)
-        plans[0].grads_upload(host, stream=copy_stream)
-        up_done[0].record(copy_stream)
-        for k in range(ke):
-            b = k % 2
-            if k + 1 < ke:                          # prefetch the next step's gradients
-                if k >= 1:
-                    copy_stream.wait_event(step_done[1 - b])
-                plans[1 - b].grads_upload(host, stream=copy_stream)
-                up_done[1 - b].record(copy_stream)
-            stream.wait_event(up_done[b])
-            t += 1
-            d_res = res_dev[k].data_ptr()
-            plans[b].grad_norm(w.max_norm, d_out=d_res, sync=False, stream=stream)
-            steps_of[b](hp, t, d_res if clip else None, stream=stream)
-            res_host[k].copy_(res_dev[k], non_blocking=True)                 # D2H of the result
-            step_done[b].record(stream)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e_ms = e0.elapsed_time(e1)
+        e_ms, t = e2e_loop(ke, t)
         finite = all(int(res_host[k].view(torch.int32)[11]) == 0 for k in range(ke))
         if pg:
             tt = torch.tensor([e_ms], device=dev)
@@ -497,9 +511,75 @@ def run_stall_curve(args):
                           "model_stationary": model}), flush=True)
 
 
+def run_cast(args):
+    """The standalone cast ("When Small Updates Disappear", sec. 6-8: an fp32
+    tensor rounded to BF16, nearest or stochastic, one read and one write
+    per element) for BF16, E4M3 and E2M2 through opt_encode, timed with CUDA
+    events over --steps launches after --warmup, beside torch's builtin
+    round-to-nearest conversions (copy_ into a preallocated BF16 / E4M3
+    tensor), which are the hardware-cast yardstick.  The input (4 B per
+    element) is larger than L2, so every launch streams from HBM."""
+    import torch
+
+    import precision_states_gb300 as ps
+
+    dev = torch.device("cuda", 0)
+    n = args.cast_elems
+    gen = torch.Generator(device=dev).manual_seed(7)
+    x = torch.randn(n, generator=gen, device=dev, dtype=torch.float32) * 1e-3
+    peak, peak_src = measured_peak()
+    stream = torch.cuda.current_stream(dev)
+    out_bytes = {"bf16": 2, "e4m3": 1, "e2m2": 0.5}
+    outs = {"bf16": torch.empty(n, dtype=torch.int16, device=dev),
+            "e4m3": torch.empty(n, dtype=torch.uint8, device=dev),
+            "e2m2": torch.empty((n + 1) // 2, dtype=torch.uint8, device=dev)}
+    builtin = {"bf16": torch.empty(n, dtype=torch.bfloat16, device=dev)}
+    if hasattr(torch, "float8_e4m3fn"):
+        builtin["e4m3"] = torch.empty(n, dtype=torch.float8_e4m3fn, device=dev)
+
+    launches = max(args.steps, 100)       # ~0.2 ms each: enough launches for a stable mean
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(launches):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / launches
+
+    ref_ms = {dt: timed(lambda t=t: t.copy_(x)) for dt, t in builtin.items()}
+    clocks = ClockSampler(0)
+    for dt in ("bf16", "e4m3", "e2m2"):
+        for rnd in ("nearest", "stochastic"):
+            clocks.start()
+            time.sleep(0.2)
+            ms = timed(lambda: ps.opt_encode(x, outs[dt], dt, rnd, seed=11, tensor_index=0, step=1,
+                                             stream=stream))
+            clk = clocks.stop()
+            nbytes = n * (4 + out_bytes[dt])
+            gbs = nbytes / (ms / 1e3) / 1e9
+            line = {"report": "standalone cast", "elements": n, "format": dt, "rounding": rnd,
+                    "ms_per_launch": round(ms, 4), "gelem_per_s": round(n / (ms / 1e3) / 1e9, 2),
+                    "hbm_gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "peak_gbs": peak, "peak_source": peak_src,
+                    "bytes_per_elem": 4 + out_bytes[dt], "launches": launches, "warmup": max(3, args.warmup),
+                    "l2": "input larger than L2 (%.2f GB)" % (4 * n / 1e9), "clocks": clk}
+            if dt in ref_ms:
+                line["builtin_rne_ms"] = round(ref_ms[dt], 4)
+                line["vs_builtin_rne"] = round(ref_ms[dt] / ms, 4)
+            print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank, local_rank, world = dist_env()
+    if args.cast:
+        if rank == 0:
+            run_cast(args)
+        return
     if args.stall_curve:
         if rank == 0:
             run_stall_curve(args)

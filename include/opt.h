@@ -230,10 +230,15 @@ int opt_unchanged_count(opt_plan* plan, uint64_t* h_count, void* stream);
 int opt_grads_upload(opt_plan* plan, const void* const* h_grad, void* stream);
 
 /* Standalone conversion of n fp32 values to a state format (and back), with
- * the same codecs and draws the step uses: element i takes the v draw of
- * element i of tensor `tensor_index` at step `step` ("When Small Updates
- * Disappear", sec. 6-8: the stand-alone cast).  d_out holds n elements of
- * `dtype` (ceil(n/2) bytes for E2M2).  Pointers 16-byte aligned. */
+ * the same codecs the step uses ("When Small Updates Disappear", sec. 6-8:
+ * the stand-alone cast).  Stochastic rounding draws one 16-bit value per
+ * element from the step's generator and key (seed; tensor `tensor_index`,
+ * step `step` in the counter), eight elements per generator call: element i
+ * takes word (i/2) mod 4 of counter i/8, its low half for even i and its
+ * high half for odd i.  d_out holds n elements of `dtype` (ceil(n/2) bytes
+ * for E2M2, the unused high nibble of an odd tail 0).  Pointers 16-byte
+ * aligned; n >= 0, step >= 0.  Returns OPT_OK, OPT_EINVAL, OPT_EUNSUPPORTED
+ * (not BF16, E4M3 or E2M2), OPT_EALIGN or OPT_ECUDA. */
 int opt_encode(const float* d_in, void* d_out, int64_t n, int32_t dtype,
                int32_t rounding, uint64_t seed, uint32_t tensor_index,
                int64_t step, void* stream);

@@ -1,8 +1,18 @@
 // codec.cu -- standalone conversion of fp32 arrays to a state format and
-// back, with the same codecs and draws the fused step uses ("When Small
-// Updates Disappear", sec. 6-8: the stand-alone fp32 -> BF16 cast with
-// nearest or stochastic rounding, one read and one write per element).
-// Element i takes the v draw of element i of the given tensor and step.
+// back, with the same codecs the fused step uses ("When Small Updates
+// Disappear", sec. 6-8: the stand-alone fp32 -> BF16 cast with nearest or
+// stochastic rounding, one read and one write per element).
+//
+// The cast needs one 16-bit draw per element, so it spends every bit of a
+// Philox call: the call for counter (g, tensor, step) serves the eight
+// elements 8g .. 8g+7, element 8g+j taking word j/2, low half for even j and
+// high half for odd j.  At one call per eight elements the generator stays
+// under the memory time.
+//
+// Work unit: a group of eight elements (32 input bytes; 16, 8 or 4 output
+// bytes), one per thread.  A ragged tail (n mod 8 elements) is finished by
+// the thread after the last full group, out of line, with guarded scalar
+// accesses; every register array is indexed by compile-time constants only.
 #include "common.cuh"
 #include "internal.h"
 
@@ -10,101 +20,179 @@ namespace psopt {
 namespace {
 
 constexpr int kCodecThreads = 256;
+// Occupancy hint: six CTAs per SM, 1536 threads.  (Eight, which caps registers
+// at 32, crashes the aarch64 build of ptxas 13.0 on these kernels.)
+constexpr int kCodecBlocksPerSM = 6;
 
-// stochastic encoders (nearest goes through the paired hardware converters)
+// Output bytes of one eight-element group, packed in the order memory
+// holds them: BF16 in w.x..w.w, E4M3 in w.x..w.y, E2M2 in w.x.  Two
+// elements per converter instruction; with stochastic rounding, draw word k
+// (low half for element 2k, high half for 2k+1) is exactly the random-bits
+// operand of pair k.
 template <int DT>
-__device__ __forceinline__ uint32_t enc_sr(float x, uint32_t r16) {
-  if (DT == OPT_BF16) return bf16_enc_sr(x, r16);
-  if (DT == OPT_E2M2) return e2m2_enc_sr(x, r16);
-  return e4m3_enc_sr(x, r16);
+__device__ __forceinline__ uint4 encode_group(const float (&x)[8], uint4 d, bool sr) {
+  const uint32_t words[4] = {d.x, d.y, d.z, d.w};
+  uint32_t pr[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float lo = x[2 * k], hi = x[2 * k + 1];
+    if (DT == OPT_BF16) pr[k] = sr ? bf16x2_sr(lo, hi, words[k]) : bf16x2_rn(lo, hi);
+    else if (DT == OPT_E4M3) pr[k] = sr ? e4m3x2_sr(lo, hi, words[k]) : e4m3x2_rn(lo, hi);
+    else {
+      const float lo4 = __fmul_rn(lo, 0.25f), hi4 = __fmul_rn(hi, 0.25f);   // exact
+      pr[k] = sr ? e2m2x2_sr_q(lo4, hi4, words[k]) : e2m2x2_rn_q(lo4, hi4);
+    }
+  }
+  uint4 w = make_uint4(0u, 0u, 0u, 0u);
+  if (DT == OPT_BF16) {
+    w = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+  } else if (DT == OPT_E4M3) {
+    w.x = pr[0] | (pr[1] << 16);
+    w.y = pr[2] | (pr[3] << 16);
+  } else {
+    // pair k holds the two codes in bytes 0 and 1; byte k of the output
+    // holds them as nibbles (even element low)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w.x |= ((pr[k] | (pr[k] >> 4)) & 0xFFu) << (8 * k);
+  }
+  return w;
 }
+
+template <int DT>
+__device__ __forceinline__ void store_group(void* out, int64_t g, uint4 w) {
+  if (DT == OPT_BF16) st_cs_u4(static_cast<char*>(out) + 16 * g, w);
+  else if (DT == OPT_E4M3) st_cs_u2(static_cast<char*>(out) + 8 * g, make_uint2(w.x, w.y));
+  else st_cs_u1(static_cast<char*>(out) + 4 * g, w.x);
+}
+
+// The ragged tail (elements 8*full .. n-1, rem of them), by one thread; out
+// of line so that its scalar accesses add nothing to the main path's
+// registers.
+template <int DT, bool SR>
+__device__ __noinline__ void encode_tail(const float* __restrict__ in, void* __restrict__ out, int64_t full,
+                                         int rem, uint32_t seed_lo, uint32_t seed_hi, uint32_t tensor,
+                                         uint32_t step32) {
+  const int64_t e0 = full * 8;
+  float xt[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) xt[j] = j < rem ? in[e0 + j] : 0.0f;
+  const uint4 d = SR ? draw_words((uint64_t)full, tensor, step32, seed_lo, seed_hi) : make_uint4(0u, 0u, 0u, 0u);
+  const uint4 w = encode_group<DT>(xt, d, SR);
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+  // bytes that belong to the tail's elements (a half-filled E2M2 byte holds
+  // 0, the code of the zero padding, in its high nibble)
+  const int nbytes = DT == OPT_BF16 ? 2 * rem : (DT == OPT_E4M3 ? rem : (rem + 1) / 2);
+  uint8_t* dst = static_cast<uint8_t*>(out) + (DT == OPT_BF16 ? 2 * e0 : (DT == OPT_E4M3 ? e0 : e0 / 2));
+#pragma unroll
+  for (int b = 0; b < 16; ++b)
+    if (b < nbytes) dst[b] = (uint8_t)(ws[b >> 2] >> (8 * (b & 3)));
+}
+
+// Thread g0 + (global thread index) encodes group g; the thread at g == full
+// finishes a ragged tail.
+template <int DT, bool SR>
+__global__ void __launch_bounds__(kCodecThreads, kCodecBlocksPerSM)
+encode_kernel(const float* __restrict__ in, void* __restrict__ out, int64_t n, int64_t g0, uint32_t seed_lo,
+              uint32_t seed_hi, uint32_t tensor, uint32_t step32) {
+  const int64_t full = n >> 3;                       // complete groups
+  const int64_t g = g0 + (int64_t)blockIdx.x * kCodecThreads + threadIdx.x;
+  if (g < full) {
+    const char* src = reinterpret_cast<const char*>(in) + 32 * g;
+    const uint4 a0 = ld_nc_u4(src), a1 = ld_nc_u4(src + 16);
+    const uint4 d = SR ? draw_words((uint64_t)g, tensor, step32, seed_lo, seed_hi) : make_uint4(0u, 0u, 0u, 0u);
+    const float x[8] = {u2f(a0.x), u2f(a0.y), u2f(a0.z), u2f(a0.w),
+                        u2f(a1.x), u2f(a1.y), u2f(a1.z), u2f(a1.w)};
+    store_group<DT>(out, g, encode_group<DT>(x, d, SR));
+  } else if (g == full && (n & 7) != 0) {
+    encode_tail<DT, SR>(in, out, full, (int)(n & 7), seed_lo, seed_hi, tensor, step32);
+  }
+}
+
+// Decode, eight elements per group: codes in, two 16-byte stores of fp32 out.
+template <int DT>
+__device__ __forceinline__ void decode_group(const void* in, int64_t g, float (&x)[8]) {
+  if (DT == OPT_BF16) {
+    const uint4 w = ld_nc_u4(static_cast<const char*>(in) + 16 * g);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      x[2 * k] = u2f(ws[k] << 16);
+      x[2 * k + 1] = u2f(ws[k] & 0xFFFF0000u);
+    }
+  } else if (DT == OPT_E4M3) {
+    const uint2 w = ld_cs_u2(static_cast<const char*>(in) + 8 * g);
+    const uint32_t ws[2] = {w.x, w.y};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) e4m3x2_dec((ws[k >> 1] >> (16 * (k & 1))) & 0xFFFFu, x[2 * k], x[2 * k + 1]);
+  } else {
+    const uint32_t w = ld_cs_u1(static_cast<const char*>(in) + 4 * g);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t byte = (w >> (8 * k)) & 0xFFu;
+      e2m2x2_dec((byte & 0xFu) | ((byte >> 4) << 8), x[2 * k], x[2 * k + 1]);
+    }
+  }
+}
+
+template <int DT>
+__device__ __noinline__ void decode_tail(const void* __restrict__ in, float* __restrict__ out, int64_t full,
+                                         int rem) {
+  const int64_t e0 = full * 8;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j < rem) {
+      float x;
+      if (DT == OPT_BF16) x = bf16_dec(static_cast<const uint16_t*>(in)[e0 + j]);
+      else if (DT == OPT_E4M3) x = e4m3_dec(static_cast<const uint8_t*>(in)[e0 + j]);
+      else x = e2m2_dec((static_cast<const uint8_t*>(in)[(e0 + j) >> 1] >> (4 * (j & 1))) & 0xFu);
+      out[e0 + j] = x;
+    }
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kCodecThreads, kCodecBlocksPerSM)
+decode_kernel(const void* __restrict__ in, float* __restrict__ out, int64_t n, int64_t g0) {
+  const int64_t full = n >> 3;
+  const int64_t g = g0 + (int64_t)blockIdx.x * kCodecThreads + threadIdx.x;
+  if (g < full) {
+    float x[8];
+    decode_group<DT>(in, g, x);
+    st_cs_u4(out + 8 * g, make_uint4(f2u(x[0]), f2u(x[1]), f2u(x[2]), f2u(x[3])));
+    st_cs_u4(out + 8 * g + 4, make_uint4(f2u(x[4]), f2u(x[5]), f2u(x[6]), f2u(x[7])));
+  } else if (g == full && (n & 7) != 0) {
+    decode_tail<DT>(in, out, full, (int)(n & 7));
+  }
+}
+
+// Grid: one thread per group (plus one for a ragged tail), not a persistent
+// grid -- for this pure stream, fresh CTAs that start with their loads kept
+// HBM busier than resident CTAs looping grid-stride (about 10 % more
+// bandwidth measured on GB300).  Launches of at most kMaxGrid CTAs, each
+// from a group offset, cover any n.
+constexpr int64_t kMaxGrid = (int64_t)1 << 30;
 
 template <int DT, bool SR>
-__global__ void __launch_bounds__(kCodecThreads)
-encode_kernel(const float* __restrict__ in, void* __restrict__ out, int64_t n, uint32_t seed_lo,
-              uint32_t seed_hi, uint32_t tensor, uint32_t step32) {
-  const int64_t groups = (n + 7) / 8;
-  for (int64_t gi = blockIdx.x * (int64_t)kCodecThreads + threadIdx.x; gi < groups;
-       gi += (int64_t)gridDim.x * kCodecThreads) {
-    const int64_t e0 = gi * 8;
-    const int cnt = (int)min((int64_t)8, n - e0);
-    float x[8];
-    if (cnt == 8) {
-      const uint4 a = ld_nc_u4(in + e0), b = ld_nc_u4(in + e0 + 4);
-      x[0] = u2f(a.x); x[1] = u2f(a.y); x[2] = u2f(a.z); x[3] = u2f(a.w);
-      x[4] = u2f(b.x); x[5] = u2f(b.y); x[6] = u2f(b.z); x[7] = u2f(b.w);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) x[j] = j < cnt ? in[e0 + j] : 0.0f;
-    }
-    uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    if (SR) {
-      const uint4 d0 = draw_words((uint64_t)e0 >> 2, tensor, step32, seed_lo, seed_hi);
-      const uint4 d1 = draw_words(((uint64_t)e0 >> 2) + 1, tensor, step32, seed_lo, seed_hi);
-      r[0] = d0.x >> 16; r[1] = d0.y >> 16; r[2] = d0.z >> 16; r[3] = d0.w >> 16;
-      r[4] = d1.x >> 16; r[5] = d1.y >> 16; r[6] = d1.z >> 16; r[7] = d1.w >> 16;
-    }
-    uint32_t c[8];
-    if (SR) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) c[j] = enc_sr<DT>(x[j], r[j]);
-    } else if (DT == OPT_BF16) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) c[j] = bf16_enc_rn(x[j]);
-    } else {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t pair = DT == OPT_E4M3 ? e4m3x2_rn(x[2 * k], x[2 * k + 1])
-                                             : e2m2x2_rn(x[2 * k], x[2 * k + 1]);
-        c[2 * k] = pair & 0xFFu;
-        c[2 * k + 1] = pair >> 8;
-      }
-    }
-    if (cnt == 8) {
-      if (DT == OPT_BF16)
-        st_cs_u4(static_cast<uint16_t*>(out) + e0,
-                 make_uint4(c[0] | (c[1] << 16), c[2] | (c[3] << 16), c[4] | (c[5] << 16),
-                            c[6] | (c[7] << 16)));
-      else if (DT == OPT_E4M3)
-        st_cs_u2(static_cast<uint8_t*>(out) + e0,
-                 make_uint2(c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24),
-                            c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24)));
-      else {
-        uint32_t w = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) w |= c[j] << (4 * j);
-        st_cs_u1(static_cast<uint8_t*>(out) + (e0 >> 1), w);
-      }
-    } else {
-      for (int j = 0; j < cnt; ++j) {
-        if (DT == OPT_BF16) static_cast<uint16_t*>(out)[e0 + j] = (uint16_t)c[j];
-        else if (DT == OPT_E4M3) static_cast<uint8_t*>(out)[e0 + j] = (uint8_t)c[j];
-      }
-      if (DT == OPT_E2M2)
-        for (int k = 0; 2 * k < cnt; ++k)
-          static_cast<uint8_t*>(out)[(e0 >> 1) + k] =
-              (uint8_t)(c[2 * k] | ((2 * k + 1 < cnt ? c[2 * k + 1] : 0u) << 4));
-    }
+cudaError_t launch_enc(const float* in, void* out, int64_t n, uint32_t seed_lo, uint32_t seed_hi,
+                       uint32_t tensor, uint32_t step32, cudaStream_t s) {
+  const int64_t threads = (n >> 3) + ((n & 7) ? 1 : 0);
+  for (int64_t g0 = 0; g0 < threads; g0 += kMaxGrid * kCodecThreads) {
+    const int64_t left = (threads - g0 + kCodecThreads - 1) / kCodecThreads;
+    const int grid = (int)(left < kMaxGrid ? left : kMaxGrid);
+    encode_kernel<DT, SR><<<grid, kCodecThreads, 0, s>>>(in, out, n, g0, seed_lo, seed_hi, tensor, step32);
   }
+  return cudaGetLastError();
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kCodecThreads)
-decode_kernel(const void* __restrict__ in, float* __restrict__ out, int64_t n) {
-  for (int64_t i = blockIdx.x * (int64_t)kCodecThreads + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * kCodecThreads) {
-    float x;
-    if (DT == OPT_BF16) x = bf16_dec(static_cast<const uint16_t*>(in)[i]);
-    else if (DT == OPT_E4M3) x = e4m3_dec(static_cast<const uint8_t*>(in)[i]);
-    else x = e2m2_dec((static_cast<const uint8_t*>(in)[i >> 1] >> (4 * (i & 1))) & 0xFu);
-    out[i] = x;
+cudaError_t launch_dec(const void* in, float* out, int64_t n, cudaStream_t s) {
+  const int64_t threads = (n >> 3) + ((n & 7) ? 1 : 0);
+  for (int64_t g0 = 0; g0 < threads; g0 += kMaxGrid * kCodecThreads) {
+    const int64_t left = (threads - g0 + kCodecThreads - 1) / kCodecThreads;
+    const int grid = (int)(left < kMaxGrid ? left : kMaxGrid);
+    decode_kernel<DT><<<grid, kCodecThreads, 0, s>>>(in, out, n, g0);
   }
-}
-
-int grid_for(int64_t items, int sm_count) {
-  const int64_t want = (items + kCodecThreads - 1) / kCodecThreads;
-  const int64_t cap = (int64_t)sm_count * 8;
-  return (int)(want < 1 ? 1 : (want < cap ? want : cap));
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -113,23 +201,21 @@ cudaError_t launch_encode(const float* in, void* out, int64_t n, int dtype, int 
                           uint32_t seed_lo, uint32_t seed_hi, uint32_t tensor, uint32_t step32,
                           int sm_count, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  const int grid = grid_for((n + 7) / 8, sm_count);
-#define PS_ENC(DT, SRV) encode_kernel<DT, SRV><<<grid, kCodecThreads, 0, s>>>(in, out, n, seed_lo, seed_hi, tensor, step32)
-  if (dtype == OPT_BF16) { if (stochastic) PS_ENC(OPT_BF16, true); else PS_ENC(OPT_BF16, false); }
-  else if (dtype == OPT_E4M3) { if (stochastic) PS_ENC(OPT_E4M3, true); else PS_ENC(OPT_E4M3, false); }
-  else { if (stochastic) PS_ENC(OPT_E2M2, true); else PS_ENC(OPT_E2M2, false); }
+  (void)sm_count;
+#define PS_ENC(DT, SRV) launch_enc<DT, SRV>(in, out, n, seed_lo, seed_hi, tensor, step32, s)
+  if (dtype == OPT_BF16) return stochastic ? PS_ENC(OPT_BF16, true) : PS_ENC(OPT_BF16, false);
+  if (dtype == OPT_E4M3) return stochastic ? PS_ENC(OPT_E4M3, true) : PS_ENC(OPT_E4M3, false);
+  return stochastic ? PS_ENC(OPT_E2M2, true) : PS_ENC(OPT_E2M2, false);
 #undef PS_ENC
-  return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const void* in, float* out, int64_t n, int dtype, int sm_count,
                           cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
-  const int grid = grid_for(n, sm_count);
-  if (dtype == OPT_BF16) decode_kernel<OPT_BF16><<<grid, kCodecThreads, 0, s>>>(in, out, n);
-  else if (dtype == OPT_E4M3) decode_kernel<OPT_E4M3><<<grid, kCodecThreads, 0, s>>>(in, out, n);
-  else decode_kernel<OPT_E2M2><<<grid, kCodecThreads, 0, s>>>(in, out, n);
-  return cudaGetLastError();
+  (void)sm_count;
+  if (dtype == OPT_BF16) return launch_dec<OPT_BF16>(in, out, n, s);
+  if (dtype == OPT_E4M3) return launch_dec<OPT_E4M3>(in, out, n, s);
+  return launch_dec<OPT_E2M2>(in, out, n, s);
 }
 
 }  // namespace psopt

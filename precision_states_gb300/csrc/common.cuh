@@ -217,36 +217,92 @@ __device__ __forceinline__ float e2m2_dec(uint32_t c) {
 // Decode of two E2M2 codes held in the low 4 bits of the two bytes of
 // pair16 (low byte first): as FP6 E3M2 codes (exponent field 0-3) they are
 // the E2M2 values over 4, which the hardware converts exactly to f16.
-__device__ __forceinline__ void e2m2x2_dec(uint32_t pair16, float& first, float& second) {
+// e2m2x2_dec_q returns those quarter values (callers fold the factor 4 into
+// a power-of-two scale), e2m2x2_dec the E2M2 values themselves.
+__device__ __forceinline__ void e2m2x2_dec_q(uint32_t pair16, float& first, float& second) {
   uint32_t h2;
   asm("cvt.rn.f16x2.e3m2x2 %0, %1;" : "=r"(h2) : "h"((unsigned short)pair16));
-  first = __fmul_rn(h2f((unsigned short)(h2 & 0xFFFFu)), 4.0f);
-  second = __fmul_rn(h2f((unsigned short)(h2 >> 16)), 4.0f);
+  first = h2f((unsigned short)(h2 & 0xFFFFu));
+  second = h2f((unsigned short)(h2 >> 16));
+}
+__device__ __forceinline__ void e2m2x2_dec(uint32_t pair16, float& first, float& second) {
+  e2m2x2_dec_q(pair16, first, second);
+  first = __fmul_rn(first, 4.0f);
+  second = __fmul_rn(second, 4.0f);
 }
 
-// The value handed to the converters: NaN stores 7 (the largest code),
-// negative values (and -0) store 0, values at or above 7 saturate.
-__device__ __forceinline__ float e2m2_clamp(float x) {
-  return (x != x) ? 7.0f : (x > 0.0f ? fminf(x, 7.0f) : 0.0f);
-}
+// The converters see E2M2 values over 4 (the E3M2 grid) clamped to
+// [0, 7/4]: NaN stores 7 (fminf returns its non-NaN operand), negative
+// values store 0, values at or above 7 saturate.  Callers pass x/4.
+__device__ __forceinline__ float e2m2_clamp_q(float x4) { return fmaxf(fminf(x4, 1.75f), 0.0f); }
 
 // Nearest, two values at a time: unsigned E2M2 is the FP6 E3M2 grid scaled
 // by 4 (E3M2 subnormals k/16 are E2M2's k/4 over 4; its binades with
 // exponent field 1-3 are E2M2's), so the hardware's nearest-even E3M2
 // conversion of x/4 (exact scaling), for 0 <= x <= 7, yields the E2M2 code
-// in the low bits of each byte (sign and exponent bits above are 0).  The
-// first operand lands in the upper byte.
-__device__ __forceinline__ uint32_t e2m2x2_rn(float lo, float hi) {
+// in the low bits of each byte (sign and exponent bits above are 0).
+// Arguments are the quarter values lo4 = lo/4, hi4 = hi/4; returns the pair
+// (lo | hi << 8).
+__device__ __forceinline__ uint32_t e2m2x2_rn_q(float lo4, float hi4) {
   unsigned short r;
-  asm("cvt.rn.satfinite.e3m2x2.f32 %0, %1, %2;"
-      : "=h"(r) : "f"(__fmul_rn(e2m2_clamp(hi), 0.25f)), "f"(__fmul_rn(e2m2_clamp(lo), 0.25f)));
+  asm("cvt.rn.satfinite.e3m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(e2m2_clamp_q(hi4)), "f"(e2m2_clamp_q(lo4)));
   return (uint32_t)r;
 }
 
-// Stochastic, branch-free: 7 lies on the grid, so the clamped value 7 keeps
-// its code (15) whatever the draw.
-__device__ __forceinline__ uint32_t e2m2_enc_sr(float x, uint32_t r16) {
-  return min(grid_code_sr<2, 0>(e2m2_clamp(x), r16), 15u);
+// ----------------------------------------- paired hardware encoders
+// Blackwell's converters round two fp32 values per instruction, and their
+// stochastic forms (cvt.rs, with a 32-bit operand of random bits) apply the
+// rule the software encoders above apply: a lane rounds away from zero
+// exactly when its 16 dropped bits plus its 16-bit draw carry past 2^16.
+// Lane layout: the BF16 form takes bits 31:16 for the upper result and bits
+// 15:0 for the lower; the four-lane FP8/FP6 forms were matched bit for bit
+// to the software rule (every code of 2^21 seeded values, NaN, Inf,
+// saturation, subnormals and negatives included) in their second and fourth
+// lanes only, which take bits 31:16 and 15:0 -- so the first and third lanes
+// are fed zeros and their results dropped.  Each encoder returns a pair
+// word with `lo` in the low half (16-bit codes) or the low byte (8-bit).
+// NaN inputs, rare, take the software encoders so that NaN codes stay those
+// of the codec definitions (the converters emit a canonical NaN).
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  if (__builtin_expect(lo != lo || hi != hi, 0)) d = bf16_enc_rn(lo) | (bf16_enc_rn(hi) << 16);
+  return d;
+}
+
+// rbits: bits 15:0 draw for lo, bits 31:16 for hi.
+__device__ __forceinline__ uint32_t bf16x2_sr(float lo, float hi, uint32_t rbits) {
+  uint32_t d;
+  asm("cvt.rs.bf16x2.f32 %0, %1, %2, %3;" : "=r"(d) : "f"(hi), "f"(lo), "r"(rbits));
+  if (__builtin_expect(lo != lo || hi != hi, 0))
+    d = bf16_enc_sr(lo, rbits & 0xFFFFu) | (bf16_enc_sr(hi, rbits >> 16) << 16);
+  return d;
+}
+
+template <bool SR>
+__device__ __forceinline__ uint32_t bf16x2_enc(float lo, float hi, uint32_t rbits) {
+  return SR ? bf16x2_sr(lo, hi, rbits) : bf16x2_rn(lo, hi);
+}
+
+// E4M3, stochastic, saturating: the pair (lo | hi << 8).
+__device__ __forceinline__ uint32_t e4m3x2_sr(float lo, float hi, uint32_t rbits) {
+  uint32_t d;
+  asm("cvt.rs.satfinite.e4m3x4.f32 %0, {%1, %2, %3, %4}, %5;"
+      : "=r"(d) : "f"(0.0f), "f"(hi), "f"(0.0f), "f"(lo), "r"(rbits));
+  uint32_t pair = __byte_perm(d, 0u, 0x4420);          // byte 0 (lo), byte 2 (hi)
+  if (__builtin_expect(lo != lo || hi != hi, 0))
+    pair = e4m3_enc_sr(lo, rbits & 0xFFFFu) | (e4m3_enc_sr(hi, rbits >> 16) << 8);
+  return pair;
+}
+
+// Unsigned E2M2, stochastic: the E3M2 grid of the quarter values (as in
+// e2m2x2_rn_q), after the clamp (7/4 lies on the grid, so no draw moves a
+// saturated value).  The pair (lo | hi << 8), codes 0-15.
+__device__ __forceinline__ uint32_t e2m2x2_sr_q(float lo4, float hi4, uint32_t rbits) {
+  uint32_t d;
+  asm("cvt.rs.satfinite.e3m2x4.f32 %0, {%1, %2, %3, %4}, %5;"
+      : "=r"(d) : "f"(0.0f), "f"(e2m2_clamp_q(hi4)), "f"(0.0f), "f"(e2m2_clamp_q(lo4)), "r"(rbits));
+  return __byte_perm(d, 0u, 0x4420);
 }
 
 // ------------------------------------------ arithmetic for the update term

@@ -14,7 +14,10 @@
 // order written (no FMA contraction), so m and v before write-back are
 // reproducible bit for bit.  Low-precision states are decoded exactly to fp32
 // and re-encoded with nearest or stochastic rounding, each tensor read and
-// written once ("When Small Updates Disappear", sec. 8.1).
+// written once ("When Small Updates Disappear", sec. 8.1); both directions
+// go through the hardware converters, two values per instruction (their
+// stochastic forms apply the same 16-bit carry rule as the codec
+// definitions; see the paired encoders in common.cuh).
 //
 // Layout: a persistent grid strides over the bucket's tiles of 2048 elements
 // (a finer table than the norm's chunks, so that short lists and lists of
@@ -197,18 +200,19 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
       e4m3x2_dec((k & 1) ? (f.v[k >> 1] >> 16) : (f.v[k >> 1] & 0xFFFFu), v[2 * k], v[2 * k + 1]);
   }
   if constexpr (VD == OPT_E2M2) {
-    // spread the nibbles into bytes: even elements, odd elements
+    // spread the nibbles into bytes: even elements, odd elements; decoded
+    // as quarter values (the factor 4 joins v_scale below)
     const uint32_t even = f.v[0] & 0x0F0F0F0Fu, odd = (f.v[0] >> 4) & 0x0F0F0F0Fu;
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      e2m2x2_dec(__byte_perm(even, odd, (uint32_t)k | ((uint32_t)(4 + k) << 4)), v[2 * k], v[2 * k + 1]);
+      e2m2x2_dec_q(__byte_perm(even, odd, (uint32_t)k | ((uint32_t)(4 + k) << 4)), v[2 * k], v[2 * k + 1]);
   }
-  // the update, two elements per packed instruction, in the order of the
-  // definition (each lane is one IEEE fp32 operation, no contraction)
-  // a low-precision v code holds v / v_scale (a power of two: exact)
+  // a low-precision v code holds v / v_scale (a power of two: exact; for
+  // E2M2 the decoded quarter value times 4 v_scale, also a power of two)
   if constexpr (VD != OPT_F32) {
+    const float vsc = VD == OPT_E2M2 ? __fmul_rn(td.v_scale, 4.0f) : td.v_scale;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], td.v_scale);
+    for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], vsc);
   }
   // the moments: scalar IEEE fp32 operations in the order of the definition
   // (no contraction), so the values before rounding match bit for bit
@@ -229,33 +233,38 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
     const float den = __fadd_rn(sqrt_approx(__fmul_rn(vnv[j], sc.inv_bc2)), sc.eps);
     pn[j] = __fsub_rn(__fmul_rn(u2f(f.p[j]), sc.decay), __fmul_rn(sc.lr, div_full(num, den)));
   }
-  uint32_t mcode[8], vcode[8];
-  float vs[8];   // the value the v code stores: v / v_scale, exact
+  // the value the v code stores: v / v_scale, exact (E2M2: a quarter of it,
+  // the converters' E3M2 grid, in the same one multiplication)
+  float vs[8];
+  const float vinv = VD == OPT_E2M2 ? __fmul_rn(td.v_inv_scale, 0.25f) : td.v_inv_scale;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) vs[j] = VD == OPT_F32 ? vnv[j] : __fmul_rn(vnv[j], td.v_inv_scale);
+  for (int j = 0; j < 8; ++j) vs[j] = VD == OPT_F32 ? vnv[j] : __fmul_rn(vnv[j], vinv);
+  // encode, two elements per converter instruction: pair k holds elements
+  // 2k (low half / low byte) and 2k+1.  Element j's m draw is the low half
+  // of draw word j and its v draw the high half, so the random-bits operand
+  // of pair k gathers those halves of words 2k and 2k+1.
+  uint32_t mpair[4], vpair[4];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    if constexpr (MD == OPT_BF16) mcode[j] = bf16_enc<SR>(mnv[j], SR ? (words[j] & 0xFFFFu) : 0u);
-    if constexpr (VD == OPT_F32) vcode[j] = f2u(vnv[j]);
-    else if constexpr (VD == OPT_BF16) vcode[j] = bf16_enc<SR>(vs[j], SR ? (words[j] >> 16) : 0u);
-    else if constexpr (VD == OPT_E2M2 && SR) vcode[j] = e2m2_enc_sr(vs[j], words[j] >> 16);
-    else if constexpr (VD == OPT_E4M3 && SR) vcode[j] = e4m3_enc_sr(vs[j], words[j] >> 16);
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t rm = SR ? __byte_perm(words[2 * k], words[2 * k + 1], 0x5410) : 0u;
+    const uint32_t rv = SR ? __byte_perm(words[2 * k], words[2 * k + 1], 0x7632) : 0u;
+    const float v0 = vs[2 * k], v1 = vs[2 * k + 1];
+    if constexpr (MD == OPT_BF16) mpair[k] = bf16x2_enc<SR>(mnv[2 * k], mnv[2 * k + 1], rm);
+    if constexpr (VD == OPT_BF16) vpair[k] = bf16x2_enc<SR>(v0, v1, rv);
+    if constexpr (VD == OPT_E4M3) vpair[k] = SR ? e4m3x2_sr(v0, v1, rv) : e4m3x2_rn(v0, v1);
+    if constexpr (VD == OPT_E2M2) vpair[k] = SR ? e2m2x2_sr_q(v0, v1, rv) : e2m2x2_rn_q(v0, v1);
   }
-  if constexpr ((VD == OPT_E4M3 || VD == OPT_E2M2) && !SR) {
-    // nearest: the hardware converters, two values per instruction
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t pair = VD == OPT_E4M3 ? e4m3x2_rn(vs[2 * k], vs[2 * k + 1])
-                                           : e2m2x2_rn(vs[2 * k], vs[2 * k + 1]);
-      vcode[2 * k] = pair & 0xFFu;
-      vcode[2 * k + 1] = pair >> 8;
-    }
-  }
+  // code of element j in the pair words
+  auto vcode_at = [&](int j) -> uint32_t {
+    if constexpr (VD == OPT_F32) return f2u(vnv[j]);
+    else if constexpr (VD == OPT_BF16) return (vpair[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+    else return (vpair[j >> 1] >> (8 * (j & 1))) & 0xFFu;
+  };
   uint32_t same = 0;
   if (count) {
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      same += (j < cnt && vcode[j] == (VBITS == 32 ? f.v[j] : code_at<VBITS>(f.v, j))) ? 1u : 0u;
+      same += (j < cnt && vcode_at(j) == (VBITS == 32 ? f.v[j] : code_at<VBITS>(f.v, j))) ? 1u : 0u;
   }
 
   if (cnt == 8) {
@@ -266,25 +275,22 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
       st_cs_u4(static_cast<float*>(td.m) + e0 + 4,
                make_uint4(f2u(mnv[4]), f2u(mnv[5]), f2u(mnv[6]), f2u(mnv[7])));
     } else {
-      st_cs_u4(static_cast<uint16_t*>(td.m) + e0,
-               make_uint4(mcode[0] | (mcode[1] << 16), mcode[2] | (mcode[3] << 16),
-                          mcode[4] | (mcode[5] << 16), mcode[6] | (mcode[7] << 16)));
+      st_cs_u4(static_cast<uint16_t*>(td.m) + e0, make_uint4(mpair[0], mpair[1], mpair[2], mpair[3]));
     }
     if constexpr (VD == OPT_F32) {
-      st_cs_u4(static_cast<float*>(td.v) + e0, make_uint4(vcode[0], vcode[1], vcode[2], vcode[3]));
-      st_cs_u4(static_cast<float*>(td.v) + e0 + 4, make_uint4(vcode[4], vcode[5], vcode[6], vcode[7]));
+      st_cs_u4(static_cast<float*>(td.v) + e0, make_uint4(f2u(vnv[0]), f2u(vnv[1]), f2u(vnv[2]), f2u(vnv[3])));
+      st_cs_u4(static_cast<float*>(td.v) + e0 + 4,
+               make_uint4(f2u(vnv[4]), f2u(vnv[5]), f2u(vnv[6]), f2u(vnv[7])));
     } else if constexpr (VD == OPT_BF16) {
-      st_cs_u4(static_cast<uint16_t*>(td.v) + e0,
-               make_uint4(vcode[0] | (vcode[1] << 16), vcode[2] | (vcode[3] << 16),
-                          vcode[4] | (vcode[5] << 16), vcode[6] | (vcode[7] << 16)));
+      st_cs_u4(static_cast<uint16_t*>(td.v) + e0, make_uint4(vpair[0], vpair[1], vpair[2], vpair[3]));
     } else if constexpr (VD == OPT_E4M3) {
       st_cs_u2(static_cast<uint8_t*>(td.v) + e0,
-               make_uint2(vcode[0] | (vcode[1] << 8) | (vcode[2] << 16) | (vcode[3] << 24),
-                          vcode[4] | (vcode[5] << 8) | (vcode[6] << 16) | (vcode[7] << 24)));
+               make_uint2(vpair[0] | (vpair[1] << 16), vpair[2] | (vpair[3] << 16)));
     } else {
+      // byte k: the pair's two codes as nibbles (even element low)
       uint32_t w = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) w |= vcode[j] << (4 * j);
+      for (int k = 0; k < 4; ++k) w |= ((vpair[k] | (vpair[k] >> 4)) & 0xFFu) << (8 * k);
       st_cs_u1(static_cast<uint8_t*>(td.v) + (e0 >> 1), w);
     }
     if constexpr (ALGO == ALGO_ADEMAMIX) {
@@ -298,10 +304,10 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
       const int64_t e = e0 + j;
       td.p[e] = pn[j];
       if constexpr (MD == OPT_F32) static_cast<float*>(td.m)[e] = mnv[j];
-      else static_cast<uint16_t*>(td.m)[e] = (uint16_t)mcode[j];
+      else static_cast<uint16_t*>(td.m)[e] = (uint16_t)((mpair[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
       if constexpr (VD == OPT_F32) static_cast<float*>(td.v)[e] = vnv[j];
-      else if constexpr (VD == OPT_BF16) static_cast<uint16_t*>(td.v)[e] = (uint16_t)vcode[j];
-      else if constexpr (VD == OPT_E4M3) static_cast<uint8_t*>(td.v)[e] = (uint8_t)vcode[j];
+      else if constexpr (VD == OPT_BF16) static_cast<uint16_t*>(td.v)[e] = (uint16_t)vcode_at(j);
+      else if constexpr (VD == OPT_E4M3) static_cast<uint8_t*>(td.v)[e] = (uint8_t)vcode_at(j);
       if constexpr (ALGO == ALGO_ADEMAMIX) td.m2[e] = m2n[j];
     }
     if constexpr (VD == OPT_E2M2) {
@@ -310,8 +316,8 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         if (2 * k >= cnt) break;
-        const uint32_t hi = (2 * k + 1 < cnt) ? vcode[2 * k + 1] : 0u;
-        static_cast<uint8_t*>(td.v)[(e0 >> 1) + k] = (uint8_t)(vcode[2 * k] | (hi << 4));
+        const uint32_t hi = (2 * k + 1 < cnt) ? vcode_at(2 * k + 1) : 0u;
+        static_cast<uint8_t*>(td.v)[(e0 >> 1) + k] = (uint8_t)(vcode_at(2 * k) | (hi << 4));
       }
     }
   }
