@@ -365,6 +365,13 @@ def run_ours(args, rank, local_rank, world):
 
         _, t = e2e_loop(2, t)                           # untimed: both buffers and plans warm
         torch.cuda.synchronize()
+        # the host link's own rate on this machine: one upload with nothing else running
+        u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        u0.record(copy_stream)
+        plans[0].grads_upload(host, stream=copy_stream)
+        u1.record(copy_stream)
+        torch.cuda.synchronize()
+        upload_alone_ms = u0.elapsed_time(u1)
         if pg:
             pg.barrier()
         torch.cuda.synchronize()
@@ -377,6 +384,8 @@ def run_ours(args, rank, local_rank, world):
         e2e = {"value": params_per_step * world * ke / (e_ms / 1e3) / 1e9, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 48, "steps": ke,
                "ms_per_step": round(e_ms / ke, 3), "all_norms_finite": finite,
+               "upload_alone_ms": round(upload_alone_ms, 3),
+               "h2d_gbs_alone": round(h2d / (upload_alone_ms / 1e3) / 1e9, 1),
                "note": "per step: opt_grads_upload of the step's gradients from pinned host memory (one "
                        "cudaMemcpyAsync per tensor, copy stream, double-buffered), opt_grad_norm, the step, "
                        "and a copy of the 48-byte norm result to pinned host memory"}

@@ -263,10 +263,22 @@ __device__ __forceinline__ uint32_t e2m2x2_rn_q(float lo4, float hi4) {
 // word with `lo` in the low half (16-bit codes) or the low byte (8-bit).
 // NaN inputs, rare, take the software encoders so that NaN codes stay those
 // of the codec definitions (the converters emit a canonical NaN).
+// The NaN paths, out of line: they are rare, and inlined they would hold
+// registers across the whole update.
+static __device__ __noinline__ uint32_t bf16x2_rn_soft(float lo, float hi) {
+  return bf16_enc_rn(lo) | (bf16_enc_rn(hi) << 16);
+}
+static __device__ __noinline__ uint32_t bf16x2_sr_soft(float lo, float hi, uint32_t rbits) {
+  return bf16_enc_sr(lo, rbits & 0xFFFFu) | (bf16_enc_sr(hi, rbits >> 16) << 16);
+}
+static __device__ __noinline__ uint32_t e4m3x2_sr_soft(float lo, float hi, uint32_t rbits) {
+  return e4m3_enc_sr(lo, rbits & 0xFFFFu) | (e4m3_enc_sr(hi, rbits >> 16) << 8);
+}
+
 __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
   uint32_t d;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
-  if (__builtin_expect(lo != lo || hi != hi, 0)) d = bf16_enc_rn(lo) | (bf16_enc_rn(hi) << 16);
+  if (__builtin_expect(lo != lo || hi != hi, 0)) d = bf16x2_rn_soft(lo, hi);
   return d;
 }
 
@@ -274,8 +286,7 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
 __device__ __forceinline__ uint32_t bf16x2_sr(float lo, float hi, uint32_t rbits) {
   uint32_t d;
   asm("cvt.rs.bf16x2.f32 %0, %1, %2, %3;" : "=r"(d) : "f"(hi), "f"(lo), "r"(rbits));
-  if (__builtin_expect(lo != lo || hi != hi, 0))
-    d = bf16_enc_sr(lo, rbits & 0xFFFFu) | (bf16_enc_sr(hi, rbits >> 16) << 16);
+  if (__builtin_expect(lo != lo || hi != hi, 0)) d = bf16x2_sr_soft(lo, hi, rbits);
   return d;
 }
 
@@ -290,8 +301,7 @@ __device__ __forceinline__ uint32_t e4m3x2_sr(float lo, float hi, uint32_t rbits
   asm("cvt.rs.satfinite.e4m3x4.f32 %0, {%1, %2, %3, %4}, %5;"
       : "=r"(d) : "f"(0.0f), "f"(hi), "f"(0.0f), "f"(lo), "r"(rbits));
   uint32_t pair = __byte_perm(d, 0u, 0x4420);          // byte 0 (lo), byte 2 (hi)
-  if (__builtin_expect(lo != lo || hi != hi, 0))
-    pair = e4m3_enc_sr(lo, rbits & 0xFFFFu) | (e4m3_enc_sr(hi, rbits >> 16) << 8);
+  if (__builtin_expect(lo != lo || hi != hi, 0)) pair = e4m3x2_sr_soft(lo, hi, rbits);
   return pair;
 }
 

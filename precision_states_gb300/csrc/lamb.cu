@@ -23,6 +23,7 @@ namespace psopt {
 namespace {
 
 constexpr int kLambThreads = kStepThreads;
+constexpr int kLambMinBlocks = 2;     // <= 128 registers per thread
 
 struct TileSums {
   double su, sp;   // sum of u^2 and of p^2 over the tile
@@ -36,7 +37,7 @@ __device__ __forceinline__ float lamb_dir(float mn, float vn, const opt_step_sca
 }
 
 template <int GT>
-__global__ void __launch_bounds__(kLambThreads, kStepMinBlocks)
+__global__ void __launch_bounds__(kLambThreads, kLambMinBlocks)
 lamb_stats_kernel(const StepArgs a, TileSums* __restrict__ sums) {
   float coef = 1.0f;
   if (a.d_norm != nullptr) {
@@ -138,7 +139,7 @@ lamb_ratio_kernel(const TileSums* __restrict__ sums, const int64_t* __restrict__
 }
 
 template <int GT>
-__global__ void __launch_bounds__(kLambThreads, kStepMinBlocks)
+__global__ void __launch_bounds__(kLambThreads, kLambMinBlocks)
 lamb_apply_kernel(const StepArgs a, const float* __restrict__ ratio) {
   if (a.d_norm != nullptr && a.d_norm->status != OPT_OK) return;
   const int off = threadIdx.x * 8;
