@@ -254,7 +254,7 @@ int opt_decode(const void* d_in, float* d_out, int64_t n, int32_t dtype, void* s
  * cudaMalloc, cudaFree or allocating library routine, and no host heap.  The
  * pages describe no such variant; it has no counterpart there.
  *
- * Scratch: one fixed device array inside the library (5,058,560 bytes, held
+ * Scratch: one fixed device array inside the library (4,534,272 bytes, held
  * by every GPU that loads the library until the process exits), large enough
  * for OPT_NOALLOC_MAX_TENSORS tensors and OPT_NOALLOC_MAX_CHUNKS chunks of
  * OPT_CHUNK_ELEMS elements (about 8.6e9 elements).  Larger lists are rejected

@@ -28,11 +28,11 @@ struct opt_plan {
   bool has_m2 = false;
   std::vector<void*> grad_dev;          // per tensor, for opt_grads_upload
   std::vector<int64_t> grad_bytes;
-  // one device allocation: tensors | chunks | tiles | slots | result | counter
+  // one device allocation: tensors | norm chunks | tiles | slots | result | counter
   void* d_mem = nullptr;
   int64_t d_bytes = 0;
   TensorDesc* d_tensors = nullptr;
-  opt_chunk* d_chunks = nullptr;
+  NormChunk* d_chunks = nullptr;           // the norm's chunks, addresses resolved
   opt_chunk* d_tiles = nullptr;
   NormSlot* d_slots = nullptr;
   opt_norm_result* d_result = nullptr;
@@ -180,6 +180,16 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
     P->grad_bytes[(size_t)i] = state_bytes(L->grad_dtype[i], L->numel[i]);
   }
 
+  // the norm's table: each chunk's first gradient element, resolved
+  std::vector<NormChunk> nchunks((size_t)nch);
+  for (int64_t k = 0; k < nch; ++k) {
+    const opt_chunk& c = chunks[(size_t)k];
+    const int64_t esize = L->grad_dtype[c.tensor] == OPT_BF16 ? 2 : 4;
+    nchunks[(size_t)k].ptr = static_cast<const char*>(L->grad[c.tensor]) + c.start * esize;
+    nchunks[(size_t)k].len = c.len;
+    nchunks[(size_t)k].pad = 0;
+  }
+
   if (cudaGetDevice(&P->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&P->sm_count, cudaDevAttrMultiProcessorCount, P->device) != cudaSuccess) {
     delete P;
@@ -188,7 +198,7 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
 
   const int64_t off_t = 0;
   const int64_t off_c = align_up(off_t + (int64_t)sizeof(TensorDesc) * L->n, 256);
-  const int64_t off_l = align_up(off_c + (int64_t)sizeof(opt_chunk) * nch, 256);
+  const int64_t off_l = align_up(off_c + (int64_t)sizeof(NormChunk) * nch, 256);
   const int64_t off_s = align_up(off_l + (int64_t)sizeof(opt_chunk) * ntl, 256);
   const int64_t off_r = align_up(off_s + (int64_t)sizeof(NormSlot) * 2 * OPT_NORM_SLOTS, 256);
   const int64_t off_u = align_up(off_r + (int64_t)sizeof(opt_norm_result), 256);
@@ -197,7 +207,7 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
   if (e != cudaSuccess) { delete P; return cuda_status(e); }
   char* base = static_cast<char*>(P->d_mem);
   P->d_tensors = reinterpret_cast<TensorDesc*>(base + off_t);
-  P->d_chunks = reinterpret_cast<opt_chunk*>(base + off_c);
+  P->d_chunks = reinterpret_cast<NormChunk*>(base + off_c);
   P->d_tiles = reinterpret_cast<opt_chunk*>(base + off_l);
   P->d_slots = reinterpret_cast<NormSlot*>(base + off_s);
   P->d_result = reinterpret_cast<opt_norm_result*>(base + off_r);
@@ -207,7 +217,7 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
   if (e == cudaSuccess && L->n > 0)
     e = cudaMemcpy(P->d_tensors, tds.data(), sizeof(TensorDesc) * (size_t)L->n, cudaMemcpyHostToDevice);
   if (e == cudaSuccess && nch > 0)
-    e = cudaMemcpy(P->d_chunks, chunks.data(), sizeof(opt_chunk) * (size_t)nch, cudaMemcpyHostToDevice);
+    e = cudaMemcpy(P->d_chunks, nchunks.data(), sizeof(NormChunk) * (size_t)nch, cudaMemcpyHostToDevice);
   if (e == cudaSuccess && ntl > 0)
     e = cudaMemcpy(P->d_tiles, tiles.data(), sizeof(opt_chunk) * (size_t)ntl, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) {
@@ -259,7 +269,7 @@ int opt_grad_norm(opt_plan* P, double max_norm, opt_norm_result* d_out, opt_norm
     if (first < 0) first = b;
     last = b;
     const int dt = b == 0 ? OPT_F32 : OPT_BF16;
-    e = launch_norm_partials(dt, P->d_tensors, P->d_chunks, P->bucket_begin[b], P->bucket_begin[b + 1],
+    e = launch_norm_partials(dt, P->d_chunks, P->bucket_begin[b], P->bucket_begin[b + 1],
                              P->d_slots + b * OPT_NORM_SLOTS, s);
   }
   if (e == cudaSuccess) {

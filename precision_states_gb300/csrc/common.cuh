@@ -37,6 +37,16 @@ struct NormSlot {
 };
 static_assert(sizeof(NormSlot) == 32, "NormSlot layout");
 
+// One chunk as the norm kernel reads it: the address of its first gradient
+// element (the tensor's base plus the chunk start) and its element count.
+// Resolved when the table is built, so a chunk costs one 16-byte load.
+struct NormChunk {
+  const void* ptr;
+  uint32_t len;
+  uint32_t pad;
+};
+static_assert(sizeof(NormChunk) == 16, "NormChunk layout");
+
 // Everything a step kernel needs besides the tables.
 struct StepArgs {
   const TensorDesc* tensors;

@@ -11,6 +11,7 @@ namespace psopt {
 
 struct TensorDesc;
 struct NormSlot;
+struct NormChunk;
 struct StepArgs;
 
 // state combinations (m_dtype, v_dtype) built into the library
@@ -29,8 +30,7 @@ int64_t build_table(int32_t n, const int64_t* numel, const int32_t* grad_dtype, 
                     opt_chunk* out, int64_t cap, int64_t bucket_begin[3]);
 
 // gradient norm: pass 1 for one dtype bucket into slots[0 .. OPT_NORM_SLOTS)
-cudaError_t launch_norm_partials(int grad_dtype, const TensorDesc* tensors,
-                                 const opt_chunk* chunks, int64_t chunk_begin,
+cudaError_t launch_norm_partials(int grad_dtype, const NormChunk* chunks, int64_t chunk_begin,
                                  int64_t chunk_end, NormSlot* slots, cudaStream_t s);
 // gradient norm: pass 2 over n_slots slots
 cudaError_t launch_norm_finalize(const NormSlot* slots, int n_slots, double max_norm,

@@ -43,13 +43,13 @@ constexpr int64_t align256(int64_t x) { return (x + 255) / 256 * 256; }
 constexpr int64_t kOffGrad = 0;                                            // const void*[T]
 constexpr int64_t kOffNumel = align256(kOffGrad + 8 * kMaxTensors);        // int64[T]
 constexpr int64_t kOffDtype = align256(kOffNumel + 8 * kMaxTensors);       // int32[T]
-constexpr int64_t kOffDesc = align256(kOffDtype + 4 * kMaxTensors);        // TensorDesc[T]
-constexpr int64_t kOffOrder = align256(kOffDesc + (int64_t)sizeof(TensorDesc) * kMaxTensors);  // int32[T]
+constexpr int64_t kOffOrder = align256(kOffDtype + 4 * kMaxTensors);       // int32[T]
 constexpr int64_t kOffBase = align256(kOffOrder + 4 * kMaxTensors);        // int64[T]: first chunk, in that order
-constexpr int64_t kOffChunks = align256(kOffBase + 8 * kMaxTensors);       // opt_chunk[C]
+constexpr int64_t kOffChunks = align256(kOffBase + 8 * kMaxTensors);       // NormChunk[C]
 constexpr int64_t kOffSlots = align256(kOffChunks + 16 * kMaxChunks);      // NormSlot[2 * OPT_NORM_SLOTS]
 constexpr int64_t kScratchBytes = align256(kOffSlots + 32 * 2 * OPT_NORM_SLOTS);
 
+static_assert(kScratchBytes == 4534272, "scratch size stated in opt.h");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 // Device address of g_noalloc_scratch per device, looked up once per device.
@@ -71,14 +71,12 @@ cudaError_t scratch_address(int device, unsigned char** out) {
 }
 
 // One CTA: per-tensor chunk counts, a stable bucket-major order (FP32
-// gradients first, then BF16, list order within a bucket), each tensor's
-// first chunk in that order, and the tensor descriptors.
+// gradients first, then BF16, list order within a bucket), and each
+// tensor's first chunk in that order.
 __global__ void __launch_bounds__(kPrepThreads)
 noalloc_prep_kernel(unsigned char* scratch, int n) {
-  const void* const* grad = reinterpret_cast<const void* const*>(scratch + kOffGrad);
   const int64_t* numel = reinterpret_cast<const int64_t*>(scratch + kOffNumel);
   const int32_t* dtype = reinterpret_cast<const int32_t*>(scratch + kOffDtype);
-  TensorDesc* desc = reinterpret_cast<TensorDesc*>(scratch + kOffDesc);
   int32_t* order = reinterpret_cast<int32_t*>(scratch + kOffOrder);
   int64_t* base = reinterpret_cast<int64_t*>(scratch + kOffBase);
 
@@ -119,10 +117,6 @@ noalloc_prep_kernel(unsigned char* scratch, int n) {
     const int t = t0 + k;
     if (t >= n) break;
     const int b = dtype[t] == OPT_BF16 ? 1 : 0;
-    TensorDesc d;
-    d.p = nullptr; d.g = grad[t]; d.m = nullptr; d.v = nullptr; d.m2 = nullptr; d.numel = numel[t];
-    d.v_scale = 1.0f; d.v_inv_scale = 1.0f; d.pad = 0;
-    desc[t] = d;
     order[pos[b]] = t;
     base[pos[b]] = next[b];
     pos[b] += 1;
@@ -131,12 +125,15 @@ noalloc_prep_kernel(unsigned char* scratch, int n) {
 }
 
 // One thread per chunk: find its tensor (last position whose first chunk is
-// <= c, by binary search over the bucket-major order) and write the entry.
+// <= c, by binary search over the bucket-major order) and write the entry
+// with the chunk's first gradient element resolved.
 __global__ void noalloc_fill_kernel(unsigned char* scratch, int n, int64_t total) {
+  const void* const* grad = reinterpret_cast<const void* const*>(scratch + kOffGrad);
   const int64_t* numel = reinterpret_cast<const int64_t*>(scratch + kOffNumel);
+  const int32_t* dtype = reinterpret_cast<const int32_t*>(scratch + kOffDtype);
   const int32_t* order = reinterpret_cast<const int32_t*>(scratch + kOffOrder);
   const int64_t* base = reinterpret_cast<const int64_t*>(scratch + kOffBase);
-  opt_chunk* chunks = reinterpret_cast<opt_chunk*>(scratch + kOffChunks);
+  NormChunk* chunks = reinterpret_cast<NormChunk*>(scratch + kOffChunks);
   for (int64_t c = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; c < total;
        c += (int64_t)gridDim.x * blockDim.x) {
     int lo = 0, hi = n;            // first position with base > c
@@ -148,10 +145,10 @@ __global__ void noalloc_fill_kernel(unsigned char* scratch, int n, int64_t total
     const int t = order[lo - 1];
     const int64_t start = (c - base[lo - 1]) * OPT_CHUNK_ELEMS;
     const int64_t left = numel[t] - start;
-    opt_chunk e;
-    e.tensor = (uint32_t)t;
+    NormChunk e;
+    e.ptr = static_cast<const char*>(grad[t]) + start * (dtype[t] == OPT_BF16 ? 2 : 4);
     e.len = (uint32_t)(left < OPT_CHUNK_ELEMS ? left : OPT_CHUNK_ELEMS);
-    e.start = start;
+    e.pad = 0;
     chunks[c] = e;
   }
 }
@@ -209,8 +206,7 @@ extern "C" int opt_grad_norm_noalloc(int32_t n, const int64_t* numel, const void
     if (e != cudaSuccess) return cuda_status(e);
   }
 
-  const TensorDesc* desc = reinterpret_cast<const TensorDesc*>(scratch + kOffDesc);
-  const opt_chunk* chunks = reinterpret_cast<const opt_chunk*>(scratch + kOffChunks);
+  const NormChunk* chunks = reinterpret_cast<const NormChunk*>(scratch + kOffChunks);
   NormSlot* slots = reinterpret_cast<NormSlot*>(scratch + kOffSlots);
   const int64_t begin[3] = {0, bucket[0], total};
   int first = -1, last = -1;
@@ -218,7 +214,7 @@ extern "C" int opt_grad_norm_noalloc(int32_t n, const int64_t* numel, const void
     if (begin[b + 1] <= begin[b]) continue;
     if (first < 0) first = b;
     last = b;
-    e = launch_norm_partials(b == 0 ? OPT_F32 : OPT_BF16, desc, chunks, begin[b], begin[b + 1],
+    e = launch_norm_partials(b == 0 ? OPT_F32 : OPT_BF16, chunks, begin[b], begin[b + 1],
                              slots + b * OPT_NORM_SLOTS, s);
   }
   if (e == cudaSuccess) {
