@@ -185,11 +185,10 @@ lamb_apply_kernel(const StepArgs a, const float* __restrict__ ratio) {
   }
 }
 
-// Persistent grid: CTAs resident at once (occupancy cached per kernel), at
-// most one per unit of work.
+// Persistent grid: CTAs resident at once (occupancy cached in the caller's
+// slot, one per kernel), at most one per unit of work.
 template <typename K>
-int grid_for_kernel(K k, int sm_count, int64_t work) {
-  static int cached_per_sm = 0;
+int grid_for_kernel(K k, int& cached_per_sm, int sm_count, int64_t work) {
   if (cached_per_sm == 0) {
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kLambThreads, 0) != cudaSuccess ||
@@ -208,14 +207,17 @@ cudaError_t launch_lamb(int grad_dtype, const StepArgs& a, void* sums, const int
                         int sm_count, cudaStream_t s, int phase) {
   const int64_t tiles = a.tile_end - a.tile_begin;
   TileSums* ts = static_cast<TileSums*>(sums);
+  // one occupancy slot per kernel instance
+  static int occ_stats[2] = {0, 0}, occ_apply[2] = {0, 0};
+  const int b = grad_dtype == OPT_BF16 ? 1 : 0;
   if (phase == 0) {
     if (tiles <= 0) return cudaSuccess;
-    if (grad_dtype == OPT_BF16) {
+    if (b) {
       auto k = lamb_stats_kernel<OPT_BF16>;
-      k<<<grid_for_kernel(k, sm_count, tiles), kLambThreads, 0, s>>>(a, ts);
+      k<<<grid_for_kernel(k, occ_stats[b], sm_count, tiles), kLambThreads, 0, s>>>(a, ts);
     } else {
       auto k = lamb_stats_kernel<OPT_F32>;
-      k<<<grid_for_kernel(k, sm_count, tiles), kLambThreads, 0, s>>>(a, ts);
+      k<<<grid_for_kernel(k, occ_stats[b], sm_count, tiles), kLambThreads, 0, s>>>(a, ts);
     }
   } else if (phase == 1) {
     if (n_tensors <= 0) return cudaSuccess;
@@ -224,12 +226,12 @@ cudaError_t launch_lamb(int grad_dtype, const StepArgs& a, void* sums, const int
                                                     a.d_norm, ratio);
   } else {
     if (tiles <= 0) return cudaSuccess;
-    if (grad_dtype == OPT_BF16) {
+    if (b) {
       auto k = lamb_apply_kernel<OPT_BF16>;
-      k<<<grid_for_kernel(k, sm_count, tiles), kLambThreads, 0, s>>>(a, ratio);
+      k<<<grid_for_kernel(k, occ_apply[b], sm_count, tiles), kLambThreads, 0, s>>>(a, ratio);
     } else {
       auto k = lamb_apply_kernel<OPT_F32>;
-      k<<<grid_for_kernel(k, sm_count, tiles), kLambThreads, 0, s>>>(a, ratio);
+      k<<<grid_for_kernel(k, occ_apply[b], sm_count, tiles), kLambThreads, 0, s>>>(a, ratio);
     }
   }
   return cudaGetLastError();

@@ -158,7 +158,10 @@ __device__ __forceinline__ void load_partial(const TensorDesc& td, int64_t e0, i
   for (int k = 0; k < F::NV; ++k) f.v[k] = 0u;
 #pragma unroll
   for (int k = 0; k < F::NM2; ++k) f.m2[k] = 0u;
-  for (int j = 0; j < cnt; ++j) {
+  // unrolled with an exit, so that the word arrays stay in registers
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    if (j >= cnt) break;
     const int64_t e = e0 + j;
     f.p[j] = f2u(td.p[e]);
     if constexpr (F::NG == 8) f.g[j] = f2u(static_cast<const float*>(td.g)[e]);
