@@ -392,6 +392,16 @@ def run_ours(args, rank, local_rank, world):
         plan_b.close()
         del host, grads_b
 
+    # per-step distribution (norm + step, CUDA events on the launching stream)
+    per_step = sorted(e[0].elapsed_time(e[2]) for e in evs)
+
+    def pct(q):
+        k = (len(per_step) - 1) * q
+        lo, hi = int(k), min(int(k) + 1, len(per_step) - 1)
+        return per_step[lo] + (per_step[hi] - per_step[lo]) * (k - lo)
+    per_step_stats = {"median": round(pct(0.5), 4), "p10": round(pct(0.1), 4), "p90": round(pct(0.9), 4),
+                      "min": round(per_step[0], 4), "max": round(per_step[-1], 4), "n": len(per_step)}
+
     peak, peak_src = measured_peak()
     bpp = step_bytes_per_param(w)
     step_bytes = int(bpp * params_per_step)
@@ -429,7 +439,8 @@ def run_ours(args, rank, local_rank, world):
                        "l2": "inputs larger than L2 (%.0f GB streamed per step)" % ((step_bytes + norm_bytes) / 1e9)},
             "hbm_gbs": round((step_bytes + norm_bytes) / (total_ms / args.steps / 1e3) / 1e9, 1),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-            "gpu_launches": launches_per_step * args.steps}
+            "gpu_launches": launches_per_step * args.steps,
+            "per_step_ms": per_step_stats}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg:

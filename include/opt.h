@@ -225,6 +225,16 @@ int opt_lamb_step(opt_plan* plan, const opt_hparams* hp, int64_t step, float max
  * the counter. */
 int opt_unchanged_count(opt_plan* plan, uint64_t* h_count, void* stream);
 
+/* Error flags raised by this plan's kernels since the last call, then
+ * cleared.  Bit OPT_FLAG_WAIT_TIMEOUT: a kernel gave up waiting for its own
+ * bulk copies (each wait is bounded in time, so a kernel never hangs) and
+ * left part of its tiles unprocessed -- the step's results are then
+ * incomplete.  0 means every kernel ran to completion.  Copies to host and
+ * synchronises the stream.  Returns OPT_OK, OPT_EINVAL (NULL argument) or
+ * OPT_ECUDA. */
+#define OPT_FLAG_WAIT_TIMEOUT 1
+int opt_plan_status(opt_plan* plan, int32_t* h_flags, void* stream);
+
 /* Copy each tensor's gradient from host memory (pinned for asynchrony) into
  * the plan's device gradient buffers: one cudaMemcpyAsync per tensor. */
 int opt_grads_upload(opt_plan* plan, const void* const* h_grad, void* stream);

@@ -23,6 +23,7 @@ OPT_NOALLOC_MAX_TENSORS, OPT_NOALLOC_MAX_CHUNKS = 8192, 262144
 OPT_F32, OPT_BF16, OPT_E4M3, OPT_E2M2 = 0, 1, 2, 3
 OPT_ROUND_NEAREST, OPT_ROUND_STOCHASTIC = 0, 1
 OPT_STEP_RESET_STATES = 1
+OPT_FLAG_WAIT_TIMEOUT = 1
 OPT_CHUNK_ELEMS = 32768
 OPT_NORM_SLOTS = 1216
 
@@ -81,6 +82,7 @@ _SIGS = {
     "opt_ademamix_step": (_c.c_int, [_vp, _c.POINTER(opt_hparams), _c.c_int64, _vp, _vp]),
     "opt_lamb_step": (_c.c_int, [_vp, _c.POINTER(opt_hparams), _c.c_int64, _c.c_float, _vp, _vp]),
     "opt_unchanged_count": (_c.c_int, [_vp, _c.POINTER(_c.c_uint64), _vp]),
+    "opt_plan_status": (_c.c_int, [_vp, _c.POINTER(_c.c_int32), _vp]),
     "opt_grads_upload": (_c.c_int, [_vp, _c.POINTER(_vp), _vp]),
     "opt_encode": (_c.c_int, [_vp, _vp, _c.c_int64, _c.c_int32, _c.c_int32, _c.c_uint64,
                               _c.c_uint32, _c.c_int64, _vp]),
@@ -277,6 +279,12 @@ class Plan:
         out = _c.c_uint64()
         _check(lib().opt_unchanged_count(self.handle, _c.byref(out), _stream_ptr(stream)),
                "opt_unchanged_count")
+        return out.value
+
+    def status(self, stream=None) -> int:
+        """Kernel error flags since the last call (0: all ran to completion)."""
+        out = _c.c_int32()
+        _check(lib().opt_plan_status(self.handle, _c.byref(out), _stream_ptr(stream)), "opt_plan_status")
         return out.value
 
     def grads_upload(self, host_grads, stream=None):

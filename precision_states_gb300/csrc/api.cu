@@ -28,7 +28,7 @@ struct opt_plan {
   bool has_m2 = false;
   std::vector<void*> grad_dev;          // per tensor, for opt_grads_upload
   std::vector<int64_t> grad_bytes;
-  // one device allocation: tensors | norm chunks | tiles | slots | result | counter
+  // one device allocation: tensors | norm chunks | tiles | slots | result | counter | flags
   void* d_mem = nullptr;
   int64_t d_bytes = 0;
   TensorDesc* d_tensors = nullptr;
@@ -37,6 +37,7 @@ struct opt_plan {
   NormSlot* d_slots = nullptr;
   opt_norm_result* d_result = nullptr;
   unsigned long long* d_unchanged = nullptr;
+  int* d_err = nullptr;                    // kernel error flags (opt_plan_status)
   // update-norm clipping (LAMB) workspace, allocated on first use
   std::vector<int64_t> tile_first, tile_count;   // per tensor, in the tile table
   void* d_lamb = nullptr;
@@ -202,7 +203,8 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
   const int64_t off_s = align_up(off_l + (int64_t)sizeof(opt_chunk) * ntl, 256);
   const int64_t off_r = align_up(off_s + (int64_t)sizeof(NormSlot) * 2 * OPT_NORM_SLOTS, 256);
   const int64_t off_u = align_up(off_r + (int64_t)sizeof(opt_norm_result), 256);
-  P->d_bytes = align_up(off_u + 8, 256);
+  const int64_t off_e = off_u + 8;
+  P->d_bytes = align_up(off_e + 8, 256);
   cudaError_t e = cudaMalloc(&P->d_mem, (size_t)P->d_bytes);
   if (e != cudaSuccess) { delete P; return cuda_status(e); }
   char* base = static_cast<char*>(P->d_mem);
@@ -212,6 +214,7 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
   P->d_slots = reinterpret_cast<NormSlot*>(base + off_s);
   P->d_result = reinterpret_cast<opt_norm_result*>(base + off_r);
   P->d_unchanged = reinterpret_cast<unsigned long long*>(base + off_u);
+  P->d_err = reinterpret_cast<int*>(base + off_e);
 
   e = cudaMemset(P->d_mem, 0, (size_t)P->d_bytes);
   if (e == cudaSuccess && L->n > 0)
@@ -309,6 +312,7 @@ static int do_step(opt_plan* P, const opt_hparams* hp, int64_t step, const opt_n
   a.d_norm = d_norm;
   a.unchanged = hp->count_unchanged ? P->d_unchanged : nullptr;
   a.reset = (hp->flags & OPT_STEP_RESET_STATES) ? 1 : 0;
+  a.err = P->d_err;
 
   DeviceGuard g(P->device);
   if (!g.ok) return OPT_ECUDA;
@@ -339,6 +343,7 @@ int opt_lamb_step(opt_plan* P, const opt_hparams* hp, int64_t step, float max_un
   a.tensors = P->d_tensors;
   a.tiles = P->d_tiles;
   a.d_norm = d_norm;
+  a.err = P->d_err;
   DeviceGuard g(P->device);
   if (!g.ok) return OPT_ECUDA;
   cudaError_t e = cudaSuccess;
@@ -394,6 +399,20 @@ int opt_unchanged_count(opt_plan* P, uint64_t* h_count, void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_status(e);
   *h_count = v;
+  return OPT_OK;
+}
+
+int opt_plan_status(opt_plan* P, int32_t* h_flags, void* stream) {
+  if (P == nullptr || h_flags == nullptr) return OPT_EINVAL;
+  DeviceGuard g(P->device);
+  if (!g.ok) return OPT_ECUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, P->d_err, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(P->d_err, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_status(e);
+  *h_flags = v;
   return OPT_OK;
 }
 

@@ -57,6 +57,7 @@ struct StepArgs {
   const opt_norm_result* d_norm;      // NULL: no clipping
   unsigned long long* unchanged;      // NULL: do not count
   int reset;                          // nonzero: start from zero moments
+  int* err;                           // kernel error flags (bit 0: a bounded wait ran out)
 };
 
 // ------------------------------------------------------------- bit views

@@ -56,11 +56,14 @@ constexpr int kStepThreads = 256;
 // - Grid: persistent (as many CTAs as are resident) except for AdEMAMix,
 //   whose five fp32 streams ran faster with one CTA per tile (0.993 against
 //   0.944 of measured).
+// - Staging: the stochastic-rounding low-precision instantiations take their
+//   input tiles through shared memory by bulk copies (step_bulk.cuh).
 template <int GT, int COMBO, int ALGO, bool SR>
 struct StepShape {
   static constexpr int kMinBlocks =
       (GT == OPT_BF16 && !SR && (COMBO == SC_BF16_E4M3 || COMBO == SC_BF16_E2M2)) ? 3 : 2;
   static constexpr bool kPersistent = ALGO != ALGO_ADEMAMIX;
+  static constexpr bool kBulk = COMBO != SC_F32 && ALGO == ALGO_ADAMW && SR;
 };
 
 template <int COMBO>

@@ -148,6 +148,7 @@ def run_lockstep(w, steps, tol, samples=None, rounding="nearest", seed=0, hp_see
             orc.compare(gpu, tol, sr)
     torch.cuda.synchronize()
     orc.compare(gpu, tol, sr)
+    assert gpu.plan.status() == 0, "a kernel reported a bounded wait that ran out"
     return gpu, orc, counts
 
 

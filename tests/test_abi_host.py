@@ -191,3 +191,10 @@ def test_plan_create_rejects_bad_v_scale(scale):
     tl.v_scale = sc
     h = ctypes.c_void_p()
     assert ps.lib().opt_plan_create(ctypes.byref(tl), ctypes.byref(h)) == ps.OPT_EINVAL
+
+
+def test_plan_status_null_arguments():
+    L = ps.lib()
+    out = ctypes.c_int32()
+    assert L.opt_plan_status(None, ctypes.byref(out), None) == ps.OPT_EINVAL
+    assert ps.OPT_FLAG_WAIT_TIMEOUT == 1
