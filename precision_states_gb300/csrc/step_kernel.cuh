@@ -56,14 +56,18 @@ constexpr int kStepThreads = 256;
 // - Grid: persistent (as many CTAs as are resident) except for AdEMAMix,
 //   whose five fp32 streams ran faster with one CTA per tile (0.993 against
 //   0.944 of measured).
-// - Staging: the stochastic-rounding low-precision instantiations take their
-//   input tiles through shared memory by bulk copies (step_bulk.cuh).
+// - Staging: the low-precision AdamW instantiations with stochastic rounding,
+//   and BF16 v with nearest rounding, take their input tiles through shared
+//   memory from a producer warp's bulk copies (step_bulk.cuh): 0.956 / 0.917
+//   / 0.869 -> 0.980 / 0.970 / 0.948 (stochastic BF16 / E4M3 / E2M2 v) and
+//   0.964 -> 0.989 (nearest BF16 v).  Nearest E4M3 and E2M2 stay on the
+//   3-CTA register pipeline, which measured equal or better.
 template <int GT, int COMBO, int ALGO, bool SR>
 struct StepShape {
   static constexpr int kMinBlocks =
       (GT == OPT_BF16 && !SR && (COMBO == SC_BF16_E4M3 || COMBO == SC_BF16_E2M2)) ? 3 : 2;
   static constexpr bool kPersistent = ALGO != ALGO_ADEMAMIX;
-  static constexpr bool kBulk = COMBO != SC_F32 && ALGO == ALGO_ADAMW && SR;
+  static constexpr bool kBulk = COMBO != SC_F32 && ALGO == ALGO_ADAMW && (SR || COMBO == SC_BF16_BF16);
 };
 
 template <int COMBO>
