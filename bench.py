@@ -11,8 +11,10 @@ algorithmic bytes / its CUDA-event time) against the measured copy bandwidth;
 ``cpu_baseline`` is the CPU oracle timed on a bounded sample.
 
 Multi-GPU: one process per GPU under torchrun, each an independent replica
-over its own copy of the list (the step shards with no data-path exchange;
-see the design doc); value = all ranks' parameters / max-over-ranks time.
+over its own copy of the list (the step is elementwise per tensor, so a
+sharded list needs no data-path exchange; the only cross-rank quantity, the
+norm, combines on the host with opt_norm_combine); value = all ranks'
+parameters / max-over-ranks time.
 
 ``--impl reference`` times the CPU oracle instead (bounded sample per step).
 """
@@ -88,7 +90,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")   # run output folder
 
     def start(self):
         try:

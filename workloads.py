@@ -6,8 +6,8 @@ states); it holds none of the optimizer's arithmetic.  Both the CUDA library
 here, so the two always see the same bytes.  torch's seeded generators are
 used on either device; a given (seed, device) always yields the same inputs.
 
-Workloads (sizes and distributions follow the configurations the pages'
-measurements are stood in for):
+Workloads (sizes and distributions follow the configurations that stand in
+for the pages' measurements):
 
 * ``adamw_1m``      one fp32 tensor of 1,048,576, fp32 grads N(0,1) fresh each
                     step, lr = wd = 0.1, 10 steps, no clipping.
