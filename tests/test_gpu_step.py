@@ -259,3 +259,24 @@ def test_lamb_rejects_low_precision_states():
     with pytest.raises(ps.OptError) as e:
         gpu.plan.lamb_step(ps.hparams(), 1, 1.0)
     assert e.value.status == ps.OPT_EUNSUPPORTED
+
+
+@pytest.mark.parametrize("v_dtype", ["f32", "bf16", "e4m3", "e2m2"])
+def test_mixed_grad_dtypes_and_empty_tensors(v_dtype):
+    """One plan over a list that mixes BF16 and FP32 gradients (two dtype
+    buckets, one launch each) and holds zero-size and one-element tensors:
+    three clipped steps with stochastic rounding, every value and code against
+    the oracle.  Covers both step kernels (register-pipelined and staged) on
+    both buckets, full and short tiles."""
+    sizes = [4096, 0, 1, 2048 * 3 + 17, 5, 0, 8192, 333, 2048]
+    m_dtype = "f32" if v_dtype == "f32" else "bf16"
+    w = W.Workload("mixed", sizes, "bf16", m_dtype=m_dtype, v_dtype=v_dtype, steps=3, max_norm=1.0,
+                   p_std=0.02, grad_std=1.0, hp=dict(lr=1e-2, weight_decay=0.1))
+    gpu = GpuSide(w, seed=5)
+    for i in (1, 2, 6, 7):
+        gpu.grads[i] = torch.empty(sizes[i], dtype=torch.float32, device="cuda")
+    gpu.plan.close()
+    gpu.plan = ps.Plan(gpu.params, gpu.grads, gpu.m, gpu.v, m_dtype=m_dtype, v_dtype=v_dtype)
+    _, _, counts = run_lockstep(w, 3, 1e-6, rounding="stochastic", count=v_dtype != "f32", gpu=gpu)
+    for got, want in counts:
+        assert got == want
