@@ -142,8 +142,10 @@ def test_scaled_v_codes(v_dtype, rounding):
     assert all(got == want for got, want in counts)
 
 
-@pytest.mark.parametrize("v_dtype", ["f32", "bf16", "e2m2"])
-def test_reset_step_starts_from_zero_states(v_dtype):
+@pytest.mark.parametrize("v_dtype,rounding", [("f32", "nearest"), ("bf16", "nearest"), ("e2m2", "nearest"),
+                                              ("bf16", "stochastic"), ("e4m3", "stochastic"),
+                                              ("e2m2", "stochastic")])
+def test_reset_step_starts_from_zero_states(v_dtype, rounding):
     """"When Small Updates Disappear" sec. 5: a reset step starts from zero
     moments.  It must equal (bitwise) a step at t = 1 after zeroing the
     states by hand, and match the oracle run from zeroed states."""
@@ -151,7 +153,8 @@ def test_reset_step_starts_from_zero_states(v_dtype):
     w = W.workload("sweep", m_dtype=md, v_dtype=v_dtype, hp=dict(lr=1e-2, weight_decay=0.1))
     w.max_norm = 0.0
     a, b = GpuSide(w, seed=4), GpuSide(w, seed=4)
-    ghp, ohp = hp_for(w)
+    sr = rounding == "stochastic"
+    ghp, ohp = hp_for(w, rounding=rounding)
     for t in (1, 2, 3):                       # both accumulate the same states
         for side in (a, b):
             W.fill_grads(w, side.grads, t, 4)
@@ -163,7 +166,7 @@ def test_reset_step_starts_from_zero_states(v_dtype):
     for x in b.m + b.v:
         x.zero_()
     b.step(1, ghp, clip=False)
-    rhp = hp_for(w)[0]
+    rhp = hp_for(w, rounding=rounding)[0]
     rhp.flags = ps.OPT_STEP_RESET_STATES
     a.step(1, rhp, clip=False)
     torch.cuda.synchronize()
@@ -172,8 +175,9 @@ def test_reset_step_starts_from_zero_states(v_dtype):
     for k in range(len(orc.samples)):
         orc.m[k][...] = 0
         orc.v[k][...] = 0
-    orc.step(1, g_np, ohp, 1.0, False, 77)
-    orc.compare(a, 1e-6, False)
+    orc.step(1, g_np, ohp, 1.0, sr, 1234)
+    orc.compare(a, 1e-6, sr)
+    assert a.plan.status() == 0 and b.plan.status() == 0
 
 
 def test_invalid_flags_and_scales():
