@@ -336,20 +336,34 @@ def run_ours(args, rank, local_rank, world):
         step_done = [torch.cuda.Event(), torch.cuda.Event()]
         h2d = sum(g.numel() * g.element_size() for g in grads)
 
+        def timing_event():
+            return torch.cuda.Event(enable_timing=True)
+
         def e2e_loop(nsteps, t):
-            """nsteps uploads + norms + steps; returns (elapsed ms, last step)."""
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            """nsteps uploads + norms + steps; returns (elapsed ms, last step,
+            mean upload ms, mean compute ms), the means from events around
+            each upload (copy stream) and each norm + step (compute stream)."""
+            e0, e1 = timing_event(), timing_event()
+            ups, comps = [], []
             e0.record(stream)
             copy_stream.wait_event(e0)
+            u = (timing_event(), timing_event())
+            u[0].record(copy_stream)
             plans[0].grads_upload(host, stream=copy_stream)
+            u[1].record(copy_stream)
+            ups.append(u)
             up_done[0].record(copy_stream)
             for k in range(nsteps):
                 b = k % 2
                 stream.wait_event(up_done[b])
                 t += 1
                 d_res = res_dev[k].data_ptr()
+                c = (timing_event(), timing_event())
+                c[0].record(stream)
                 plans[b].grad_norm(w.max_norm, d_out=d_res, sync=False, stream=stream)
                 steps_of[b](hp, t, d_res if clip else None, stream=stream)
+                c[1].record(stream)
+                comps.append(c)
                 res_host[k].copy_(res_dev[k], non_blocking=True)             # D2H of the result
                 step_done[b].record(stream)
                 # prefetch the next step's gradients into the other buffer once
@@ -359,13 +373,18 @@ def run_ours(args, rank, local_rank, world):
                 if k + 1 < nsteps:
                     if k >= 1:
                         copy_stream.wait_event(step_done[1 - b])
+                    u = (timing_event(), timing_event())
+                    u[0].record(copy_stream)
                     plans[1 - b].grads_upload(host, stream=copy_stream)
+                    u[1].record(copy_stream)
+                    ups.append(u)
                     up_done[1 - b].record(copy_stream)
             e1.record(stream)
             torch.cuda.synchronize()
-            return e0.elapsed_time(e1), t
+            mean = lambda pairs: sum(x.elapsed_time(y) for x, y in pairs) / max(len(pairs), 1)
+            return e0.elapsed_time(e1), t, mean(ups), mean(comps)
 
-        _, t = e2e_loop(2, t)                           # untimed: both buffers and plans warm
+        _, t, _, _ = e2e_loop(2, t)                     # untimed: both buffers and plans warm
         torch.cuda.synchronize()
         # the host link's own rate on this machine: one upload with nothing else running
         u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -377,7 +396,7 @@ def run_ours(args, rank, local_rank, world):
         if pg:
             pg.barrier()
         torch.cuda.synchronize()
-        e_ms, t = e2e_loop(ke, t)
+        e_ms, t, upload_ms, compute_ms = e2e_loop(ke, t)
         finite = all(int(res_host[k].view(torch.int32)[11]) == 0 for k in range(ke))
         if pg:
             tt = torch.tensor([e_ms], device=dev)
@@ -388,6 +407,8 @@ def run_ours(args, rank, local_rank, world):
                "ms_per_step": round(e_ms / ke, 3), "all_norms_finite": finite,
                "upload_alone_ms": round(upload_alone_ms, 3),
                "h2d_gbs_alone": round(h2d / (upload_alone_ms / 1e3) / 1e9, 1),
+               "upload_ms_in_loop": round(upload_ms, 3), "compute_ms_in_loop": round(compute_ms, 3),
+               "h2d_gbs_in_loop": round(h2d / (upload_ms / 1e3) / 1e9, 1),
                "note": "per step: opt_grads_upload of the step's gradients from pinned host memory (one "
                        "cudaMemcpyAsync per tensor, copy stream, double-buffered), opt_grad_norm, the step, "
                        "and a copy of the 48-byte norm result to pinned host memory"}
