@@ -144,11 +144,6 @@ __device__ __forceinline__ uint32_t bf16_enc_sr(float x, uint32_t r16) {
   return (w + r16) >> 16;
 }
 
-template <bool SR>
-__device__ __forceinline__ uint32_t bf16_enc(float x, uint32_t r16) {
-  return SR ? bf16_enc_sr(x, r16) : bf16_enc_rn(x);
-}
-
 // ------------------------------------------------- small-grid rounding core
 // Stochastic rounding of a (finite, 0 <= a below the grid's largest value)
 // onto a grid with P fraction bits whose binades start at 2^EMIN (constant
