@@ -310,7 +310,11 @@ typedef struct opt_chunk {
 int64_t opt_chunk_table(int32_t n, const int64_t* numel, const int32_t* grad_dtype,
                         opt_chunk* out, int64_t cap, int64_t bucket_begin[3]);
 
-/* Per-step scalars, formed in double and rounded once to fp32. */
+/* Per-step scalars, formed in double and rounded once to fp32.  Returns
+ * OPT_EINVAL for step < 1 or hyperparameters outside the ranges
+ * torch.optim.AdamW accepts (0 <= beta1, beta2 < 1; 0 <= beta3 <= 1;
+ * lr, eps, weight_decay >= 0; all finite).  Every step entry point applies
+ * the same check before any launch. */
 typedef struct opt_step_scalars {
   float lr, decay;            /* decay = 1 - lr wd */
   float beta1, omb1;          /* omb = 1 - beta */

@@ -76,6 +76,13 @@ int opt_step_scalars_compute(const opt_hparams* hp, int64_t step, opt_step_scala
   if (hp == nullptr || out == nullptr || step < 1) return OPT_EINVAL;
   const double lr = hp->lr, wd = hp->weight_decay;
   const double b1 = hp->beta1, b2 = hp->beta2, b3 = hp->beta3;
+  // the ranges torch.optim.AdamW accepts, and finite: beta1, beta2 < 1 keep
+  // the bias corrections 1 - beta^t positive; beta3 = 1 freezes m2
+  const double vals[7] = {lr, wd, b1, b2, b3, (double)hp->alpha, (double)hp->eps};
+  for (double x : vals)
+    if (!std::isfinite(x)) return OPT_EINVAL;
+  if (lr < 0.0 || wd < 0.0 || hp->eps < 0.0f) return OPT_EINVAL;
+  if (!(b1 >= 0.0 && b1 < 1.0) || !(b2 >= 0.0 && b2 < 1.0) || !(b3 >= 0.0 && b3 <= 1.0)) return OPT_EINVAL;
   out->lr = hp->lr;
   out->decay = (float)(1.0 - lr * wd);
   out->beta1 = hp->beta1;

@@ -198,3 +198,24 @@ def test_plan_status_null_arguments():
     out = ctypes.c_int32()
     assert L.opt_plan_status(None, ctypes.byref(out), None) == ps.OPT_EINVAL
     assert ps.OPT_FLAG_WAIT_TIMEOUT == 1
+
+
+@pytest.mark.parametrize("field,value", [
+    ("beta1", 1.0), ("beta1", -0.1), ("beta2", 1.0), ("beta3", 1.5), ("lr", -1e-3), ("eps", -1e-8),
+    ("weight_decay", -0.1), ("lr", float("nan")), ("alpha", float("inf")), ("beta2", float("nan")),
+])
+def test_step_scalars_reject_out_of_range_hparams(field, value):
+    """The ranges torch.optim.AdamW accepts, and finite."""
+    hp = ps.hparams()
+    setattr(hp, field, value)
+    with pytest.raises(ps.OptError) as e:
+        ps.opt_step_scalars_compute(hp, 1)
+    assert e.value.status == ps.OPT_EINVAL
+    L = ps.lib()
+    assert L.opt_adamw_step(None, ctypes.byref(hp), 1, None, None) == ps.OPT_EINVAL
+
+
+def test_step_scalars_accept_edge_hparams():
+    hp = ps.hparams(lr=0.0, eps=0.0, weight_decay=0.0, beta1=0.0, beta2=0.0, beta3=1.0)
+    s = ps.opt_step_scalars_compute(hp, 3)
+    assert s["omb3"] == 0.0 and s["inv_bc1"] == 1.0 and s["inv_bc2"] == 1.0
