@@ -2,6 +2,7 @@
 // kernel launch files.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -13,6 +14,30 @@ struct TensorDesc;
 struct NormSlot;
 struct NormChunk;
 struct StepArgs;
+
+// Resident CTAs per SM of one kernel, cached per device and safe to fill
+// from several host threads.  The value is a property of the kernel and the
+// architecture, but a dynamic shared-memory size above the default has to be
+// enabled on each device, so the first launch on a device does that too.
+constexpr int kMaxDevices = 64;
+struct OccupancyCache {
+  std::atomic<int> per_sm[kMaxDevices];
+};
+
+template <typename K>
+inline int cached_occupancy(K kernel, OccupancyCache& cache, int threads, int smem_bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = -1;
+  int v = dev >= 0 ? cache.per_sm[dev].load(std::memory_order_relaxed) : 0;
+  if (v > 0) return v;
+  if (smem_bytes > 48 * 1024 &&
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess)
+    return 0;      // the launch reports the error
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kernel, threads, smem_bytes) != cudaSuccess || v < 1)
+    v = 1;
+  if (dev >= 0) cache.per_sm[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
 
 // state combinations (m_dtype, v_dtype) built into the library
 enum StateCombo { SC_F32 = 0, SC_BF16_BF16 = 1, SC_BF16_E4M3 = 2, SC_BF16_E2M2 = 3 };

@@ -185,18 +185,11 @@ lamb_apply_kernel(const StepArgs a, const float* __restrict__ ratio) {
   }
 }
 
-// Persistent grid: CTAs resident at once (occupancy cached in the caller's
-// slot, one per kernel), at most one per unit of work.
+// Persistent grid: CTAs resident at once (occupancy cached per kernel
+// instance and device), at most one per unit of work.
 template <typename K>
-int grid_for_kernel(K k, int& cached_per_sm, int sm_count, int64_t work) {
-  if (cached_per_sm == 0) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kLambThreads, 0) != cudaSuccess ||
-        per_sm < 1)
-      per_sm = 1;
-    cached_per_sm = per_sm;
-  }
-  const int64_t full = (int64_t)cached_per_sm * sm_count;
+int grid_for_kernel(K k, OccupancyCache& occ, int sm_count, int64_t work) {
+  const int64_t full = (int64_t)cached_occupancy(k, occ, kLambThreads, 0) * sm_count;
   return (int)(work < full ? work : full);
 }
 
@@ -208,7 +201,7 @@ cudaError_t launch_lamb(int grad_dtype, const StepArgs& a, void* sums, const int
   const int64_t tiles = a.tile_end - a.tile_begin;
   TileSums* ts = static_cast<TileSums*>(sums);
   // one occupancy slot per kernel instance
-  static int occ_stats[2] = {0, 0}, occ_apply[2] = {0, 0};
+  static OccupancyCache occ_stats[2], occ_apply[2];
   const int b = grad_dtype == OPT_BF16 ? 1 : 0;
   if (phase == 0) {
     if (tiles <= 0) return cudaSuccess;

@@ -257,17 +257,10 @@ cudaError_t launch_bulk(const StepArgs& a, int sm_count, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;
   auto k = step_bulk_kernel<GT, COMBO, SR>;
   constexpr int bytes = BulkLayout<GT, COMBO>::BYTES;
-  static int cached_per_sm = 0;
-  if (cached_per_sm == 0) {
-    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
-      return cudaGetLastError();
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kBulkThreads, bytes) != cudaSuccess ||
-        per_sm < 1)
-      per_sm = 1;
-    cached_per_sm = per_sm;
-  }
-  const int64_t full = (int64_t)cached_per_sm * sm_count;
+  static OccupancyCache occ;
+  const int per_sm = cached_occupancy(k, occ, kBulkThreads, bytes);
+  if (per_sm < 1) return cudaGetLastError();
+  const int64_t full = (int64_t)per_sm * sm_count;
   const int grid = (int)(n < full ? n : full);
   k<<<grid, kBulkThreads, bytes, s>>>(a);
   return cudaGetLastError();

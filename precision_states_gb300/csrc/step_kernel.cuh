@@ -434,16 +434,10 @@ cudaError_t launch_one(const StepArgs& a, int sm_count, cudaStream_t s) {
   const int64_t n = a.tile_end - a.tile_begin;
   if (n <= 0) return cudaSuccess;
   auto k = step_kernel<GT, COMBO, ALGO, SR>;
-  static int cached_per_sm = 0;
-  if (cached_per_sm == 0) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kStepThreads, 0) != cudaSuccess ||
-        per_sm < 1)
-      per_sm = 1;
-    cached_per_sm = per_sm;
-  }
+  static OccupancyCache occ;
+  const int per_sm = cached_occupancy(k, occ, kStepThreads, 0);
   constexpr int64_t kMaxGrid = 0x7FFFFFFF;
-  const int64_t full = StepShape<GT, COMBO, ALGO, SR>::kPersistent ? (int64_t)cached_per_sm * sm_count : kMaxGrid;
+  const int64_t full = StepShape<GT, COMBO, ALGO, SR>::kPersistent ? (int64_t)per_sm * sm_count : kMaxGrid;
   const int grid = (int)(n < full ? n : full);
   k<<<grid, kStepThreads, 0, s>>>(a);
   return cudaGetLastError();
