@@ -14,7 +14,7 @@ Parity pins (tests/test_oracle_*.py): codecs against torch casts, brute force
 and the carry rule of "When Small Updates Disappear" sec. 6.1; the norm
 against exact rational arithmetic; the step against the one-step closed form
 of bitsandbytes PR #2040 and against torch.optim.AdamW in float64; Philox
-against its published known-answer vector.
+against the independent host-side Philox4_32_10 generator of cuRAND.
 """
 from __future__ import annotations
 

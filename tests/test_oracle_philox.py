@@ -1,25 +1,59 @@
 """Pins for the oracle's Philox4x32-10 generator and its draw layout.
 
 The generator follows Salmon et al., "Parallel Random Numbers: As Easy as
-1, 2, 3" (SC'11), sec. 3.  Its pins are the known-answer vectors published
-with that paper's reference implementation (zero counter and key, all-ones,
-and the pi-digits vector) -- three independent 128-bit answers that a wrong
-multiplier, Weyl constant, word order or round count cannot all reproduce."""
+1, 2, 3" (SC'11), sec. 3.  It is pinned against an independent
+implementation: the host-side Philox4_32_10 generator of the cuRAND library
+in the CUDA toolkit, which runs on the CPU.  That generator's output stream
+is laid out in blocks of four words; block b is the generator's output for
+counter (b // 65536 low, b // 65536 high, b mod 65536, 0) under the key
+(seed low, seed high) -- so comparisons at chosen offsets check the round
+function, both multipliers, the key schedule, the output word order and
+counter words x, y and z.  (Word w enters the rounds as word y does; the
+draw tests below check that it changes the draws.)"""
+import ctypes
+import os
+
 import numpy as np
+import pytest
 
 import oracle
 
-KAT = [
-    ((0, 0, 0, 0), (0, 0), (0x6627E8D5, 0xE169C58D, 0xBC57AC4C, 0x9B00DBD8)),
-    ((0xFFFFFFFF,) * 4, (0xFFFFFFFF,) * 2, (0x408F276D, 0x41C83B0E, 0xA20BC7C6, 0x6D5451FD)),
-    ((0x243F6A88, 0x85A308D3, 0x13198A2E, 0x03707344), (0xA4093822, 0x299F31D0),
-     (0xD16CFE09, 0x94FDCCEB, 0x5001E420, 0x24126EA1)),
-]
+_CURAND_PATHS = ["/usr/local/cuda/lib64/libcurand.so", "libcurand.so", "libcurand.so.10"]
+_PHILOX4_32_10 = 161          # curandRngType_t of the Philox4x32-10 generator
 
 
-def test_philox_known_answers():
-    for ctr, key, want in KAT:
-        assert oracle.philox4x32_10(ctr, key) == want
+def _curand():
+    for path in _CURAND_PATHS:
+        try:
+            return ctypes.CDLL(path)
+        except OSError:
+            continue
+    pytest.skip("cuRAND library not found")
+
+
+def curand_block(lib, seed: int, block: int):
+    """The four words of block `block` of cuRAND's host Philox stream."""
+    gen = ctypes.c_void_p()
+    assert lib.curandCreateGeneratorHost(ctypes.byref(gen), _PHILOX4_32_10) == 0
+    try:
+        assert lib.curandSetPseudoRandomGeneratorSeed(gen, ctypes.c_ulonglong(seed)) == 0
+        assert lib.curandSetGeneratorOffset(gen, ctypes.c_ulonglong(4 * block)) == 0
+        out = (ctypes.c_uint32 * 4)()
+        assert lib.curandGenerate(gen, out, ctypes.c_size_t(4)) == 0
+        return tuple(out)
+    finally:
+        lib.curandDestroyGenerator(gen)
+
+
+@pytest.mark.parametrize("seed", [0, 7, 0x0123456789ABCDEF, 0xFFFFFFFFFFFFFFFF])
+def test_philox_matches_curand(seed):
+    lib = _curand()
+    key = (seed & 0xFFFFFFFF, seed >> 32)
+    for block in (0, 1, 5000, 65535, 65536, 70000, (1 << 20) + 7, (1 << 48) + 65536 * 3 + 11,
+                  (1 << 50) + 9, (1 << 60) + (1 << 34) + 12345):
+        j, s = divmod(block, 65536)
+        ctr = (j & 0xFFFFFFFF, j >> 32, s, 0)
+        assert oracle.philox4x32_10(ctr, key) == curand_block(lib, seed, block), (hex(seed), block)
 
 
 def test_draws_layout_element_tied():
