@@ -184,11 +184,12 @@ int opt_plan_info(const opt_plan* plan, int64_t* n_chunks, int64_t* total_numel,
 
 /* Global gradient norm over every tensor of the plan ("perf(training): fused
  * multi-tensor gradient-norm reduction", 'Correctness properties').  One
- * partial-sum launch per gradient dtype into fixed slots, then one finishing
- * launch; bit-identical run to run for the same inputs and plan.  Writes the
- * result to d_out (device, 48 bytes, may be NULL to use the plan's own
- * buffer, whose device address opt_plan_norm_buffer returns).  If h_out is
- * non-NULL the result is also copied to it and the stream is synchronised.
+ * partial-sum launch per gradient dtype into fixed slots; the CTA that
+ * completes last reduces the slots in a fixed order.  Bit-identical run to
+ * run for the same inputs and plan.  Writes the result to d_out (device, 48
+ * bytes, may be NULL to use the plan's own buffer, whose device address
+ * opt_plan_norm_buffer returns).  If h_out is non-NULL the result is also
+ * copied to it and the stream is synchronised.
  * Returns OPT_OK, OPT_ENONFINITE (only when h_out is given), or an error. */
 int opt_grad_norm(opt_plan* plan, double max_norm, opt_norm_result* d_out,
                   opt_norm_result* h_out, void* stream);
@@ -264,7 +265,7 @@ int opt_decode(const void* d_in, float* d_out, int64_t n, int32_t dtype, void* s
  * cudaMalloc, cudaFree or allocating library routine, and no host heap.  The
  * pages describe no such variant; it has no counterpart there.
  *
- * Scratch: one fixed device array inside the library (4,534,272 bytes, held
+ * Scratch: one fixed device array inside the library (4,534,528 bytes, held
  * by every GPU that loads the library until the process exits), large enough
  * for OPT_NOALLOC_MAX_TENSORS tensors and OPT_NOALLOC_MAX_CHUNKS chunks of
  * OPT_CHUNK_ELEMS elements (about 8.6e9 elements).  Larger lists are rejected
@@ -281,7 +282,8 @@ int opt_decode(const void* d_in, float* d_out, int64_t n, int32_t dtype, void* s
  * stream capture.  Every call shares the one array: calls whose device work
  * overlaps (on two streams, or from two host threads) race and must be
  * serialised by the caller.  Each call overwrites every part of the array it
- * reads, so nothing carries over from an earlier call. */
+ * reads, except a completion counter that every call returns to 0, so
+ * nothing carries over from an earlier call. */
 #define OPT_NOALLOC_MAX_TENSORS 8192
 #define OPT_NOALLOC_MAX_CHUNKS 262144
 int opt_grad_norm_noalloc(int32_t n, const int64_t* numel, const void* const* grad,

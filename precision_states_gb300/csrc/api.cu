@@ -28,7 +28,8 @@ struct opt_plan {
   bool has_m2 = false;
   std::vector<void*> grad_dev;          // per tensor, for opt_grads_upload
   std::vector<int64_t> grad_bytes;
-  // one device allocation: tensors | norm chunks | tiles | slots | result | counter | flags
+  // one device allocation: tensors | norm chunks | tiles | slots | result | counter | flags |
+  // norm completion counter
   void* d_mem = nullptr;
   int64_t d_bytes = 0;
   TensorDesc* d_tensors = nullptr;
@@ -38,6 +39,7 @@ struct opt_plan {
   opt_norm_result* d_result = nullptr;
   unsigned long long* d_unchanged = nullptr;
   int* d_err = nullptr;                    // kernel error flags (opt_plan_status)
+  unsigned int* d_done = nullptr;          // the norm's completion counter
   // update-norm clipping (LAMB) workspace, allocated on first use
   std::vector<int64_t> tile_first, tile_count;   // per tensor, in the tile table
   void* d_lamb = nullptr;
@@ -204,7 +206,8 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
   const int64_t off_r = align_up(off_s + (int64_t)sizeof(NormSlot) * 2 * OPT_NORM_SLOTS, 256);
   const int64_t off_u = align_up(off_r + (int64_t)sizeof(opt_norm_result), 256);
   const int64_t off_e = off_u + 8;
-  P->d_bytes = align_up(off_e + 8, 256);
+  const int64_t off_d = off_e + 8;
+  P->d_bytes = align_up(off_d + 8, 256);
   cudaError_t e = cudaMalloc(&P->d_mem, (size_t)P->d_bytes);
   if (e != cudaSuccess) { delete P; return cuda_status(e); }
   char* base = static_cast<char*>(P->d_mem);
@@ -215,6 +218,7 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
   P->d_result = reinterpret_cast<opt_norm_result*>(base + off_r);
   P->d_unchanged = reinterpret_cast<unsigned long long*>(base + off_u);
   P->d_err = reinterpret_cast<int*>(base + off_e);
+  P->d_done = reinterpret_cast<unsigned int*>(base + off_d);
 
   e = cudaMemset(P->d_mem, 0, (size_t)P->d_bytes);
   if (e == cudaSuccess && L->n > 0)
@@ -263,23 +267,8 @@ int opt_grad_norm(opt_plan* P, double max_norm, opt_norm_result* d_out, opt_norm
   if (!g.ok) return OPT_ECUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   opt_norm_result* dst = d_out ? d_out : P->d_result;
-  cudaError_t e = cudaSuccess;
-  // one partial-sum launch per non-empty dtype bucket, each into its own
-  // OPT_NORM_SLOTS slots; the finish reduces the slots of the buckets used
-  int first = -1, last = -1;
-  for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
-    if (P->bucket_begin[b + 1] <= P->bucket_begin[b]) continue;
-    if (first < 0) first = b;
-    last = b;
-    const int dt = b == 0 ? OPT_F32 : OPT_BF16;
-    e = launch_norm_partials(dt, P->d_chunks, P->bucket_begin[b], P->bucket_begin[b + 1],
-                             P->d_slots + b * OPT_NORM_SLOTS, s);
-  }
-  if (e == cudaSuccess) {
-    const int n_slots = first < 0 ? 0 : (last - first + 1) * OPT_NORM_SLOTS;
-    e = launch_norm_finalize(P->d_slots + (first < 0 ? 0 : first * OPT_NORM_SLOTS), n_slots, max_norm,
-                             dst, s);
-  }
+  // one pass-1 launch per non-empty dtype bucket; its last CTA finishes
+  cudaError_t e = launch_norm(P->d_chunks, P->bucket_begin, P->d_slots, P->d_done, max_norm, dst, s);
   if (e != cudaSuccess) return cuda_status(e);
   if (h_out != nullptr) {
     e = cudaMemcpyAsync(h_out, dst, sizeof(opt_norm_result), cudaMemcpyDeviceToHost, s);

@@ -54,12 +54,12 @@ constexpr int64_t kTileElems = 2048;
 int64_t build_table(int32_t n, const int64_t* numel, const int32_t* grad_dtype, int64_t elems,
                     opt_chunk* out, int64_t cap, int64_t bucket_begin[3]);
 
-// gradient norm: pass 1 for one dtype bucket into slots[0 .. OPT_NORM_SLOTS)
-cudaError_t launch_norm_partials(int grad_dtype, const NormChunk* chunks, int64_t chunk_begin,
-                                 int64_t chunk_end, NormSlot* slots, cudaStream_t s);
-// gradient norm: pass 2 over n_slots slots
-cudaError_t launch_norm_finalize(const NormSlot* slots, int n_slots, double max_norm,
-                                 opt_norm_result* out, cudaStream_t s);
+// The gradient norm: one pass-1 launch per non-empty dtype bucket b (chunks
+// [bucket_begin[b], bucket_begin[b + 1]) into slots[b * OPT_NORM_SLOTS ...]),
+// the last CTA to complete finishing into `out`.  `done` is a counter that is
+// 0 between norms (the finishing CTA resets it).
+cudaError_t launch_norm(const NormChunk* chunks, const int64_t bucket_begin[3], NormSlot* slots,
+                        unsigned int* done, double max_norm, opt_norm_result* out, cudaStream_t s);
 
 // fused step for one bucket (persistent grid of sm_count x occupancy CTAs)
 cudaError_t launch_step_fp32_states(int grad_dtype, int algo, const StepArgs& args, int sm_count,

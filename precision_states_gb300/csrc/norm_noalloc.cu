@@ -16,13 +16,14 @@
 // that device current, and caches it.  Each call then copies the caller's
 // host arrays into the array (cudaMemcpyAsync, no staging buffer of ours),
 // builds the chunk table on the device in the same order opt_plan_create
-// builds it on the host, and runs the same two norm kernels as opt_grad_norm
-// -- so the result is the same, bit for bit.
+// builds it on the host, and runs the same norm kernels as opt_grad_norm --
+// so the result is the same, bit for bit.
 //
 // Every call shares the array and overwrites the parts it reads before
-// reading them, so nothing carries over from the previous call.  Two calls
-// whose device work overlaps (different streams, or different host threads)
-// race on the array.
+// reading them -- all but the norm's completion counter, which the
+// finishing CTA returns to 0 -- so nothing carries over from the previous
+// call.  Two calls whose device work overlaps (different streams, or
+// different host threads) race on the array.
 #include <cstdint>
 #include <mutex>
 
@@ -47,9 +48,10 @@ constexpr int64_t kOffOrder = align256(kOffDtype + 4 * kMaxTensors);       // in
 constexpr int64_t kOffBase = align256(kOffOrder + 4 * kMaxTensors);        // int64[T]: first chunk, in that order
 constexpr int64_t kOffChunks = align256(kOffBase + 8 * kMaxTensors);       // NormChunk[C]
 constexpr int64_t kOffSlots = align256(kOffChunks + 16 * kMaxChunks);      // NormSlot[2 * OPT_NORM_SLOTS]
-constexpr int64_t kScratchBytes = align256(kOffSlots + 32 * 2 * OPT_NORM_SLOTS);
+constexpr int64_t kOffDone = align256(kOffSlots + 32 * 2 * OPT_NORM_SLOTS);    // uint32: completion counter
+constexpr int64_t kScratchBytes = align256(kOffDone + 4);
 
-static_assert(kScratchBytes == 4534272, "scratch size stated in opt.h");
+static_assert(kScratchBytes == 4534528, "scratch size stated in opt.h");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 // Device address of g_noalloc_scratch per device, looked up once per device.
@@ -208,18 +210,8 @@ extern "C" int opt_grad_norm_noalloc(int32_t n, const int64_t* numel, const void
 
   const NormChunk* chunks = reinterpret_cast<const NormChunk*>(scratch + kOffChunks);
   NormSlot* slots = reinterpret_cast<NormSlot*>(scratch + kOffSlots);
+  unsigned int* done = reinterpret_cast<unsigned int*>(scratch + kOffDone);
   const int64_t begin[3] = {0, bucket[0], total};
-  int first = -1, last = -1;
-  for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
-    if (begin[b + 1] <= begin[b]) continue;
-    if (first < 0) first = b;
-    last = b;
-    e = launch_norm_partials(b == 0 ? OPT_F32 : OPT_BF16, chunks, begin[b], begin[b + 1],
-                             slots + b * OPT_NORM_SLOTS, s);
-  }
-  if (e == cudaSuccess) {
-    const int n_slots = first < 0 ? 0 : (last - first + 1) * OPT_NORM_SLOTS;
-    e = launch_norm_finalize(slots + (first < 0 ? 0 : first * OPT_NORM_SLOTS), n_slots, max_norm, d_out, s);
-  }
+  e = launch_norm(chunks, begin, slots, done, max_norm, d_out, s);
   return cuda_status(e);
 }

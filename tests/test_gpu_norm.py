@@ -116,3 +116,37 @@ def test_all_zero_and_no_clip():
     grads = [torch.zeros(n, dtype=torch.bfloat16, device="cuda") for n in (1, 33, 70000)]
     _, r = check(grads, max_norm=0.0)
     assert r.norm2 == 0.0 and r.clip_coef == 1.0
+
+
+@pytest.mark.parametrize("mixed", [False, True])
+def test_every_call_finishes_into_its_output(mixed):
+    """The finish runs in the CTA that completes last and resets the
+    completion counter; a counter left behind would skip the next finish and
+    leave the old result in place.  Each call here writes into a buffer
+    filled with a sentinel, on gradients scaled by 2^k since the last call:
+    scaling by a power of two is exact, so the sum of squares scales by 4^k
+    exactly and the result must follow bit for bit."""
+    w = W.workload("sweep")
+    grads = W.make_grads(w, "cuda", step=1, seed=41)
+    if mixed:
+        g32 = W.make_grads(W.workload("sweep", grad_dtype="f32"), "cuda", step=1, seed=42)
+        grads = [grads[i] if i % 3 else g32[i] for i in range(len(grads))]
+    plan = plan_for(grads)
+    d_out = torch.empty(6, dtype=torch.float64, device="cuda")
+    base = None
+    for k in range(4):
+        d_out.fill_(float("nan"))
+        plan.grad_norm(1.0, d_out=d_out.data_ptr(), sync=False)
+        torch.cuda.synchronize()
+        r = ps.opt_norm_result.from_buffer_copy(d_out.cpu().numpy().tobytes())
+        assert r.status == 0
+        if base is None:
+            want = oracle.grad_norm(host(grads), 1.0)
+            assert rel_err(r.norm2, want["norm2"]) <= TOL
+            base = r
+        else:
+            assert r.sumsq == base.sumsq * 4.0 ** k and r.norm2 == base.norm2 * 2.0 ** k
+            assert r.norm_inf == base.norm_inf * 2.0 ** k
+        for g in grads:
+            g.mul_(2.0)
+    plan.close()

@@ -2,7 +2,9 @@
 cannot allocate device memory (their device memory belongs to a framework's
 caching allocator or a fixed budget reserved up front, so they cannot build a
 plan, which allocates a workspace).  It is called through the C ABI and its
-result is compared with opt_grad_norm's on the same gradients, on two calls
+result is compared bit for bit with opt_grad_norm's on the same gradients
+(both sum the same slot spans in the same order: the plan's are built on the
+host, the no-allocation call's by a kernel), on two calls
 in a row with different lists, so that anything the first call leaves in the
 shared scratch array would show up in the second.  Collected last on purpose
 (file name) so a failure here does not hide the other tests."""
@@ -17,9 +19,6 @@ import precision_states_gb300 as ps
 import workloads as W
 
 pytestmark = pytest.mark.gpu
-
-TOL = 1e-12   # the norm tolerance used throughout the tests
-
 
 def via_plan(grads, max_norm):
     params = [torch.zeros(g.numel(), device="cuda") for g in grads]
@@ -52,7 +51,7 @@ def same(a, b):
         if math.isnan(y):
             assert math.isnan(x)
         else:
-            assert abs(x - y) <= TOL * abs(y), (k, x, y)
+            assert x == y, (k, x, y)
     assert a.clip_coef == b.clip_coef
 
 
@@ -72,6 +71,11 @@ def test_noalloc_matches_plan_norm_twice():
     b = via_noalloc(second, 1.0, d_out)
     same(b, via_plan(second, 1.0))
     assert a.norm2 != b.norm2
+    # a list with fewer elements than slots, most slots empty
+    gen = torch.Generator(device="cuda").manual_seed(34)
+    third = [torch.randn(n, device="cuda", generator=gen).to(torch.bfloat16) for n in (3, 0, 5, 900)]
+    third[2] = third[2].float()
+    same(via_noalloc(third, 1.0, d_out), via_plan(third, 1.0))
 
 
 def test_noalloc_rejects_lists_beyond_its_limits():
