@@ -42,15 +42,17 @@ namespace psopt {
 namespace {
 
 // 128 threads and 8 CTAs per SM: the 1216 slots are one wave, and each
-// thread may hold 64 registers, enough for six 16-byte loads in flight that
-// rotate (each register refilled as soon as its vector is summed).  Against
+// thread may hold 64 registers -- enough for four 16-byte loads in flight
+// that rotate (each register refilled as soon as its vector is summed) and
+// two float-float chains (alternate vectors), so that the additions of one
+// vector need not wait for the previous vector's.  Measured on GB300 against
 // 256 threads at the 32-register cap with four loads issued together and
-// then summed, this measured 1.6 % faster on the Llama-3-8B list and 2 % on
-// the 740-tensor list; four rotating loads gained half as much on the
-// former.  Plain reads in the same order reach 7.35 TB/s on GB300, so what
-// remains is the float-float arithmetic's issue cost.
+// then summed into one chain: 2.5 % faster on the Llama-3-8B list, 4 % on
+// the 740-tensor list.  (Six rotating loads and one chain gained 1.6 and
+// 2 %; a packed magnitude max that cut a tenth of the instructions gained
+// nothing.)  Plain reads in the same order reach 7.35 TB/s on GB300.
 constexpr int kNormThreads = 128;
-constexpr int kDepth = 6;            // 16-byte loads in flight per thread
+constexpr int kDepth = 4;            // 16-byte loads in flight per thread
 
 // Two float-float accumulators (lane x, lane y): value = hi + lo per lane.
 struct FF2 {
@@ -273,24 +275,32 @@ norm_partials_kernel(const NormChunk* __restrict__ chunks, int64_t cbegin, int64
     uint32_t cmax = 0;
     // this thread's vectors tid, tid + T, ...: kDepth 16-byte loads in
     // flight, rotating -- each register is refilled with the vector kDepth
-    // ahead as soon as it has been used
+    // ahead as soon as it has been used -- and two summation chains
     int left = nvec > tid ? (nvec - tid + kNormThreads - 1) / kNormThreads : 0;
     const char* q = g + tid * 16;
     constexpr int kStep = kNormThreads * 16;
     if (left >= kDepth) {
       uint4 w[kDepth];
+      FF2 acc2 = {0ull, 0ull};     // a second chain: odd vectors of a round
 #pragma unroll
       for (int d = 0; d < kDepth; ++d) w[d] = ld_nc_u4(q + d * kStep);
       q += kDepth * kStep;
       for (left -= kDepth; left >= kDepth; left -= kDepth, q += kDepth * kStep) {
 #pragma unroll
         for (int d = 0; d < kDepth; ++d) {
-          cmax = max(cmax, acc_vec<GT>(acc, w[d]));
+          cmax = max(cmax, acc_vec<GT>((d & 1) ? acc2 : acc, w[d]));
           w[d] = ld_nc_u4(q + d * kStep);
         }
       }
 #pragma unroll
-      for (int d = 0; d < kDepth; ++d) cmax = max(cmax, acc_vec<GT>(acc, w[d]));
+      for (int d = 0; d < kDepth; ++d) cmax = max(cmax, acc_vec<GT>((d & 1) ? acc2 : acc, w[d]));
+      // fold the second chain in: float-float sum of the two, lane-wise
+      const f2_t s = add2(acc.hi, acc2.hi);
+      const f2_t bb = sub2(s, acc.hi);
+      const f2_t aa = sub2(s, bb);
+      const f2_t e = add2(sub2(acc.hi, aa), sub2(acc2.hi, bb));
+      acc.lo = add2(add2(acc.lo, acc2.lo), e);
+      acc.hi = s;
     }
     for (; left > 0; --left, q += kStep) cmax = max(cmax, acc_vec<GT>(acc, ld_nc_u4(q)));
     // ragged tail: the thread that would own vector nvec loads it element-wise
