@@ -96,7 +96,8 @@ typedef enum { OPT_ROUND_NEAREST = 0, OPT_ROUND_STOCHASTIC = 1 } opt_round;
  *   (F32, F32), (BF16, BF16), (BF16, E4M3), (BF16, E2M2).
  * param_dtype must be F32; grad_dtype[i] is F32 or BF16 per tensor.  m2 is
  * used only by opt_ademamix_step (FP32 states only); pass NULL otherwise.
- * Every non-NULL pointer must be 16-byte aligned.  Tensors with numel 0 may
+ * Every non-NULL pointer must be 16-byte aligned; the AdamW step reads FP32
+ * p, m and v faster where they are 32-byte aligned.  Tensors with numel 0 may
  * have NULL pointers.  The plan copies what it needs: the arrays may be
  * freed after opt_plan_create returns.
  *

@@ -177,6 +177,11 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
     t.numel = L->numel[i];
     t.v_scale = L->v_scale ? L->v_scale[i] : 1.0f;
     t.v_inv_scale = 1.0f / t.v_scale;     // exact for a power of two
+    // FP32 p, m, v that start on a 32-byte boundary take 32-byte loads in
+    // the AdamW step
+    auto a32 = [](const void* q) { return ((uintptr_t)q & 31u) == 0; };
+    t.a32 = (a32(t.p) ? kA32P : 0u) | (L->m_dtype == OPT_F32 && a32(t.m) ? kA32M : 0u) |
+            (L->v_dtype == OPT_F32 && a32(t.v) ? kA32V : 0u);
     t.pad = 0;
     P->total_numel += L->numel[i];
     P->grad_dev[(size_t)i] = const_cast<void*>(L->grad[i]);

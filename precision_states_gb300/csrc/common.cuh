@@ -21,9 +21,11 @@ struct TensorDesc {
   int64_t numel;
   float v_scale;       // stored v code holds v / v_scale (power of two)
   float v_inv_scale;   // 1 / v_scale, exact
-  uint64_t pad;
+  uint32_t a32;        // kA32* bits: the FP32 streams whose base is 32-byte aligned
+  uint32_t pad;
 };
 static_assert(sizeof(TensorDesc) == 64, "TensorDesc layout");
+enum : uint32_t { kA32P = 1u, kA32M = 2u, kA32V = 4u };
 static_assert(sizeof(opt_chunk) == 16, "opt_chunk layout");
 
 // One fixed slot of the gradient-norm pass: the slot's chunks are
@@ -343,6 +345,14 @@ __device__ __forceinline__ uint4 ld_nc_u4(const void* p) {
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
   return r;
+}
+// 32 bytes in one evict-first load (sm_100+); the address must be 32-byte
+// aligned.
+__device__ __forceinline__ void ld_cs_v8(const void* p, uint32_t* r) {
+  asm volatile("ld.global.cs.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                 "=r"(r[7])
+               : "l"(p));
 }
 // Read-modify-write streams (p, m, v): evict-first loads and stores.
 __device__ __forceinline__ uint4 ld_cs_u4(const void* p) {

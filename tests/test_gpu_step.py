@@ -284,3 +284,44 @@ def test_mixed_grad_dtypes_and_empty_tensors(v_dtype):
     _, _, counts = run_lockstep(w, 3, 1e-6, rounding="stochastic", count=v_dtype != "f32", gpu=gpu)
     for got, want in counts:
         assert got == want
+
+
+def _offset16(t: torch.Tensor) -> torch.Tensor:
+    """A copy of t that starts 16 bytes into a fresh allocation: 16-byte
+    aligned (the ABI's rule) but not 32-byte aligned."""
+    k = 16 // t.element_size()
+    buf = torch.empty(t.numel() + k, dtype=t.dtype, device=t.device)
+    assert buf.data_ptr() % 32 == 0
+    view = buf[k:k + t.numel()]
+    view.copy_(t)
+    assert view.data_ptr() % 32 == 16
+    return view
+
+
+@pytest.mark.parametrize("algo", ["adamw", "ademamix"])
+@pytest.mark.parametrize("gdt", ["bf16", "f32"])
+def test_fp32_streams_without_32_byte_alignment(algo, gdt):
+    """The AdamW step reads FP32 p, m and v 32 bytes at a time where the
+    stream's base is 32-byte aligned and 16 bytes at a time where it is not;
+    the choice is per tensor and per stream.  Here p, g, m, v and m2 of
+    different tensors sit 16 bytes off a 32-byte boundary in different
+    combinations, against the oracle (AdEMAMix, which always reads 16 bytes
+    at a time, alongside)."""
+    w = W.workload("sweep", algo=algo, grad_dtype=gdt, hp=dict(lr=0.1, weight_decay=0.1))
+    gpu = GpuSide(w, seed=9)
+    for i in range(len(w.sizes)):
+        if w.sizes[i] == 0:
+            continue
+        if i % 2 == 0:
+            gpu.params[i] = _offset16(gpu.params[i])
+        if i % 3 == 0:
+            gpu.grads[i] = _offset16(gpu.grads[i])
+        if i % 4 == 1:
+            gpu.m[i] = _offset16(gpu.m[i])
+        if i % 5 != 2:
+            gpu.v[i] = _offset16(gpu.v[i])
+        if gpu.m2 is not None and i % 2 == 1:
+            gpu.m2[i] = _offset16(gpu.m2[i])
+    gpu.plan.close()
+    gpu.plan = ps.Plan(gpu.params, gpu.grads, gpu.m, gpu.v, gpu.m2)
+    run_lockstep(w, 2, 1e-6, gpu=gpu)
