@@ -153,13 +153,11 @@ lamb_apply_kernel(const StepArgs a, const float* __restrict__ ratio) {
     float p[8], m[8], v[8];
     if (cnt == 8) {
       uint32_t w[8];
-      put4(w, ld_cs_u4(td.p + e0)); put4(w + 4, ld_cs_u4(td.p + e0 + 4));
+      ld_cs_x8(td.p + e0, td.a32 & kA32P, w);
       for (int j = 0; j < 8; ++j) p[j] = u2f(w[j]);
-      put4(w, ld_cs_u4(static_cast<const float*>(td.m) + e0));
-      put4(w + 4, ld_cs_u4(static_cast<const float*>(td.m) + e0 + 4));
+      ld_cs_x8(static_cast<const float*>(td.m) + e0, td.a32 & kA32M, w);
       for (int j = 0; j < 8; ++j) m[j] = u2f(w[j]);
-      put4(w, ld_cs_u4(static_cast<const float*>(td.v) + e0));
-      put4(w + 4, ld_cs_u4(static_cast<const float*>(td.v) + e0 + 4));
+      ld_cs_x8(static_cast<const float*>(td.v) + e0, td.a32 & kA32V, w);
       for (int j = 0; j < 8; ++j) v[j] = u2f(w[j]);
     } else {
       for (int j = 0; j < 8; ++j) {
