@@ -33,7 +33,7 @@ struct TileSums {
 __device__ __forceinline__ float lamb_dir(float mn, float vn, const opt_step_scalars& sc) {
   const float num = __fmul_rn(mn, sc.inv_bc1);
   const float den = __fadd_rn(sqrt_approx(__fmul_rn(vn, sc.inv_bc2)), sc.eps);
-  return div_full(num, den);
+  return div_approx(num, den);
 }
 
 template <int GT>

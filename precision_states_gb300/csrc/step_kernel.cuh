@@ -275,7 +275,8 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
     float num = __fmul_rn(mnv[j], sc.inv_bc1);
     if constexpr (ALGO == ALGO_ADEMAMIX) num = __fadd_rn(num, __fmul_rn(sc.alpha, m2n[j]));
     const float den = __fadd_rn(sqrt_approx(__fmul_rn(vnv[j], sc.inv_bc2)), sc.eps);
-    pn[j] = __fsub_rn(__fmul_rn(u2f(f.p[j]), sc.decay), __fmul_rn(sc.lr, div_full(num, den)));
+    const float u = COMBO == SC_BF16_BF16 ? div_full(num, den) : div_approx(num, den);
+    pn[j] = __fsub_rn(__fmul_rn(u2f(f.p[j]), sc.decay), __fmul_rn(sc.lr, u));
   }
   // the value the v code stores: v / v_scale, exact (E2M2: a quarter of it,
   // the converters' E3M2 grid, in the same one multiplication)

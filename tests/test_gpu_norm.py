@@ -150,3 +150,30 @@ def test_every_call_finishes_into_its_output(mixed):
         for g in grads:
             g.mul_(2.0)
     plan.close()
+
+
+def test_two_plans_on_two_streams_concurrently():
+    """Each plan owns its slots and its completion counter, so norms of two
+    plans issued on two streams at the same time finish independently; each
+    result equals the oracle's for its own list, for several rounds."""
+    wa, wb = W.workload("clip_740"), W.workload("sweep")
+    ga = W.make_grads(wa, "cuda", step=1, seed=51)
+    gb = W.make_grads(wb, "cuda", step=1, seed=52)
+    pa, pb = plan_for(ga), plan_for(gb)
+    want_a = oracle_norm_parallel(host(ga), 1.0)
+    want_b = oracle.grad_norm(host(gb), 1.0)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = [(torch.full((6,), float("nan"), dtype=torch.float64, device="cuda"),
+             torch.full((6,), float("nan"), dtype=torch.float64, device="cuda")) for _ in range(4)]
+    torch.cuda.synchronize()
+    for da, db in outs:
+        pa.grad_norm(1.0, d_out=da.data_ptr(), sync=False, stream=sa)
+        pb.grad_norm(1.0, d_out=db.data_ptr(), sync=False, stream=sb)
+    torch.cuda.synchronize()
+    for da, db in outs:
+        ra = ps.opt_norm_result.from_buffer_copy(da.cpu().numpy().tobytes())
+        rb = ps.opt_norm_result.from_buffer_copy(db.cpu().numpy().tobytes())
+        assert rel_err(ra.norm2, want_a["norm2"]) <= TOL and ra.clip_coef == want_a["clip_coef"]
+        assert rel_err(rb.norm2, want_b["norm2"]) <= TOL and rb.clip_coef == want_b["clip_coef"]
+    pa.close()
+    pb.close()
