@@ -325,3 +325,44 @@ def test_fp32_streams_without_32_byte_alignment(algo, gdt):
     gpu.plan.close()
     gpu.plan = ps.Plan(gpu.params, gpu.grads, gpu.m, gpu.v, gpu.m2)
     run_lockstep(w, 2, 1e-6, gpu=gpu)
+
+
+@pytest.mark.parametrize("case", ["lr0", "beta1_0", "beta2_0"])
+@pytest.mark.parametrize("v_dtype", ["f32", "e4m3"])
+def test_degenerate_hyperparameters(case, v_dtype):
+    """Edge values of the hyperparameters, against the oracle: lr = 0 (the
+    parameters stay bit-for-bit as they were while the moments move),
+    beta1 = 0 (m is the clipped gradient) and beta2 = 0 (v is its square)."""
+    hp = dict(lr=1e-2, weight_decay=0.1)
+    hp.update({"lr0": dict(lr=0.0), "beta1_0": dict(beta1=0.0), "beta2_0": dict(beta2=0.0)}[case])
+    m_dtype = "f32" if v_dtype == "f32" else "bf16"
+    w = W.workload("sweep", m_dtype=m_dtype, v_dtype=v_dtype, hp=hp)
+    gpu = GpuSide(w, seed=21)
+    p0 = [p.clone() for p in gpu.params]
+    run_lockstep(w, 3, 1e-6, rounding="stochastic" if v_dtype != "f32" else "nearest", gpu=gpu)
+    if case == "lr0":
+        for a, b in zip(gpu.params, p0):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_ademamix_without_slow_moment_is_adamw_bitwise():
+    """AdEMAMix with alpha = 0 and beta3 = 1 keeps m2 at zero and adds
+    nothing to the update, so it must leave p, m and v with exactly the bits
+    AdamW leaves on the same inputs (the two run as different kernels)."""
+    hp = dict(lr=1e-2, weight_decay=0.1, alpha=0.0, beta3=1.0)
+    wa = W.workload("sweep", algo="adamw", hp=hp)
+    we = W.workload("sweep", algo="ademamix", hp=hp)
+    ga, ge = GpuSide(wa, seed=23), GpuSide(we, seed=23)
+    hpa, _ = hp_for(wa)
+    hpe, _ = hp_for(we)
+    for t in range(1, 4):
+        W.fill_grads(wa, ga.grads, t, 23)
+        W.fill_grads(we, ge.grads, t, 23)
+        ga.step(t, hpa, clip=True)
+        ge.step(t, hpe, clip=True)
+    torch.cuda.synchronize()
+    for name in ("params", "m", "v"):
+        for a, b in zip(getattr(ga, name), getattr(ge, name)):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32)), name
+    for m2 in ge.m2:
+        assert not m2.any()
