@@ -50,7 +50,11 @@ namespace {
 // then summed into one chain: 2.5 % faster on the Llama-3-8B list, 4 % on
 // the 740-tensor list.  (Six rotating loads and one chain gained 1.6 and
 // 2 %; a packed magnitude max that cut a tenth of the instructions gained
-// nothing.)  Plain reads in the same order reach 7.35 TB/s on GB300.
+// nothing; eight 16-byte cp.async copies in flight per thread into its own
+// shared-memory slots, pipelined within each chunk, were 3 % slower on the
+// Llama-3-8B list and 12 % on the 740-tensor list; 32-byte loads read no
+// faster than 16-byte ones in a probe of this access order.)  Plain reads
+// in the same order reach 7.44 TB/s on GB300.
 constexpr int kNormThreads = 128;
 constexpr int kDepth = 4;            // 16-byte loads in flight per thread
 
