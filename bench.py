@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--lamb", type=float, default=None, metavar="MAX_UNORM",
                     help="time the update-norm clipping (LAMB) step with this bound instead of AdamW")
     ap.add_argument("--e2e-steps", type=int, default=0, help="0: same as --steps")
+    ap.add_argument("--graph", action="store_true",
+                    help="FP32 states: device step counter, norm and step replayed from CUDA graphs")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-seconds", type=float, default=12.0)
@@ -267,17 +269,31 @@ def run_ours(args, rank, local_rank, world):
         w.algo = "lamb"
         step_fn = lambda hp_, t_, dn_, stream=None: plan.lamb_step(hp_, t_, args.lamb, dn_, stream=stream)
     # the norm is one launch per gradient dtype (one here; its last CTA
-    # finishes), the step one launch (LAMB: three passes)
-    launches_per_step = (1 if clip else 0) + (3 if args.lamb is not None else 1)
+    # finishes), the step one launch (LAMB: three passes); with --graph the
+    # device step counter adds one launch
+    launches_per_step = (1 if clip else 0) + (3 if args.lamb is not None else 1) + (1 if args.graph else 0)
+    if args.graph and (w.m_dtype != "f32" or args.lamb is not None):
+        raise SystemExit("--graph needs FP32 states and the AdamW or AdEMAMix step")
+    hp_step = hp
+    if args.graph:
+        hp_step = ps.opt_hparams.from_buffer_copy(hp)
+        hp_step.flags |= ps.OPT_STEP_DEVICE_COUNTER
+    graphs = {}
 
     def one_step(t, ev=None):
         if ev is not None:
             ev[0].record(stream)
         if clip:
-            plan.grad_norm(w.max_norm, sync=False, stream=stream)
+            if "norm" in graphs:
+                graphs["norm"].replay()
+            else:
+                plan.grad_norm(w.max_norm, sync=False, stream=stream)
         if ev is not None:
             ev[1].record(stream)
-        step_fn(hp, t, d_norm, stream=stream)
+        if "step" in graphs:
+            graphs["step"].replay()
+        else:
+            step_fn(hp_step, 0 if args.graph else t, d_norm, stream=stream)
         if ev is not None:
             ev[2].record(stream)
 
@@ -286,6 +302,17 @@ def run_ours(args, rank, local_rank, world):
         t += 1
         one_step(t)
     torch.cuda.synchronize()
+    if args.graph:
+        # capture once (nothing runs); each replay is the counter's next step
+        side = torch.cuda.Stream(dev)
+        if clip:
+            graphs["norm"] = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graphs["norm"], stream=side):
+                plan.grad_norm(w.max_norm, sync=False, stream=side)
+        graphs["step"] = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graphs["step"], stream=side):
+            step_fn(hp_step, 0, d_norm, stream=side)
+        torch.cuda.synchronize()
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
@@ -461,6 +488,7 @@ def run_ours(args, rank, local_rank, world):
                        "grad_dtype": w.grad_dtype, "m_dtype": w.m_dtype, "v_dtype": w.v_dtype,
                        "rounding": args.rounding, "algo": w.algo,
                        "clip_max_norm": w.max_norm, "parallelism": f"replicas{world}",
+                       "launch": "cuda-graph replay, device step counter" if args.graph else "direct",
                        "l2": "inputs larger than L2 (%.0f GB streamed per step)" % ((step_bytes + norm_bytes) / 1e9)},
             "hbm_gbs": round((step_bytes + norm_bytes) / (total_ms / args.steps / 1e3) / 1e9, 1),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,

@@ -154,6 +154,19 @@ typedef struct opt_hparams {
  * (the state it started from). */
 #define OPT_STEP_RESET_STATES 1
 
+/* Step number from the plan's device step counter (FP32 states only,
+ * otherwise OPT_EUNSUPPORTED).  Pass step = 0 (anything else is
+ * OPT_EINVAL): the call advances the counter on the device and takes the
+ * step it reaches, so a CUDA graph captured around opt_grad_norm and the step
+ * replays as step t, t + 1, ... with no host work per step.  One extra
+ * one-thread launch forms the step's two bias corrections on the device, in
+ * double from the FP32 betas, rounded once to FP32: the value the host forms
+ * for the same step, give or take the last bit (the device's pow is not
+ * the host's).  The counter starts at 0 (the first counted step is 1); set
+ * it with opt_plan_set_step, for example to 1 on a reset step.  Counted and
+ * host-numbered steps may be mixed; they do not see each other's numbers. */
+#define OPT_STEP_DEVICE_COUNTER 2
+
 /* ---- norm result (48 bytes, written by opt_grad_norm) -------------------
  * sumsq    sum of squares of all finite gradient elements (fp64)
  * norm2    sqrt(sumsq); NaN if any NaN, else +Inf if any +-Inf
@@ -199,10 +212,16 @@ const opt_norm_result* opt_plan_norm_buffer(const opt_plan* plan);
 /* One fused step over every tensor of the plan, in place.  d_norm: a device
  * opt_norm_result from opt_grad_norm, or NULL for no clipping.  When
  * d_norm->status is OPT_ENONFINITE the kernels leave p and every state
- * untouched (the step is skipped on the device, no host sync).  step >= 1.
- * One launch per gradient-dtype bucket. */
+ * untouched (the step is skipped on the device, no host sync).  step >= 1,
+ * or 0 with OPT_STEP_DEVICE_COUNTER.  One launch per gradient-dtype bucket
+ * (one more with the device counter). */
 int opt_adamw_step(opt_plan* plan, const opt_hparams* hp, int64_t step,
                    const opt_norm_result* d_norm, void* stream);
+/* Set the plan's device step counter (OPT_STEP_DEVICE_COUNTER) so that the
+ * next counted step is next_step (>= 1, else OPT_EINVAL), in stream order;
+ * a launch, so it may itself be captured. */
+int opt_plan_set_step(opt_plan* plan, int64_t next_step, void* stream);
+
 /* As opt_adamw_step plus m2 and alpha; needs FP32 states and m2 pointers. */
 int opt_ademamix_step(opt_plan* plan, const opt_hparams* hp, int64_t step,
                       const opt_norm_result* d_norm, void* stream);

@@ -29,7 +29,7 @@ struct opt_plan {
   std::vector<void*> grad_dev;          // per tensor, for opt_grads_upload
   std::vector<int64_t> grad_bytes;
   // one device allocation: tensors | norm chunks | tiles | slots | result | counter | flags |
-  // norm completion counter
+  // norm completion counter | step counter | step scalars
   void* d_mem = nullptr;
   int64_t d_bytes = 0;
   TensorDesc* d_tensors = nullptr;
@@ -40,6 +40,8 @@ struct opt_plan {
   unsigned long long* d_unchanged = nullptr;
   int* d_err = nullptr;                    // kernel error flags (opt_plan_status)
   unsigned int* d_done = nullptr;          // the norm's completion counter
+  int64_t* d_step = nullptr;               // device step counter (last step taken)
+  opt_step_scalars* d_sc = nullptr;        // its step's scalars
   // update-norm clipping (LAMB) workspace, allocated on first use
   std::vector<int64_t> tile_first, tile_count;   // per tensor, in the tile table
   void* d_lamb = nullptr;
@@ -212,7 +214,9 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
   const int64_t off_u = align_up(off_r + (int64_t)sizeof(opt_norm_result), 256);
   const int64_t off_e = off_u + 8;
   const int64_t off_d = off_e + 8;
-  P->d_bytes = align_up(off_d + 8, 256);
+  const int64_t off_k = align_up(off_d + 8, 16);
+  const int64_t off_q = off_k + 16;
+  P->d_bytes = align_up(off_q + (int64_t)sizeof(opt_step_scalars), 256);
   cudaError_t e = cudaMalloc(&P->d_mem, (size_t)P->d_bytes);
   if (e != cudaSuccess) { delete P; return cuda_status(e); }
   char* base = static_cast<char*>(P->d_mem);
@@ -224,6 +228,8 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
   P->d_unchanged = reinterpret_cast<unsigned long long*>(base + off_u);
   P->d_err = reinterpret_cast<int*>(base + off_e);
   P->d_done = reinterpret_cast<unsigned int*>(base + off_d);
+  P->d_step = reinterpret_cast<int64_t*>(base + off_k);
+  P->d_sc = reinterpret_cast<opt_step_scalars*>(base + off_q);
 
   e = cudaMemset(P->d_mem, 0, (size_t)P->d_bytes);
   if (e == cudaSuccess && L->n > 0)
@@ -286,8 +292,11 @@ int opt_grad_norm(opt_plan* P, double max_norm, opt_norm_result* d_out, opt_norm
 
 static int do_step(opt_plan* P, const opt_hparams* hp, int64_t step, const opt_norm_result* d_norm,
                    void* stream, int algo) {
-  if (P == nullptr || hp == nullptr || step < 1) return OPT_EINVAL;
-  if ((hp->flags & ~OPT_STEP_RESET_STATES) != 0) return OPT_EINVAL;
+  if (P == nullptr || hp == nullptr) return OPT_EINVAL;
+  if ((hp->flags & ~(OPT_STEP_RESET_STATES | OPT_STEP_DEVICE_COUNTER)) != 0) return OPT_EINVAL;
+  const bool dev_step = (hp->flags & OPT_STEP_DEVICE_COUNTER) != 0;
+  if (dev_step ? step != 0 : step < 1) return OPT_EINVAL;
+  if (dev_step && P->combo != SC_F32) return OPT_EUNSUPPORTED;
   if (hp->rounding != OPT_ROUND_NEAREST && hp->rounding != OPT_ROUND_STOCHASTIC) return OPT_EINVAL;
   if (d_norm != nullptr && ((uintptr_t)d_norm & 7u)) return OPT_EALIGN;
   if (algo == ALGO_ADEMAMIX) {
@@ -296,7 +305,9 @@ static int do_step(opt_plan* P, const opt_hparams* hp, int64_t step, const opt_n
   }
   StepArgs a;
   std::memset(&a, 0, sizeof a);
-  int st = opt_step_scalars_compute(hp, step, &a.sc);
+  // with the device counter the block's bias corrections are formed on the
+  // device for the counter's next step; the rest is validated and formed here
+  int st = opt_step_scalars_compute(hp, dev_step ? 1 : step, &a.sc);
   if (st != OPT_OK) return st;
   a.tensors = P->d_tensors;
   a.tiles = P->d_tiles;
@@ -312,6 +323,10 @@ static int do_step(opt_plan* P, const opt_hparams* hp, int64_t step, const opt_n
   if (!g.ok) return OPT_ECUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
+  if (dev_step) {
+    e = launch_step_scalars(a.sc, P->d_step, P->d_sc, s);
+    a.d_sc = P->d_sc;
+  }
   for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
     a.tile_begin = P->tile_begin[b];
     a.tile_end = P->tile_begin[b + 1];
@@ -394,6 +409,13 @@ int opt_unchanged_count(opt_plan* P, uint64_t* h_count, void* stream) {
   if (e != cudaSuccess) return cuda_status(e);
   *h_count = v;
   return OPT_OK;
+}
+
+int opt_plan_set_step(opt_plan* P, int64_t next_step, void* stream) {
+  if (P == nullptr || next_step < 1) return OPT_EINVAL;
+  DeviceGuard g(P->device);
+  if (!g.ok) return OPT_ECUDA;
+  return cuda_status(launch_set_step(P->d_step, next_step - 1, static_cast<cudaStream_t>(stream)));
 }
 
 int opt_plan_status(opt_plan* P, int32_t* h_flags, void* stream) {

@@ -60,6 +60,7 @@ struct StepArgs {
   unsigned long long* unchanged;      // NULL: do not count
   int reset;                          // nonzero: start from zero moments
   int* err;                           // kernel error flags (bit 0: a bounded wait ran out)
+  const opt_step_scalars* d_sc;       // non-NULL: use these scalars (device memory), not sc
 };
 
 // ------------------------------------------------------------- bit views

@@ -64,6 +64,11 @@ cudaError_t launch_norm(const NormChunk* chunks, const int64_t bucket_begin[3], 
 // fused step for one bucket (persistent grid of sm_count x occupancy CTAs)
 cudaError_t launch_step_fp32_states(int grad_dtype, int algo, const StepArgs& args, int sm_count,
                                     cudaStream_t s);
+// device step counter: advance it and write the step's scalars (base with
+// the bias corrections of the new step) to `out`; or set it to `value`
+cudaError_t launch_step_scalars(const opt_step_scalars& base, int64_t* counter, opt_step_scalars* out,
+                                cudaStream_t s);
+cudaError_t launch_set_step(int64_t* counter, int64_t value, cudaStream_t s);
 cudaError_t launch_step_lowp_states(int grad_dtype, int combo, int stochastic, const StepArgs& args,
                                     int sm_count, cudaStream_t s);
 

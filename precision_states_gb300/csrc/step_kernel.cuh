@@ -380,7 +380,11 @@ __device__ __forceinline__ bool next_tile(int64_t& i, const StepArgs& a, int off
   return false;
 }
 
-template <int GT, int COMBO, int ALGO, bool SR>
+// DEVSC: the step's scalars come from device memory (a.d_sc, written by
+// the device step counter's kernel just before), so that a captured CUDA
+// graph can replay the step with a new step number; otherwise they are a
+// kernel argument.
+template <int GT, int COMBO, int ALGO, bool SR, bool DEVSC = false>
 __global__ void __launch_bounds__(kStepThreads, (StepShape<GT, COMBO, ALGO, SR>::kMinBlocks))
 step_kernel(const StepArgs a) {
   float coef = 1.0f;
@@ -388,6 +392,9 @@ step_kernel(const StepArgs a) {
     if (a.d_norm->status != OPT_OK) return;     // non-finite norm: leave all untouched
     coef = a.d_norm->clip_coef;
   }
+  opt_step_scalars sc_dev;
+  if constexpr (DEVSC) sc_dev = *a.d_sc;
+  const opt_step_scalars& sc = DEVSC ? sc_dev : a.sc;
   const bool count = a.unchanged != nullptr;
   const bool reset = a.reset != 0;
   const int off = threadIdx.x * 8;
@@ -427,7 +434,7 @@ step_kernel(const StepArgs a) {
       if (ncnt == 8) load_full(ntd, ne0, reset, nxt);
       else load_partial(ntd, ne0, ncnt, reset, nxt);
     }
-    same += update_store<GT, COMBO, ALGO, SR>(ctd, ce0, ccnt, cur, coef, a.sc, ctensor, a.seed_lo,
+    same += update_store<GT, COMBO, ALGO, SR>(ctd, ce0, ccnt, cur, coef, sc, ctensor, a.seed_lo,
                                               a.seed_hi, a.step32, count);
     cur = nxt;
     ctd = ntd;
@@ -448,11 +455,11 @@ step_kernel(const StepArgs a) {
 // a property of the kernel, cached), but no more than there are tiles.
 // Non-persistent shapes launch one CTA per tile (the tile loop then runs
 // once; it still covers any tiles past the grid-size limit).
-template <int GT, int COMBO, int ALGO, bool SR>
+template <int GT, int COMBO, int ALGO, bool SR, bool DEVSC = false>
 cudaError_t launch_one(const StepArgs& a, int sm_count, cudaStream_t s) {
   const int64_t n = a.tile_end - a.tile_begin;
   if (n <= 0) return cudaSuccess;
-  auto k = step_kernel<GT, COMBO, ALGO, SR>;
+  auto k = step_kernel<GT, COMBO, ALGO, SR, DEVSC>;
   static OccupancyCache occ;
   const int per_sm = cached_occupancy(k, occ, kStepThreads, 0);
   constexpr int64_t kMaxGrid = 0x7FFFFFFF;

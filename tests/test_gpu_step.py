@@ -366,3 +366,95 @@ def test_ademamix_without_slow_moment_is_adamw_bitwise():
             assert torch.equal(a.view(torch.int32), b.view(torch.int32)), name
     for m2 in ge.m2:
         assert not m2.any()
+
+
+def _counted_lockstep(w, gpu, steps, seed, launch, first_step=1):
+    """Steps first_step .. first_step + steps - 1 on the oracle beside the
+    GPU's device-counted steps; `launch()` issues the GPU's norm and step."""
+    orc = OracleSide(gpu, range(len(w.sizes)))
+    _, ohp = hp_for(w)
+    for t in range(first_step, first_step + steps):
+        W.fill_grads(w, gpu.grads, t, seed)
+        want = oracle.grad_norm([W.to_numpy_codes(g) for g in gpu.grads], w.max_norm)
+        g_np = orc.grads(gpu.grads)
+        launch()
+        orc.step(t, g_np, ohp, want["clip_coef"], False, 0)
+    torch.cuda.synchronize()
+    orc.compare(gpu, 1e-5, False)
+
+
+@pytest.mark.parametrize("algo", ["adamw", "ademamix"])
+@pytest.mark.parametrize("gdt", ["bf16", "f32"])
+def test_device_step_counter_matches_oracle(algo, gdt):
+    """OPT_STEP_DEVICE_COUNTER: step argument 0, the step number taken from
+    the plan's device counter (advanced by each call), the bias corrections
+    formed on the device; five steps against the oracle's steps 1..5."""
+    w = W.workload("sweep", algo=algo, grad_dtype=gdt, hp=dict(lr=1e-2, weight_decay=0.1))
+    gpu = GpuSide(w, seed=31)
+    ghp, _ = hp_for(w)
+    ghp.flags |= ps.OPT_STEP_DEVICE_COUNTER
+    fn = gpu.plan.ademamix_step if algo == "ademamix" else gpu.plan.adamw_step
+
+    def launch():
+        gpu.plan.grad_norm(w.max_norm, sync=False)
+        fn(ghp, 0, gpu.plan.norm_buffer())
+    _counted_lockstep(w, gpu, 5, 31, launch)
+
+
+def test_device_step_counter_set_step():
+    """opt_plan_set_step(7): the next counted steps are 7, 8, 9."""
+    w = W.workload("sweep", hp=dict(lr=1e-2, weight_decay=0.1))
+    gpu = GpuSide(w, seed=32)
+    ghp, _ = hp_for(w)
+    ghp.flags |= ps.OPT_STEP_DEVICE_COUNTER
+    gpu.plan.set_step(7)
+
+    def launch():
+        gpu.plan.grad_norm(w.max_norm, sync=False)
+        gpu.plan.adamw_step(ghp, 0, gpu.plan.norm_buffer())
+    _counted_lockstep(w, gpu, 3, 32, launch, first_step=7)
+
+
+def test_cuda_graph_replays_counted_steps():
+    """The norm and a device-counted step captured once in a CUDA graph;
+    each replay is the next step (1, 2, 3, 4), against the oracle."""
+    w = W.workload("sweep", hp=dict(lr=1e-2, weight_decay=0.1))
+    ghp, _ = hp_for(w)
+    ghp.flags |= ps.OPT_STEP_DEVICE_COUNTER
+    side = torch.cuda.Stream()
+    # warm up (occupancy caches, first launches) on a throwaway plan
+    warm = GpuSide(w, seed=98)
+    with torch.cuda.stream(side):
+        warm.plan.grad_norm(w.max_norm, sync=False)
+        warm.plan.adamw_step(ghp, 0, warm.plan.norm_buffer())
+    torch.cuda.synchronize()
+    gpu = GpuSide(w, seed=34)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        gpu.plan.grad_norm(w.max_norm, sync=False)
+        gpu.plan.adamw_step(ghp, 0, gpu.plan.norm_buffer())
+    _counted_lockstep(w, gpu, 4, 34, graph.replay)
+    assert gpu.plan.status() == 0
+
+
+def test_device_step_counter_rejects():
+    w = W.workload("sweep")
+    gpu = GpuSide(w, seed=35)
+    hp = ps.hparams(device_step=True)
+    with pytest.raises(ps.OptError) as e:
+        gpu.plan.adamw_step(hp, 1)                    # a step number with the counter
+    assert e.value.status == ps.OPT_EINVAL
+    with pytest.raises(ps.OptError) as e:
+        gpu.plan.adamw_step(ps.hparams(), 0)          # step 0 without it
+    assert e.value.status == ps.OPT_EINVAL
+    with pytest.raises(ps.OptError) as e:
+        gpu.plan.set_step(0)
+    assert e.value.status == ps.OPT_EINVAL
+    with pytest.raises(ps.OptError) as e:
+        gpu.plan.lamb_step(hp, 0, 1.0)
+    assert e.value.status == ps.OPT_EINVAL
+    wl = W.workload("sweep", m_dtype="bf16", v_dtype="e4m3")
+    low = GpuSide(wl, seed=36)
+    with pytest.raises(ps.OptError) as e:
+        low.plan.adamw_step(hp, 0)
+    assert e.value.status == ps.OPT_EUNSUPPORTED
