@@ -56,7 +56,7 @@ extern "C" {
 #define OPT_ENONFINITE    1   /* a status, not a failure: the gradient norm was
                                  NaN or Inf; a step given this norm changes
                                  nothing */
-#define OPT_EINVAL       -1   /* NULL pointer, negative size, bad enum, step < 1 */
+#define OPT_EINVAL       -1   /* NULL pointer, negative size, bad enum, bad step */
 #define OPT_EUNSUPPORTED -2   /* dtype combination not built (e.g. FP8 grads) */
 #define OPT_EALIGN       -3   /* a device pointer not 16-byte aligned */
 #define OPT_ECUDA        -4   /* a CUDA runtime call failed */

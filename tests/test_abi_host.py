@@ -200,6 +200,14 @@ def test_plan_status_null_arguments():
     assert ps.OPT_FLAG_WAIT_TIMEOUT == 1
 
 
+def test_set_step_and_step_flags_on_the_host():
+    """opt_plan_set_step rejects a missing plan before any CUDA call, and
+    the device-counter flag is the bit the header defines."""
+    assert ps.lib().opt_plan_set_step(None, 1, None) == ps.OPT_EINVAL
+    assert ps.OPT_STEP_DEVICE_COUNTER == 2 and ps.OPT_STEP_RESET_STATES == 1
+    assert ps.hparams(device_step=True, reset_states=True).flags == 3
+
+
 @pytest.mark.parametrize("field,value", [
     ("beta1", 1.0), ("beta1", -0.1), ("beta2", 1.0), ("beta3", 1.5), ("lr", -1e-3), ("eps", -1e-8),
     ("weight_decay", -0.1), ("lr", float("nan")), ("alpha", float("inf")), ("beta2", float("nan")),
