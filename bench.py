@@ -17,6 +17,8 @@ norm, combines on the host with opt_norm_combine); value = all ranks'
 parameters / max-over-ranks time.
 
 ``--impl reference`` times the CPU oracle instead (bounded sample per step).
+``--graph`` (FP32 states) takes the step number from the plan's device
+counter and replays the norm and the step from CUDA graphs captured once.
 """
 from __future__ import annotations
 
