@@ -94,7 +94,9 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")   # run output folder
+        # the raw samples, beside the summary the JSON line carries
+        out_dir = os.environ.get("BENCH_OUT_DIR", os.path.join(ROOT, "bench_out"))
+        self.path = os.path.join(out_dir, f"clocks_rank{gpu_index}.csv")
 
     def start(self):
         try:
