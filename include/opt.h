@@ -293,7 +293,9 @@ int opt_decode(const void* d_in, float* d_out, int64_t n, int32_t dtype, void* s
  *
  * Inputs: n tensors; numel, grad (device pointers, 16-byte aligned) and
  * grad_dtype (OPT_F32 or OPT_BF16) are HOST arrays, copied into the scratch
- * array on `stream` during the call, so they may be reused when it returns.
+ * array on `stream` by cudaMemcpyAsync.  Ordinary (pageable) host arrays may
+ * be reused as soon as the call returns; page-locked ones must stay
+ * unchanged until `stream` has reached this call.
  * d_out: device, 8-byte aligned, 48 bytes.  Returns OPT_OK or an error
  * status; the norm's own status (OPT_ENONFINITE) is in d_out->status.
  *

@@ -84,16 +84,22 @@ class OracleSide:
     def grads(self, gpu_grads):
         return [W.to_numpy_codes(self.cut(gpu_grads, k, "grad")) for k in range(len(self.samples))]
 
-    def step(self, t: int, grads_np, ohp, coef: float, stochastic: bool, seed: int):
-        """grads_np: host gradient arrays for the samples (same order)."""
-        unchanged = 0
-        for k, (i, start, n) in enumerate(self.samples):
-            unchanged += oracle.adam_tensor(
+    def step(self, t: int, grads_np, ohp, coef: float, stochastic: bool, seed: int, threads: int = 1):
+        """grads_np: host gradient arrays for the samples (same order).  With
+        threads > 1 the samples are stepped concurrently (each is its own
+        host array and the C calls release the GIL); the per-element results
+        do not depend on it."""
+        def one(k):
+            i, start, n = self.samples[k]
+            return oracle.adam_tensor(
                 ALGO[self.w.algo], self.p[k], grads_np[k], self.m[k], self.v[k], ohp, t,
                 m2=None if self.m2 is None else self.m2[k], m_dtype=self.w.m_dtype,
                 v_dtype=self.w.v_dtype, coef=coef, stochastic=stochastic, seed=seed, tensor_index=i,
                 index_base=start, v_scale=1.0 if self.v_scale is None else self.v_scale[i])
-        return unchanged
+        if threads <= 1:
+            return sum(one(k) for k in range(len(self.samples)))
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            return sum(ex.map(one, range(len(self.samples))))
 
     def compare(self, gpu: GpuSide, tol: float, exact_codes: bool):
         """FP32 values within tol (1+|x|); low-precision codes identical
@@ -116,7 +122,7 @@ class OracleSide:
 
 
 def run_lockstep(w, steps, tol, samples=None, rounding="nearest", seed=0, hp_seed=77, count=False,
-                 checkpoints=(), norm_threads=16, gpu=None):
+                 checkpoints=(), norm_threads=16, gpu=None, step_threads=1):
     """Run `steps` steps of workload `w` on the GPU (whole list, clip from the
     GPU's own norm when w.max_norm > 0) and on the oracle (its own norm over
     every gradient, the step on `samples`), comparing the norms every step and
@@ -140,7 +146,7 @@ def run_lockstep(w, steps, tol, samples=None, rounding="nearest", seed=0, hp_see
             del all_np
         g_np = orc.grads(gpu.grads)
         gpu.step(t, ghp, clip)
-        same = orc.step(t, g_np, ohp, coef, sr, hp_seed)
+        same = orc.step(t, g_np, ohp, coef, sr, hp_seed, threads=step_threads)
         if count:
             counts.append((gpu.plan.unchanged_count(), same))
         if t in checkpoints:
