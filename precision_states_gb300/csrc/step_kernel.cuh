@@ -62,12 +62,17 @@ constexpr int kStepThreads = 256;
 //   / 0.869 -> 0.980 / 0.970 / 0.948 (stochastic BF16 / E4M3 / E2M2 v) and
 //   0.964 -> 0.989 (nearest BF16 v).  Nearest E4M3 and E2M2 stay on the
 //   3-CTA register pipeline, which measured equal or better.
+// - Entry lookahead: where registers allow (2 CTAs per SM), a thread
+//   requests the table entry of the tile after its next one a whole tile
+//   ahead, so that only the descriptor load stands between a tile's entry
+//   and its data requests.
 template <int GT, int COMBO, int ALGO, bool SR>
 struct StepShape {
   static constexpr int kMinBlocks =
       (GT == OPT_BF16 && !SR && (COMBO == SC_BF16_E4M3 || COMBO == SC_BF16_E2M2)) ? 3 : 2;
   static constexpr bool kPersistent = ALGO != ALGO_ADEMAMIX;
   static constexpr bool kBulk = COMBO != SC_F32 && ALGO == ALGO_ADAMW && (SR || COMBO == SC_BF16_BF16);
+  static constexpr bool kLookahead = kPersistent && kMinBlocks == 2;
 };
 
 template <int COMBO>
@@ -397,10 +402,14 @@ step_kernel(const StepArgs a) {
   const opt_step_scalars& sc = DEVSC ? sc_dev : a.sc;
   const bool count = a.unchanged != nullptr;
   const bool reset = a.reset != 0;
+  constexpr bool LA = StepShape<GT, COMBO, ALGO, SR>::kLookahead;
   const int off = threadIdx.x * 8;
   int64_t i = a.tile_begin + blockIdx.x;
-  opt_chunk tl;
+  opt_chunk tl, la;     // la: with LA, the entry of tile i + gridDim.x, requested a tile early
+  if (LA && i + gridDim.x < a.tile_end) la = a.tiles[i + gridDim.x];
+  const int64_t i0 = i;
   bool have = next_tile(i, a, off, tl);
+  if (LA && have && i != i0 && i + gridDim.x < a.tile_end) la = a.tiles[i + gridDim.x];   // rare: skipped
 
   Frag<GT, COMBO, ALGO> cur, nxt;
   TensorDesc ctd;
@@ -420,7 +429,23 @@ step_kernel(const StepArgs a) {
     // request the next group before working on the current one
     int64_t j = i + gridDim.x;
     opt_chunk ntl;
-    const bool have_next = next_tile(j, a, off, ntl);
+    bool have_next;
+    if constexpr (LA) {
+      have_next = false;
+      if (j < a.tile_end) {
+        ntl = la;
+        if (j + gridDim.x < a.tile_end) la = a.tiles[j + gridDim.x];
+        have_next = off < (int)ntl.len;
+        if (!have_next) {
+          // rare: no group of this thread in that tile (a tensor's short last tile)
+          j += gridDim.x;
+          have_next = next_tile(j, a, off, ntl);
+          if (have_next && j + gridDim.x < a.tile_end) la = a.tiles[j + gridDim.x];
+        }
+      }
+    } else {
+      have_next = next_tile(j, a, off, ntl);
+    }
     TensorDesc ntd;
     int64_t ne0 = 0;
     int ncnt = 0;
