@@ -468,7 +468,15 @@ def run_ours(args, rank, local_rank, world):
         plan_b.close()
         del host, grads_b
 
-    # per-step distribution (norm + step, CUDA events on the launching stream)
+    # per-step distribution (norm + step, CUDA events on the launching stream);
+    # every sample goes to a JSONL file beside the clock samples
+    out_dir = os.environ.get("BENCH_OUT_DIR", os.path.join(ROOT, "bench_out"))
+    os.makedirs(out_dir, exist_ok=True)
+    with open(os.path.join(out_dir, f"steps_rank{rank}.jsonl"), "w") as fh:
+        for k, e in enumerate(evs):
+            fh.write(json.dumps({"workload": w.name, "timed_step": k, "norm_ms": round(norm_ms[k], 5),
+                                 "step_ms": round(step_ms[k], 5),
+                                 "total_ms": round(e[0].elapsed_time(e[2]), 5)}) + "\n")
     per_step = sorted(e[0].elapsed_time(e[2]) for e in evs)
 
     def pct(q):
