@@ -61,12 +61,16 @@ class OracleSide:
     a slice is element start + k of its tensor, which selects its
     stochastic-rounding draws."""
 
-    def __init__(self, gpu: GpuSide, samples):
+    def __init__(self, gpu: GpuSide, samples, track_moves: bool = False):
         self.w = gpu.w
         self.v_scale = gpu.v_scale
         self.samples = [(s, 0, gpu.w.sizes[s]) if isinstance(s, int) else tuple(s) for s in samples]
         self.idx = [i for i, _, _ in self.samples]
         self.p = [W.to_numpy_codes(self.cut(gpu.params, k, "f32")) for k in range(len(self.samples))]
+        # with track_moves: per element, the sums over steps of |p_t - p_(t-1)|
+        # and of max(|p_(t-1)|, |p_t|) in the oracle (see update_bound)
+        self.moved = [np.zeros(a.size) for a in self.p] if track_moves else None
+        self.mag = [np.zeros(a.size) for a in self.p] if track_moves else None
         self.m = [W.to_numpy_codes(self.cut(gpu.m, k, self.w.m_dtype)) for k in range(len(self.samples))]
         self.v = [W.to_numpy_codes(self.cut(gpu.v, k, self.w.v_dtype)) for k in range(len(self.samples))]
         self.m2 = ([W.to_numpy_codes(self.cut(gpu.m2, k, self.w.m_dtype)) for k in range(len(self.samples))]
@@ -96,18 +100,29 @@ class OracleSide:
                 m2=None if self.m2 is None else self.m2[k], m_dtype=self.w.m_dtype,
                 v_dtype=self.w.v_dtype, coef=coef, stochastic=stochastic, seed=seed, tensor_index=i,
                 index_base=start, v_scale=1.0 if self.v_scale is None else self.v_scale[i])
+        before = [a.astype(np.float64) for a in self.p] if self.moved is not None else None
         if threads <= 1:
-            return sum(one(k) for k in range(len(self.samples)))
-        with ThreadPoolExecutor(max_workers=threads) as ex:
-            return sum(ex.map(one, range(len(self.samples))))
+            same = sum(one(k) for k in range(len(self.samples)))
+        else:
+            with ThreadPoolExecutor(max_workers=threads) as ex:
+                same = sum(ex.map(one, range(len(self.samples))))
+        if before is not None:
+            for k, b in enumerate(before):
+                now = self.p[k].astype(np.float64)
+                self.moved[k] += np.abs(now - b)
+                self.mag[k] += np.maximum(np.abs(now), np.abs(b))
+        return same
 
-    def compare(self, gpu: GpuSide, tol: float, exact_codes: bool):
-        """FP32 values within tol (1+|x|); low-precision codes identical
+    def compare(self, gpu: GpuSide, tol: float, exact_codes: bool, steps: int = 0):
+        """FP32 values within tol (1+|x|) -- for p past 100 steps, when moves
+        are tracked, plus update_bound; low-precision codes identical
         (exact_codes) or >= 99.99 % identical and one step off."""
         w = self.w
         for k, (i, start, n) in enumerate(self.samples):
             what = f"tensor {i} [{start}:{start + n}]"
-            assert_close_scaled(W.to_numpy_codes(self.cut(gpu.params, k, "f32")), self.p[k], tol, "p " + what)
+            extra = update_bound(self.moved[k], self.mag[k]) if self.moved is not None and steps > 100 else None
+            assert_close_scaled(W.to_numpy_codes(self.cut(gpu.params, k, "f32")), self.p[k], tol, "p " + what,
+                                extra)
             gm = W.to_numpy_codes(self.cut(gpu.m, k, w.m_dtype))
             gv = W.to_numpy_codes(self.cut(gpu.v, k, w.v_dtype))
             if w.m_dtype == "f32":
@@ -121,14 +136,49 @@ class OracleSide:
                                     "m2 " + what)
 
 
+def fp32_tol(t: int) -> float:
+    """Tolerance on FP32 values, scaled as tol * (1 + |x|), after t steps.
+
+    1e-6 after one step and 1e-5 up to 100 steps are the stated bounds.  Past
+    100 steps the dominant difference is systematic: the kernel multiplies p
+    by the decay factor 1 - lr wd rounded once to fp32 (at most 2^-25 off,
+    relative, for a factor in [1/2, 1)), the oracle by the factor in double,
+    so after t steps p differs by up to t 2^-25 relative from that alone.
+    The bound adds that term: 1e-5 + t 2^-25 (4.0e-5 at t = 1000)."""
+    if t <= 1:
+        return 1e-6
+    if t <= 100:
+        return 1e-5
+    return 1e-5 + t * 2.0 ** -25
+
+
+def update_bound(moved: np.ndarray, mag: np.ndarray) -> np.ndarray:
+    """Second term of the FP32 bound on p past 100 steps, per element.
+
+    Each step the kernel forms the update lr u in fp32 with the approximate
+    square root and reciprocal of sm_103a (a few ulp in all), and rounds
+    p (1 - lr wd), lr u and their difference separately; the oracle computes
+    the step in double and rounds p once.  So every step can put p up to
+    about 2^-21 |lr u| + 1.5 ulp(max(|p_(t-1)|, |p_t|)) away from the oracle,
+    and the differences stay when p later shrinks.  Where a low-precision v
+    sits at zero (unscaled E4M3 / E2M2 v below half its first grid step) the
+    update is m / (sqrt(v_t) + eps) with v_t from the current gradient alone,
+    and both the update and p can grow far beyond p's start.  The bound is
+    2^-20 times the oracle's own sum over steps of |p_t - p_(t-1)| (`moved`)
+    plus 2^-22 times its sum of max(|p_(t-1)|, |p_t|) (`mag`)."""
+    return moved * 2.0 ** -20 + mag * 2.0 ** -22
+
+
 def run_lockstep(w, steps, tol, samples=None, rounding="nearest", seed=0, hp_seed=77, count=False,
-                 checkpoints=(), norm_threads=16, gpu=None, step_threads=1):
+                 checkpoints=(), norm_threads=16, gpu=None, step_threads=1, track_moves=False):
     """Run `steps` steps of workload `w` on the GPU (whole list, clip from the
     GPU's own norm when w.max_norm > 0) and on the oracle (its own norm over
     every gradient, the step on `samples`), comparing the norms every step and
-    the sampled states at each checkpoint and at the end."""
+    the sampled states at each checkpoint and at the end.  `tol` is a number,
+    or a function of the step count (such as fp32_tol)."""
+    tol_at = tol if callable(tol) else (lambda _t: tol)
     gpu = gpu or GpuSide(w, seed=seed)
-    orc = OracleSide(gpu, range(len(w.sizes)) if samples is None else samples)
+    orc = OracleSide(gpu, range(len(w.sizes)) if samples is None else samples, track_moves=track_moves)
     ghp, ohp = hp_for(w, rounding=rounding, seed=hp_seed, count=count)
     sr = rounding == "stochastic"
     clip = w.max_norm > 0
@@ -151,9 +201,9 @@ def run_lockstep(w, steps, tol, samples=None, rounding="nearest", seed=0, hp_see
             counts.append((gpu.plan.unchanged_count(), same))
         if t in checkpoints:
             torch.cuda.synchronize()
-            orc.compare(gpu, tol, sr)
+            orc.compare(gpu, tol_at(t), sr, steps=t)
     torch.cuda.synchronize()
-    orc.compare(gpu, tol, sr)
+    orc.compare(gpu, tol_at(steps), sr, steps=steps)
     assert gpu.plan.status() == 0, "a kernel reported a bounded wait that ran out"
     return gpu, orc, counts
 
@@ -173,12 +223,15 @@ def rel_err(a: float, b: float) -> float:
     return abs(a - b) / max(abs(b), 1e-300)
 
 
-def assert_close_scaled(got: np.ndarray, want: np.ndarray, tol: float, what: str):
-    """max |got - want| <= tol * (1 + |want|), elementwise."""
+def assert_close_scaled(got: np.ndarray, want: np.ndarray, tol: float, what: str, extra=None):
+    """|got - want| <= tol * (1 + |want|) (+ extra, per element), elementwise."""
     got = np.asarray(got, dtype=np.float64)
     want = np.asarray(want, dtype=np.float64)
     assert got.shape == want.shape, what
-    bad = np.abs(got - want) > tol * (1.0 + np.abs(want))
+    bound = tol * (1.0 + np.abs(want))
+    if extra is not None:
+        bound = bound + extra
+    bad = np.abs(got - want) > bound
     bad |= np.isnan(got) != np.isnan(want)
     if bad.any():
         i = int(np.argmax(bad))

@@ -6,7 +6,8 @@ tensors and of slices of the large ones.
 * clip_740: 740 tensors, 197M params, BF16 grads, clip 1.0, 20 steps.
 * ademamix_gpt2: GPT-2-small list, 124M params, FP32 grads, 50 steps.
 * lowp_gpt2: the same list with BF16 m and BF16 / E4M3 / E2M2 v, nearest
-  and stochastic, plus the FP32 control; unchanged-v counts exact.
+  and stochastic, plus the FP32 control, all 1,000 steps; unchanged-v counts
+  exact.
 * llama3_8b: the 8.03e9-parameter list, all 5 steps; each step the norm over
   all of it and the clipped step on 16 sampled tensors (always the embedding
   and a 4096-vector).
@@ -17,7 +18,7 @@ import torch
 
 import precision_states_gb300 as ps
 import workloads as W
-from harness import GpuSide, OracleSide, hp_for, oracle_norm_parallel, rel_err, run_lockstep
+from harness import GpuSide, OracleSide, fp32_tol, hp_for, oracle_norm_parallel, rel_err, run_lockstep
 
 pytestmark = pytest.mark.gpu
 
@@ -66,13 +67,15 @@ def test_ademamix_gpt2_fifty_steps():
 @pytest.mark.parametrize("mode", ["f32", "bf16-nearest", "bf16-stochastic", "e4m3-nearest",
                                   "e4m3-stochastic", "e2m2-nearest", "e2m2-stochastic"])
 def test_lowp_gpt2_modes(mode):
-    """All seven state modes of the low-precision workload, 120 of its 1,000
-    steps (the grad scale falls 10x over the full 1,000; here over 120 so the
-    whole decay is exercised), full list on the GPU, codes compared on a
-    sample.  The unchanged-v count is checked exactly on a second plan over
-    the sampled tensors alone."""
+    """All seven state modes of the low-precision workload over all of its
+    1,000 steps (the grad scale falls 10x linearly over them), full list on
+    the GPU, codes compared on a sample at steps 1, 10, 100, 500 and 1,000,
+    FP32 values within fp32_tol of the step count (p past 100 steps also
+    within update_bound of the oracle's own moves).  The unchanged-v count is
+    checked exactly on a second plan over the sampled tensors alone."""
     vd, _, rnd = mode.partition("-")
-    w = W.workload("lowp_gpt2", sigma_decay_steps=120)
+    w = W.workload("lowp_gpt2")
+    assert w.steps == 1000 and w.sigma_decay_steps == 1000
     if vd == "f32":
         w.m_dtype = w.v_dtype = "f32"
     else:
@@ -80,7 +83,8 @@ def test_lowp_gpt2_modes(mode):
     rounding = rnd or "nearest"
     small = [i for i, n in enumerate(w.sizes) if n < 10_000]
     samples = small[:6] + slices(w, seed=3, count=2, length=8192)
-    run_lockstep(w, 120, 1e-5, samples=samples, rounding=rounding, checkpoints=(1, 10, 60))
+    run_lockstep(w, w.steps, fp32_tol, samples=samples, rounding=rounding, checkpoints=(1, 10, 100, 500),
+                 track_moves=True)
     free()
     if vd == "f32":
         return   # FP32 v: the oracle forms v in double, so bitwise stalls need not match
