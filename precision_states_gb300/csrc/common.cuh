@@ -244,6 +244,10 @@ __device__ __forceinline__ void e2m2x2_dec(uint32_t pair16, float& first, float&
 // [0, 7/4]: NaN stores 7 (fminf returns its non-NaN operand), negative
 // values store 0, values at or above 7 saturate.  Callers pass x/4.
 __device__ __forceinline__ float e2m2_clamp_q(float x4) { return fmaxf(fminf(x4, 1.75f), 0.0f); }
+// The step's v is never negative (b2 v + (1 - b2) g^2 with v, b2, 1 - b2 >= 0,
+// or NaN), so there only the upper clamp is needed.
+template <bool NONNEG>
+__device__ __forceinline__ float e2m2_clamp_q(float x4) { return NONNEG ? fminf(x4, 1.75f) : e2m2_clamp_q(x4); }
 
 // Nearest, two values at a time: unsigned E2M2 is the FP6 E3M2 grid scaled
 // by 4 (E3M2 subnormals k/16 are E2M2's k/4 over 4; its binades with
@@ -252,9 +256,11 @@ __device__ __forceinline__ float e2m2_clamp_q(float x4) { return fmaxf(fminf(x4,
 // in the low bits of each byte (sign and exponent bits above are 0).
 // Arguments are the quarter values lo4 = lo/4, hi4 = hi/4; returns the pair
 // (lo | hi << 8).
+template <bool NONNEG = false>
 __device__ __forceinline__ uint32_t e2m2x2_rn_q(float lo4, float hi4) {
   unsigned short r;
-  asm("cvt.rn.satfinite.e3m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(e2m2_clamp_q(hi4)), "f"(e2m2_clamp_q(lo4)));
+  asm("cvt.rn.satfinite.e3m2x2.f32 %0, %1, %2;"
+      : "=h"(r) : "f"(e2m2_clamp_q<NONNEG>(hi4)), "f"(e2m2_clamp_q<NONNEG>(lo4)));
   return (uint32_t)r;
 }
 
@@ -317,10 +323,12 @@ __device__ __forceinline__ uint32_t e4m3x2_sr(float lo, float hi, uint32_t rbits
 // Unsigned E2M2, stochastic: the E3M2 grid of the quarter values (as in
 // e2m2x2_rn_q), after the clamp (7/4 lies on the grid, so no draw moves a
 // saturated value).  The pair (lo | hi << 8), codes 0-15.
+template <bool NONNEG = false>
 __device__ __forceinline__ uint32_t e2m2x2_sr_q(float lo4, float hi4, uint32_t rbits) {
   uint32_t d;
   asm("cvt.rs.satfinite.e3m2x4.f32 %0, {%1, %2, %3, %4}, %5;"
-      : "=r"(d) : "f"(0.0f), "f"(e2m2_clamp_q(hi4)), "f"(0.0f), "f"(e2m2_clamp_q(lo4)), "r"(rbits));
+      : "=r"(d)
+      : "f"(0.0f), "f"(e2m2_clamp_q<NONNEG>(hi4)), "f"(0.0f), "f"(e2m2_clamp_q<NONNEG>(lo4)), "r"(rbits));
   return __byte_perm(d, 0u, 0x4420);
 }
 

@@ -8,10 +8,10 @@
 // warps fit on an SM and few bytes are in flight per warp.  Here the words
 // in flight live in shared memory:
 //   - a CTA has kStepThreads consumer threads (8 warps) and one producer
-//     warp, and a ring of kBulkStages stages, each holding one whole tile
+//     warp, and a ring of S stages (4 or 5), each holding one whole tile
 //     (2048 elements of p, g, m, v) and a header (the tile's table entry and
 //     its tensor's descriptor);
-//   - the producer (lane 0 of the last warp) runs up to kBulkStages tiles
+//   - the producer (lane 0 of the last warp) runs up to S tiles
 //     ahead: it waits for a stage to be released, writes the header, and
 //     requests the tile with four cp.async.bulk copies completing on the
 //     stage's "full" mbarrier (expect_tx with the byte count);
@@ -34,20 +34,26 @@
 
 namespace psopt {
 
-constexpr int kBulkStages = 4;
+constexpr int kSmemPerSm = 228 * 1024;                      // shared memory per SM
+constexpr int kSmemReservedPerCta = 1024;                   // the runtime's share of each CTA
 constexpr int kBulkConsumers = kStepThreads / 32;          // consumer warps
 constexpr int kBulkThreads = kStepThreads + 32;            // + the producer warp
 constexpr unsigned long long kWaitNs = 2000000000ull;      // 2 s
 
-// Shared-memory layout: barriers, then kBulkStages stages of
-// {header, p, g, m, v}; every part a multiple of 16 bytes.
+// Shared-memory layout: barriers, then S stages of {header, p, g, m, v};
+// every part a multiple of 16 bytes.  S is 4, or 5 for BF16 v with nearest
+// rounding where two CTAs still fit on an SM.  Measured on GB300 (GPT-2
+// list, A/B/A/B on two boxes): a fifth stage lifted nearest BF16 v by
+// 0.8-1.8 %, to 0.991-1.003 of the measured copy bandwidth; for the
+// stochastic modes five or six stages cost 2-3 % (E2M2 0.927 -> 0.900, E4M3
+// 0.967 -> 0.943, BF16 0.997 -> 0.981).
 struct BulkHeader {
   opt_chunk tl;
   TensorDesc td;
 };
 static_assert(sizeof(BulkHeader) == 80, "BulkHeader layout");
 
-template <int GT, int COMBO>
+template <int GT, int COMBO, bool SR>
 struct BulkLayout {
   static constexpr int VD = Combo<COMBO>::V;
   static constexpr int N = (int)kTileElems;
@@ -58,8 +64,11 @@ struct BulkLayout {
   static constexpr int V = VD == OPT_BF16 ? 2 * N : VD == OPT_E4M3 ? N : N / 2;
   static constexpr int OFF_P = HDR, OFF_G = OFF_P + P, OFF_M = OFF_G + G, OFF_V = OFF_M + M;
   static constexpr int STAGE = OFF_V + V;
-  static constexpr int BAR_BYTES = 16 * kBulkStages;       // full[S], then empty[S]
-  static constexpr int BYTES = BAR_BYTES + STAGE * kBulkStages;
+  static constexpr bool fits(int s) { return 2 * (16 * s + STAGE * s + kSmemReservedPerCta) <= kSmemPerSm; }
+  static constexpr int S = (!SR && COMBO == SC_BF16_BF16 && fits(5)) ? 5 : 4;
+  static_assert(fits(S), "two CTAs per SM");
+  static constexpr int BAR_BYTES = 16 * S;                  // full[S], then empty[S]
+  static constexpr int BYTES = BAR_BYTES + STAGE * S;
   static_assert(STAGE % 16 == 0 && BAR_BYTES % 16 == 0, "bulk copy alignment");
   static_assert(kStepThreads * 8 == N, "one tile per stage");
 };
@@ -125,9 +134,9 @@ __device__ __forceinline__ uint32_t lds_u1(uint32_t a) {
 template <int GT, int COMBO, bool SR>
 __global__ void __launch_bounds__(kBulkThreads, 2)
 step_bulk_kernel(const StepArgs a) {
-  using L = BulkLayout<GT, COMBO>;
+  using L = BulkLayout<GT, COMBO, SR>;
   using F = Frag<GT, COMBO, ALGO_ADAMW>;
-  constexpr int S = kBulkStages;
+  constexpr int S = L::S;
   extern __shared__ __align__(128) unsigned char smem[];
   if (a.d_norm != nullptr && a.d_norm->status != OPT_OK) return;   // non-finite norm: leave all untouched
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -256,7 +265,7 @@ cudaError_t launch_bulk(const StepArgs& a, int sm_count, cudaStream_t s) {
   const int64_t n = a.tile_end - a.tile_begin;
   if (n <= 0) return cudaSuccess;
   auto k = step_bulk_kernel<GT, COMBO, SR>;
-  constexpr int bytes = BulkLayout<GT, COMBO>::BYTES;
+  constexpr int bytes = BulkLayout<GT, COMBO, SR>::BYTES;
   static OccupancyCache occ;
   const int per_sm = cached_occupancy(k, occ, kBulkThreads, bytes);
   if (per_sm < 1) return cudaGetLastError();

@@ -302,7 +302,7 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
     if constexpr (MD == OPT_BF16) mpair[k] = bf16x2_enc<SR>(mnv[2 * k], mnv[2 * k + 1], rm);
     if constexpr (VD == OPT_BF16) vpair[k] = bf16x2_enc<SR>(v0, v1, rv);
     if constexpr (VD == OPT_E4M3) vpair[k] = SR ? e4m3x2_sr(v0, v1, rv) : e4m3x2_rn(v0, v1);
-    if constexpr (VD == OPT_E2M2) vpair[k] = SR ? e2m2x2_sr_q(v0, v1, rv) : e2m2x2_rn_q(v0, v1);
+    if constexpr (VD == OPT_E2M2) vpair[k] = SR ? e2m2x2_sr_q<true>(v0, v1, rv) : e2m2x2_rn_q<true>(v0, v1);
   }
   // code of element j in the pair words
   auto vcode_at = [&](int j) -> uint32_t {
