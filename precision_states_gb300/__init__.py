@@ -298,5 +298,14 @@ class Plan:
         return out.value
 
     def grads_upload(self, host_grads, stream=None):
+        """Copy host gradients (one tensor per list entry, the plan's sizes and
+        gradient dtypes) into the plan's device gradients on `stream`."""
+        if len(host_grads) != len(self.numel):
+            raise ValueError("host gradient list differs in length from the plan's")
+        for i, t in enumerate(host_grads):
+            want = 2 if self.grad_dtype[i] == OPT_BF16 else 4
+            if t.numel() != self.numel[i] or t.element_size() != want or not t.is_contiguous():
+                raise ValueError(f"host gradient {i}: expected {self.numel[i]} contiguous elements of "
+                                 f"{want} bytes")
         arr = (_vp * max(len(host_grads), 1))(*[t.data_ptr() for t in host_grads])
         _check(lib().opt_grads_upload(self.handle, arr, _stream_ptr(stream)), "opt_grads_upload")

@@ -458,3 +458,38 @@ def test_device_step_counter_rejects():
     with pytest.raises(ps.OptError) as e:
         low.plan.adamw_step(hp, 0)
     assert e.value.status == ps.OPT_EUNSUPPORTED
+
+
+def test_grads_upload_copies_every_tensor_exactly():
+    """opt_grads_upload: host gradients (pinned and pageable, BF16 and FP32,
+    zero-size and one-element tensors) land in the plan's device gradients
+    bit for bit, on a side stream; the norm over them equals the oracle's.
+    The binding rejects a host list that does not match the plan."""
+    sizes = [4096, 0, 1, 2048 * 3 + 17, 5]
+    w = W.Workload("upload", sizes, "bf16", steps=1, max_norm=1.0, p_std=0.02, grad_std=1.0)
+    gpu = GpuSide(w, seed=3)
+    gpu.grads[2] = torch.empty(1, dtype=torch.float32, device="cuda")
+    gpu.grads[4] = torch.empty(5, dtype=torch.float32, device="cuda")
+    gpu.plan.close()
+    gpu.plan = ps.Plan(gpu.params, gpu.grads, gpu.m, gpu.v)
+    gen = torch.Generator().manual_seed(11)
+    host = []
+    for i, g in enumerate(gpu.grads):
+        h = torch.randn(g.numel(), generator=gen).to(g.dtype)
+        host.append(h.pin_memory() if i % 2 == 0 else h)
+    side = torch.cuda.Stream()
+    gpu.plan.grads_upload(host, stream=side)
+    side.synchronize()
+    for h, g in zip(host, gpu.grads):
+        assert torch.equal(g.cpu().view(torch.int16 if g.dtype == torch.bfloat16 else torch.int32),
+                           h.view(torch.int16 if h.dtype == torch.bfloat16 else torch.int32))
+    got = gpu.plan.grad_norm(1.0)
+    want = oracle.grad_norm([W.to_numpy_codes(h) for h in host], 1.0)
+    assert abs(got.norm2 - want["norm2"]) <= 1e-12 * want["norm2"] and got.clip_coef == want["clip_coef"]
+    with pytest.raises(ValueError):
+        gpu.plan.grads_upload(host[:-1])
+    with pytest.raises(ValueError):
+        gpu.plan.grads_upload(host[:-1] + [torch.zeros(4, dtype=torch.float32)])
+    with pytest.raises(ValueError):
+        gpu.plan.grads_upload([host[0].float()] + host[1:])
+    gpu.plan.close()
