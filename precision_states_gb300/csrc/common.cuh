@@ -352,6 +352,11 @@ __device__ __forceinline__ float div_approx(float a, float b) {
   asm("div.approx.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
   return r;
 }
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
 __device__ __forceinline__ float div_full(float a, float b) {
   float r;
   asm("div.full.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
