@@ -51,6 +51,19 @@ def step_bytes_per_param(w) -> float:
     return b
 
 
+def resident_bytes(w) -> float:
+    """Bytes one step's inputs occupy: p, g, m, v (and m2)."""
+    per = (4 + ELEM_BYTES[w.grad_dtype] + ELEM_BYTES[w.m_dtype] + ELEM_BYTES[w.v_dtype]
+           + (ELEM_BYTES[w.m_dtype] if w.algo == "ademamix" else 0))
+    return per * w.numel
+
+
+def needs_l2_flush(w) -> bool:
+    """A list whose inputs come to less than four times L2 is flushed from L2
+    before every timed step; larger ones stream from HBM anyway."""
+    return resident_bytes(w) < 4 * L2_BYTES
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -292,9 +305,7 @@ def run_ours(args, rank, local_rank, world):
     # that L2 holds neither the step's data nor dirty lines of the flush.
     # Such steps are timed by their own events (norm start to step end), so
     # the flush stays out of the figure.
-    resident = sum(n * (4 + ELEM_BYTES[w.grad_dtype] + ELEM_BYTES[w.m_dtype] + ELEM_BYTES[w.v_dtype]
-                        + (ELEM_BYTES[w.m_dtype] if w.algo == "ademamix" else 0)) for n in w.sizes)
-    flush = resident < 4 * L2_BYTES
+    flush = needs_l2_flush(w)
     if flush:
         flush_w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
         flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)

@@ -25,3 +25,35 @@ def test_reference_arm_prints_the_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """Launched as the multi-GPU bench is (torch.distributed.run, two ranks,
+    127.0.0.1), only rank 0 runs the oracle and prints; the other rank exits
+    0 without work."""
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+                        "--master-addr", "127.0.0.1", "--master-port", "29533",
+                        os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                        "--workload", "sweep", "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip().startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+
+
+def test_l2_flush_only_for_lists_that_fit():
+    """bench.py flushes L2 before each timed step only where the step's
+    inputs would otherwise stay in it: the 1M-parameter list (16.8 MB), not
+    the 740-tensor, GPT-2 or Llama-3-8B lists."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    assert bench.resident_bytes(W.workload("adamw_1m")) == 16 * (1 << 20)
+    assert bench.needs_l2_flush(W.workload("adamw_1m"))
+    for name in ("clip_740", "ademamix_gpt2", "lowp_gpt2", "llama3_8b"):
+        assert not bench.needs_l2_flush(W.workload(name)), name
+    w = W.workload("lowp_gpt2")
+    w.v_dtype = "e2m2"
+    assert not bench.needs_l2_flush(w)
