@@ -144,3 +144,44 @@ def test_single_tensor_beyond_32bit_indexing():
     orc.compare(gpu, 1e-6, True)
     del gpu, orc
     free()
+
+
+def _omb(beta: float) -> np.float32:
+    """(1 - beta) as the step forms it: in double from the fp32 beta, rounded once."""
+    return np.float32(1.0 - float(np.float32(beta)))
+
+
+@pytest.mark.parametrize("name,states", [("clip_740", "f32"), ("lowp_gpt2", "bf16")])
+def test_every_element_updated_exactly_once(name, states):
+    """One step from zero moments over a whole list: every element's new m
+    and v must equal (1-b1) g' and (1-b2) g'^2 (g' = g times the clip
+    coefficient), bit for bit, in every tensor -- an element skipped would
+    keep 0, one updated twice would not match.  The 740-tensor list runs the
+    register-pipelined FP32 kernel (about 317 tiles per CTA, 740 short
+    tiles); the GPT-2 list with BF16 m and v (nearest) the staged kernel.
+    Reference values are torch fp32 operations (round to nearest, and for
+    BF16 codes torch's nearest-even cast), the same operations in the same
+    order."""
+    w = W.workload(name)
+    if states == "bf16":
+        w.v_dtype = "bf16"
+    gpu = GpuSide(w, seed=21)
+    hp, _ = hp_for(w)
+    clip = w.max_norm > 0
+    gpu.step(1, hp, clip)
+    coef = np.float32(gpu.plan.grad_norm(w.max_norm).clip_coef) if clip else np.float32(1.0)
+    omb1, omb2 = _omb(0.9), _omb(w.hp.get("beta2", 0.999))
+    for i, g in enumerate(gpu.grads):
+        ge = g.float() * torch.tensor(coef, device="cuda")
+        # + 0.0: the kernel adds b * 0 = +0 first, which turns a -0 into +0
+        m_want = ge * torch.tensor(omb1, device="cuda") + 0.0
+        v_want = (ge * ge) * torch.tensor(omb2, device="cuda") + 0.0
+        if states == "f32":
+            assert torch.equal(gpu.m[i].view(torch.int32), m_want.view(torch.int32)), f"m of tensor {i}"
+            assert torch.equal(gpu.v[i].view(torch.int32), v_want.view(torch.int32)), f"v of tensor {i}"
+        else:
+            assert torch.equal(gpu.m[i], m_want.to(torch.bfloat16).view(torch.int16)), f"m of tensor {i}"
+            assert torch.equal(gpu.v[i], v_want.to(torch.bfloat16).view(torch.int16)), f"v of tensor {i}"
+    assert gpu.plan.status() == 0
+    del gpu
+    free()
