@@ -151,14 +151,16 @@ def _omb(beta: float) -> np.float32:
     return np.float32(1.0 - float(np.float32(beta)))
 
 
-@pytest.mark.parametrize("name,states", [("clip_740", "f32"), ("lowp_gpt2", "bf16")])
+@pytest.mark.parametrize("name,states", [("clip_740", "f32"), ("lowp_gpt2", "bf16"), ("llama3_8b", "f32")])
 def test_every_element_updated_exactly_once(name, states):
     """One step from zero moments over a whole list: every element's new m
     and v must equal (1-b1) g' and (1-b2) g'^2 (g' = g times the clip
     coefficient), bit for bit, in every tensor -- an element skipped would
     keep 0, one updated twice would not match.  The 740-tensor list runs the
     register-pipelined FP32 kernel (about 317 tiles per CTA, 740 short
-    tiles); the GPT-2 list with BF16 m and v (nearest) the staged kernel.
+    tiles); the GPT-2 list with BF16 m and v (nearest) the staged kernel;
+    the Llama-3-8B list (8.03e9 elements, the benchmark's launch) the FP32
+    kernel again, with about 12,900 tiles per CTA.
     Reference values are torch fp32 operations (round to nearest, and for
     BF16 codes torch's nearest-even cast), the same operations in the same
     order."""
