@@ -177,3 +177,46 @@ def test_two_plans_on_two_streams_concurrently():
         assert rel_err(rb.norm2, want_b["norm2"]) <= TOL and rb.clip_coef == want_b["clip_coef"]
     pa.close()
     pb.close()
+
+
+def _noalloc_norm(grads, max_norm, d_out):
+    import ctypes
+    n = len(grads)
+    numel = (ctypes.c_int64 * max(n, 1))(*[g.numel() for g in grads])
+    ptrs = (ctypes.c_void_p * max(n, 1))(*[g.data_ptr() for g in grads])
+    dts = (ctypes.c_int32 * max(n, 1))(*[ps.OPT_BF16 if g.dtype == torch.bfloat16 else ps.OPT_F32 for g in grads])
+    assert ps.lib().opt_grad_norm_noalloc(n, numel, ptrs, dts, max_norm, d_out.data_ptr(), None) == ps.OPT_OK
+    torch.cuda.synchronize()
+    return ps.opt_norm_result.from_buffer_copy(bytes(d_out.cpu().numpy()))
+
+
+@pytest.mark.parametrize("name", ["clip_740", "llama3_8b", "mixed"])
+def test_norm_counts_every_element_once(name):
+    """Every gradient element enters the norm exactly once, over whole lists:
+    with BF16 gradients all 1 and FP32 gradients all 2, the sum of squares is
+    an integer (exact in the float-float and fp64 accumulators) and must equal
+    N_bf16 + 4 N_f32; a chunk skipped, summed twice or counted in the wrong
+    bucket changes it by at least 1.  The plan and the no-allocation paths
+    both."""
+    if name == "mixed":
+        sizes = [32768 * 3 + 5, 1, 70001, 32768, 32767, 4097, 0, 9]
+        dts = [torch.bfloat16 if i % 2 == 0 else torch.float32 for i in range(len(sizes))]
+    else:
+        w = W.workload(name)
+        sizes = w.sizes
+        dts = [torch.bfloat16] * len(sizes)
+    grads = [torch.full((n,), 1.0 if dt == torch.bfloat16 else 2.0, dtype=dt, device="cuda")
+             for n, dt in zip(sizes, dts)]
+    want = float(sum(n if dt == torch.bfloat16 else 4 * n for n, dt in zip(sizes, dts)))
+    assert want < 2.0 ** 53
+    plan = plan_for(grads)
+    got = plan.grad_norm(0.0)
+    assert got.sumsq == want and got.norm2 == math.sqrt(want), (got.sumsq, want)
+    assert got.norm_inf == (2.0 if torch.float32 in dts else 1.0)
+    assert got.nan_count == 0 and got.inf_count == 0 and got.status == 0
+    plan.close()
+    del plan
+    torch.cuda.empty_cache()
+    d_out = torch.zeros(48, dtype=torch.uint8, device="cuda")
+    na = _noalloc_norm(grads, 0.0, d_out)
+    assert na.sumsq == want and na.norm_inf == got.norm_inf
