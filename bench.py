@@ -571,7 +571,7 @@ def run_reference(args, rank, world):
             "data": "synthetic",
             "config": {"workload": w.name, "tensors": len(w.sizes), "params_per_gpu": w.numel,
                        "grad_dtype": w.grad_dtype, "m_dtype": w.m_dtype, "v_dtype": w.v_dtype,
-                       "clip_max_norm": w.max_norm, "parallelism": "replicas1",
+                       "clip_max_norm": w.max_norm, "parallelism": f"replicas{world}",
                        "sampled_params_per_step": smp.numel},
             "cpu_baseline": cb,
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
