@@ -571,6 +571,7 @@ def run_reference(args, rank, world):
             "data": "synthetic",
             "config": {"workload": w.name, "tensors": len(w.sizes), "params_per_gpu": w.numel,
                        "grad_dtype": w.grad_dtype, "m_dtype": w.m_dtype, "v_dtype": w.v_dtype,
+                       "rounding": args.rounding, "algo": w.algo,
                        "clip_max_norm": w.max_norm, "parallelism": f"replicas{world}",
                        "sampled_params_per_step": smp.numel},
             "cpu_baseline": cb,
