@@ -31,8 +31,12 @@ def test_reference_arm_under_torchrun_prints_once():
     """Launched as the multi-GPU bench is (torch.distributed.run, two ranks,
     127.0.0.1), only rank 0 runs the oracle and prints; the other rank exits
     0 without work."""
+    import socket
+    with socket.socket() as sock:              # a free port for the rendezvous
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
     r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
-                        "--master-addr", "127.0.0.1", "--master-port", "29533",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port),
                         os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
                         "--workload", "sweep", "--steps", "1", "--warmup", "0"],
                        capture_output=True, text=True, timeout=600, cwd=ROOT)
