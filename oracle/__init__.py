@@ -33,6 +33,8 @@ _HDR = os.path.join(_HERE, "oracle.h")
 
 F32, BF16, E4M3, E2M2, F64 = 0, 1, 2, 3, 4
 ADAMW, ADEMAMIX = 0, 1
+# planted mistakes (ORC_MUT_* in oracle.h), for tests that show a pin is not vacuous
+MUT_DECAY_AFTER, MUT_U_FROM_CODES, MUT_NO_BIAS_CORR, MUT_SCALE_IN_SQRT = 1, 2, 4, 8
 
 _DT = {"f32": F32, "bf16": BF16, "e4m3": E4M3, "e2m2": E2M2, "f64": F64}
 
@@ -212,13 +214,14 @@ def adam_tensor(algo: int, p: np.ndarray, g: np.ndarray, m: np.ndarray, v: np.nd
                 hp: HParams, step: int, *, m2: np.ndarray | None = None, m_dtype="f32",
                 v_dtype="f32", coef: float = 1.0, stochastic: bool = False, seed: int = 0,
                 tensor_index: int = 0, index_base: int = 0, v_scale: float = 1.0,
-                decay_after: bool = False) -> int:
+                decay_after: bool = False, mutation: int = 0) -> int:
     """One step on one tensor, in place.  p: float32 (or float64 with every
     other array float64).  g: float32 or uint16 BF16 codes.  m/m2: float32 or
     uint16 BF16 codes.  v: float32, uint16 BF16, uint8 E4M3 codes, or uint8
     packed E2M2 (ceil(n/2) bytes).  Element i of the arrays is element
     index_base + i of the tensor (selects the stochastic-rounding draws).
-    Returns the count of v codes unchanged."""
+    `mutation` (MUT_* bits, 0 = the oracle) plants a mistake for tests that
+    show the pins catch it.  Returns the count of v codes unchanged."""
     for a in (p, g, m, v) + ((m2,) if m2 is not None else ()):
         if not a.flags["C_CONTIGUOUS"]:
             raise ValueError("arrays must be C-contiguous")
@@ -231,7 +234,7 @@ def adam_tensor(algo: int, p: np.ndarray, g: np.ndarray, m: np.ndarray, v: np.nd
         None if m2 is None else m2.ctypes.data, _DT[m_dtype] if p_dt != F64 else F64,
         v.ctypes.data, _DT[v_dtype] if p_dt != F64 else F64, ctypes.byref(hp), int(step),
         float(coef), int(stochastic), int(seed), int(tensor_index), int(index_base), float(v_scale),
-        int(decay_after),
+        int(mutation) | (MUT_DECAY_AFTER if decay_after else 0),
         ctypes.byref(unchanged))
     if rc != 0:
         raise ValueError("unsupported oracle combination")

@@ -290,8 +290,9 @@ void oracle_grad_norm(int32_t n, const int64_t* numel, const void* const* grads,
  *   v  <- b2 v  + (1-b2) g^2
  *   u  <- (m/(1-b1^t) [+ alpha m2]) / (sqrt(v/(1-b2^t)) + eps)
  *   p  <- p (1 - lr wd) - lr u             decay-first: both terms from old p
- * The wrong decay-after ordering, p <- (p - lr u)(1 - lr wd), is selectable
- * only so that tests can show the pins reject it.
+ * The wrong decay-after ordering, p <- (p - lr u)(1 - lr wd), and three
+ * plausible mistakes in the low-precision update (ORC_MUT_* in oracle.h) are
+ * selectable only so that tests can show the pins reject them.
  *
  * FP32 (and F64) states: every step is done in double from the stored values
  * and the results are rounded once to the storage type.
@@ -302,7 +303,10 @@ void oracle_grad_norm(int32_t n, const int64_t* numel, const void* const* grads,
  * operation at a time in this order, with no fused multiply-add:
  *   g' = g * coef;  m' = b1*m + omb1*g';  v' = b2*v + omb2*(g'*g')
  * where omb = (float)(1 - (double)b).  m' and v' are then encoded (nearest or
- * stochastic) and the parameter update is done in double from m' and v'.
+ * stochastic) and the parameter update is done in double from m' and v',
+ * the values before rounding: the fused step forms the update and the
+ * write-back from the same in-register value ("When Small Updates
+ * Disappear", sec. 8.1), never from the codes it has just rounded.
  * ====================================================================== */
 static double load_state(const void* s, int dtype, int64_t i) {
   switch (dtype) {
@@ -372,7 +376,7 @@ int oracle_adam_tensor(int algo, int64_t n,
                        void* v, int v_dtype,
                        const oracle_hparams* hp, int64_t step, float coef,
                        int stochastic, uint64_t seed, uint32_t tensor_index,
-                       int64_t index_base, double v_scale, int decay_after,
+                       int64_t index_base, double v_scale, int mutation,
                        int64_t* unchanged) {
   if (step < 1 || index_base < 0) return -1;
   if (v_dtype == ORC_E2M2 && (index_base & 1)) return -1;
@@ -428,18 +432,27 @@ int oracle_adam_tensor(int algo, int64_t n,
       if (stochastic)
         oracle_draws(seed, step, tensor_index, index_base + i, &r16_m, &r16_v);
     }
-    double num = m_new / bc1;
-    if (algo == ORC_ADEMAMIX) num += alpha * m2_new;
-    double u = num / (sqrt(v_new / bc2) + eps);
-    double pn = decay_after ? (pi - lr * u) * decay : pi * decay - lr * u;
-
-    if (wide) ((double*)p)[i] = pn;
-    else      ((float*)p)[i] = (float)pn;
     store_state(m, m_dtype, i, n, m_new, stochastic, r16_m);
     uint32_t new_code = store_state(v, v_dtype, i, n, lowp ? v_new / v_scale : v_new, stochastic, r16_v);
     if (algo == ORC_ADEMAMIX)
       store_state(m2, m_dtype, i, n, m2_new, stochastic, r16_m);
     if (!wide && new_code == old_code) ++same;
+
+    /* the update, from the new moments before rounding */
+    double mu = m_new, vu = v_new, c1 = bc1, c2 = bc2;
+    if (lowp && (mutation & ORC_MUT_U_FROM_CODES)) {
+      mu = load_state(m, m_dtype, i);
+      vu = load_state(v, v_dtype, i) * v_scale;
+    }
+    if (lowp && (mutation & ORC_MUT_SCALE_IN_SQRT)) vu = vu / v_scale;
+    if (lowp && (mutation & ORC_MUT_NO_BIAS_CORR)) c1 = c2 = 1.0;
+    double num = mu / c1;
+    if (algo == ORC_ADEMAMIX) num += alpha * m2_new;
+    double u = num / (sqrt(vu / c2) + eps);
+    double pn = (mutation & ORC_MUT_DECAY_AFTER) ? (pi - lr * u) * decay : pi * decay - lr * u;
+
+    if (wide) ((double*)p)[i] = pn;
+    else      ((float*)p)[i] = (float)pn;
   }
   if (unchanged) *unchanged = same;
   return 0;

@@ -96,12 +96,21 @@ enum { ORC_ADAMW = 0, ORC_ADEMAMIX = 1 };
  * must be even for E2M2).  v_scale (1 unless v is low precision): the v
  * code holds v / v_scale ("When Small Updates Disappear", sec. 2.3 and 5:
  * a coarse grid flushes a small second moment; a power-of-two scale moves v
- * onto the grid without changing the rounding rule).  `decay_after` != 0
- * selects the wrong,
- * decay-after ordering; it exists only so tests can show that the pins catch
- * it.  *unchanged (if non-NULL) receives the count of v codes (or f32 words)
- * left bitwise unchanged by this step.  Returns 0, or -1 on an unsupported
- * combination. */
+ * onto the grid without changing the rounding rule).  `mutation` is 0 for
+ * the oracle itself; its ORC_MUT_* bits each plant one plausible mistake,
+ * and exist only so that tests can show the pins catch it.  *unchanged (if
+ * non-NULL) receives the count of v codes (or f32 words) left bitwise
+ * unchanged by this step.  Returns 0, or -1 on an unsupported combination. */
+enum {
+  ORC_MUT_DECAY_AFTER = 1,    /* p <- (p - lr u)(1 - lr wd): the ordering the
+                                 decay-ordering PR fixed */
+  ORC_MUT_U_FROM_CODES = 2,   /* low-precision states: u from the re-decoded
+                                 stored codes, not the values before rounding */
+  ORC_MUT_NO_BIAS_CORR = 4,   /* low-precision states: u without 1/(1-b1^t) and
+                                 1/(1-b2^t) */
+  ORC_MUT_SCALE_IN_SQRT = 8   /* low-precision states: u from v / v_scale (the
+                                 stored value) instead of v */
+};
 int oracle_adam_tensor(int algo, int64_t n,
                        void* p, int p_dtype,
                        const void* g, int g_dtype,
@@ -109,7 +118,7 @@ int oracle_adam_tensor(int algo, int64_t n,
                        void* v, int v_dtype,
                        const oracle_hparams* hp, int64_t step, float coef,
                        int stochastic, uint64_t seed, uint32_t tensor_index,
-                       int64_t index_base, double v_scale, int decay_after,
+                       int64_t index_base, double v_scale, int mutation,
                        int64_t* unchanged);
 
 /* LAMB-style update-norm clipping of one tensor (FP32 states), in place:
