@@ -167,6 +167,18 @@ typedef struct opt_hparams {
  * host-numbered steps may be mixed; they do not see each other's numbers. */
 #define OPT_STEP_DEVICE_COUNTER 2
 
+/* Wait drill: make the staged step kernel's bounded waits run out on purpose,
+ * so that a caller can test its handling of OPT_FLAG_WAIT_TIMEOUT without a
+ * GPU fault.  The kernel's producer withholds each thread block's first tile
+ * (no copy is issued for it, and nothing completes its stage), so every
+ * consumer's first wait runs out after the plan's wait limit
+ * (opt_plan_set_wait_limit; set it short, say 1 ms, for a drill).  The step
+ * then processes no tile: p and every state are left as they were, and
+ * opt_plan_status reports OPT_FLAG_WAIT_TIMEOUT.  Only for AdamW steps that
+ * run the staged kernel (low-precision states with stochastic rounding, or
+ * BF16 v with nearest rounding); others return OPT_EUNSUPPORTED. */
+#define OPT_STEP_WAIT_DRILL 4
+
 /* ---- norm result (48 bytes, written by opt_grad_norm) -------------------
  * sumsq    sum of squares of all finite gradient elements (fp64)
  * norm2    sqrt(sumsq); NaN if any NaN, else +Inf if any +-Inf
@@ -247,14 +259,36 @@ int opt_lamb_step(opt_plan* plan, const opt_hparams* hp, int64_t step, float max
 int opt_unchanged_count(opt_plan* plan, uint64_t* h_count, void* stream);
 
 /* Error flags raised by this plan's kernels since the last call, then
- * cleared.  Bit OPT_FLAG_WAIT_TIMEOUT: a kernel gave up waiting for its own
- * bulk copies (each wait is bounded in time, so a kernel never hangs) and
- * left part of its tiles unprocessed -- the step's results are then
- * incomplete.  0 means every kernel ran to completion.  Copies to host and
+ * cleared.  0 means every kernel ran to completion.  Copies to host and
  * synchronises the stream.  Returns OPT_OK, OPT_EINVAL (NULL argument) or
- * OPT_ECUDA. */
+ * OPT_ECUDA.
+ *
+ * OPT_FLAG_WAIT_TIMEOUT: the staged step kernel (low-precision states with
+ *   stochastic rounding, and BF16 v with nearest rounding, take their tiles
+ *   through shared memory) gave up a wait on its own bulk copies -- each wait
+ *   is bounded in time (opt_plan_set_wait_limit), so the kernel never hangs
+ *   -- and left part of its tiles unprocessed.  That step's outputs (p and
+ *   every state) are then partly updated and must be discarded: restore them
+ *   from a copy taken before the step.  Before leaving, the kernel let every
+ *   copy it had issued land; the plan itself is intact, and once this call
+ *   has cleared the flag it may be used again.
+ * OPT_FLAG_DRAIN_TIMEOUT: in addition, one of those final waits for issued
+ *   copies ran out too (no healthy GPU takes that long: the limit is the
+ *   wait limit plus 10 s), so a thread block may have left with copies
+ *   still targeting its shared memory.  Treat the whole CUDA context as
+ *   unreliable: discard the step's outputs, destroy every plan, and reset
+ *   the device before further work. */
 #define OPT_FLAG_WAIT_TIMEOUT 1
+#define OPT_FLAG_DRAIN_TIMEOUT 2
 int opt_plan_status(opt_plan* plan, int32_t* h_flags, void* stream);
+
+/* Limit, in nanoseconds of the GPU's global timer, of each wait of the
+ * staged step kernel on this plan (see OPT_FLAG_WAIT_TIMEOUT); 2 s unless
+ * set.  0 <= ns <= 10 s, else OPT_EINVAL.  The register-pipelined step
+ * kernels, the norm and the codecs do not wait on anything.  A short limit
+ * keeps a wait drill (OPT_STEP_WAIT_DRILL) short.  Host only: takes effect
+ * from the next step call. */
+int opt_plan_set_wait_limit(opt_plan* plan, uint64_t ns);
 
 /* Copy each tensor's gradient from host memory (pinned for asynchrony) into
  * the plan's device gradient buffers: one cudaMemcpyAsync per tensor. */

@@ -24,7 +24,8 @@ OPT_F32, OPT_BF16, OPT_E4M3, OPT_E2M2 = 0, 1, 2, 3
 OPT_ROUND_NEAREST, OPT_ROUND_STOCHASTIC = 0, 1
 OPT_STEP_RESET_STATES = 1
 OPT_STEP_DEVICE_COUNTER = 2
-OPT_FLAG_WAIT_TIMEOUT = 1
+OPT_STEP_WAIT_DRILL = 4
+OPT_FLAG_WAIT_TIMEOUT, OPT_FLAG_DRAIN_TIMEOUT = 1, 2
 OPT_CHUNK_ELEMS = 32768
 OPT_NORM_SLOTS = 1216
 
@@ -85,6 +86,7 @@ _SIGS = {
     "opt_unchanged_count": (_c.c_int, [_vp, _c.POINTER(_c.c_uint64), _vp]),
     "opt_plan_status": (_c.c_int, [_vp, _c.POINTER(_c.c_int32), _vp]),
     "opt_plan_set_step": (_c.c_int, [_vp, _c.c_int64, _vp]),
+    "opt_plan_set_wait_limit": (_c.c_int, [_vp, _c.c_uint64]),
     "opt_grads_upload": (_c.c_int, [_vp, _c.POINTER(_vp), _vp]),
     "opt_encode": (_c.c_int, [_vp, _vp, _c.c_int64, _c.c_int32, _c.c_int32, _c.c_uint64,
                               _c.c_uint32, _c.c_int64, _vp]),
@@ -143,12 +145,13 @@ def opt_strerror(status: int) -> str:
 
 def hparams(lr=1e-3, beta1=0.9, beta2=0.999, beta3=0.9999, alpha=5.0, eps=1e-8, weight_decay=0.0,
             rounding="nearest", seed=0, count_unchanged=False, reset_states=False,
-            device_step=False) -> opt_hparams:
+            device_step=False, wait_drill=False) -> opt_hparams:
     r = OPT_ROUND_STOCHASTIC if rounding in ("stochastic", "sr", OPT_ROUND_STOCHASTIC) else OPT_ROUND_NEAREST
     return opt_hparams(lr, beta1, beta2, beta3, alpha, eps, weight_decay, r, seed,
                        1 if count_unchanged else 0,
                        (OPT_STEP_RESET_STATES if reset_states else 0) |
-                       (OPT_STEP_DEVICE_COUNTER if device_step else 0))
+                       (OPT_STEP_DEVICE_COUNTER if device_step else 0) |
+                       (OPT_STEP_WAIT_DRILL if wait_drill else 0))
 
 
 def opt_chunk_table(numel, grad_dtype):
@@ -296,6 +299,10 @@ class Plan:
         out = _c.c_int32()
         _check(lib().opt_plan_status(self.handle, _c.byref(out), _stream_ptr(stream)), "opt_plan_status")
         return out.value
+
+    def set_wait_limit(self, ns: int):
+        """Limit of each wait of the staged step kernel, in ns (0 .. 10 s)."""
+        _check(lib().opt_plan_set_wait_limit(self.handle, ns), "opt_plan_set_wait_limit")
 
     def grads_upload(self, host_grads, stream=None):
         """Copy host gradients (one tensor per list entry, the plan's sizes and

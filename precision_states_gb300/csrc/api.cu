@@ -14,6 +14,11 @@
 
 using namespace psopt;
 
+// Each wait of the staged step kernel gives up after this long unless the
+// plan sets another limit (opt_plan_set_wait_limit).
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;      // 2 s
+constexpr uint64_t kMaxWaitNs = 10000000000ull;         // 10 s
+
 struct opt_plan {
   int device = 0;
   int sm_count = 0;
@@ -39,6 +44,7 @@ struct opt_plan {
   opt_norm_result* d_result = nullptr;
   unsigned long long* d_unchanged = nullptr;
   int* d_err = nullptr;                    // kernel error flags (opt_plan_status)
+  uint64_t wait_ns = kDefaultWaitNs;       // limit of each wait of the staged step
   unsigned int* d_done = nullptr;          // the norm's completion counter
   int64_t* d_step = nullptr;               // device step counter (last step taken)
   opt_step_scalars* d_sc = nullptr;        // its step's scalars
@@ -293,11 +299,15 @@ int opt_grad_norm(opt_plan* P, double max_norm, opt_norm_result* d_out, opt_norm
 static int do_step(opt_plan* P, const opt_hparams* hp, int64_t step, const opt_norm_result* d_norm,
                    void* stream, int algo) {
   if (P == nullptr || hp == nullptr) return OPT_EINVAL;
-  if ((hp->flags & ~(OPT_STEP_RESET_STATES | OPT_STEP_DEVICE_COUNTER)) != 0) return OPT_EINVAL;
+  if ((hp->flags & ~(OPT_STEP_RESET_STATES | OPT_STEP_DEVICE_COUNTER | OPT_STEP_WAIT_DRILL)) != 0)
+    return OPT_EINVAL;
   const bool dev_step = (hp->flags & OPT_STEP_DEVICE_COUNTER) != 0;
   if (dev_step ? step != 0 : step < 1) return OPT_EINVAL;
   if (dev_step && P->combo != SC_F32) return OPT_EUNSUPPORTED;
   if (hp->rounding != OPT_ROUND_NEAREST && hp->rounding != OPT_ROUND_STOCHASTIC) return OPT_EINVAL;
+  const bool drill = (hp->flags & OPT_STEP_WAIT_DRILL) != 0;
+  if (drill && (algo != ALGO_ADAMW || !step_is_staged(P->combo, hp->rounding == OPT_ROUND_STOCHASTIC)))
+    return OPT_EUNSUPPORTED;
   if (d_norm != nullptr && ((uintptr_t)d_norm & 7u)) return OPT_EALIGN;
   if (algo == ALGO_ADEMAMIX) {
     if (P->combo != SC_F32) return OPT_EUNSUPPORTED;
@@ -318,6 +328,8 @@ static int do_step(opt_plan* P, const opt_hparams* hp, int64_t step, const opt_n
   a.unchanged = hp->count_unchanged ? P->d_unchanged : nullptr;
   a.reset = (hp->flags & OPT_STEP_RESET_STATES) ? 1 : 0;
   a.err = P->d_err;
+  a.wait_ns = P->wait_ns;
+  a.drill = drill ? 1 : 0;
 
   DeviceGuard g(P->device);
   if (!g.ok) return OPT_ECUDA;
@@ -429,6 +441,12 @@ int opt_plan_status(opt_plan* P, int32_t* h_flags, void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_status(e);
   *h_flags = v;
+  return OPT_OK;
+}
+
+int opt_plan_set_wait_limit(opt_plan* P, uint64_t ns) {
+  if (P == nullptr || ns > kMaxWaitNs) return OPT_EINVAL;
+  P->wait_ns = ns;
   return OPT_OK;
 }
 

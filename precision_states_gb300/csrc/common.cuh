@@ -59,8 +59,10 @@ struct StepArgs {
   const opt_norm_result* d_norm;      // NULL: no clipping
   unsigned long long* unchanged;      // NULL: do not count
   int reset;                          // nonzero: start from zero moments
-  int* err;                           // kernel error flags (bit 0: a bounded wait ran out)
+  int* err;                           // kernel error flags (OPT_FLAG_*)
   const opt_step_scalars* d_sc;       // non-NULL: use these scalars (device memory), not sc
+  unsigned long long wait_ns;         // limit of each wait of the staged step (opt_plan_set_wait_limit)
+  int drill;                          // nonzero: the staged step's waits run out on purpose
 };
 
 // ------------------------------------------------------------- bit views

@@ -44,6 +44,11 @@ enum StateCombo { SC_F32 = 0, SC_BF16_BF16 = 1, SC_BF16_E4M3 = 2, SC_BF16_E2M2 =
 enum Algo { ALGO_ADAMW = 0, ALGO_ADEMAMIX = 1 };
 
 int state_combo(int32_t m_dtype, int32_t v_dtype);   // -1 if not built
+// whether the AdamW step of a state combination runs the staged kernel
+// (tiles through shared memory by bulk copies, bounded waits)
+__host__ __device__ constexpr inline bool step_is_staged(int combo, bool stochastic) {
+  return combo != SC_F32 && (stochastic || combo == SC_BF16_BF16);
+}
 
 // Elements per tile of the step's work table: one 8-element group for each
 // of the step kernel's 256 threads.

@@ -24,10 +24,25 @@
 // of a tensor) is not copied: the producer completes "full" with a plain
 // arrive and the consumers load it from global memory as step_kernel does.
 //
-// Every wait is bounded in time (kWaitNs of %globaltimer).  A wait that
-// runs out sets bit 0 of *a.err and the thread stops; consumers first wait
-// (again bounded) for the copies the producer may still have in flight.  The
-// host reads the flag with opt_plan_status.
+// Every wait is bounded in time by %globaltimer: the producer's and the
+// consumers' waits by a.wait_ns (the plan's limit, 2 s unless set).  A wait
+// that runs out sets OPT_FLAG_WAIT_TIMEOUT in *a.err and the thread stops
+// working.  Before a consumer warp leaves, it makes sure no copy still
+// targets the stages: the producer, when it stops (at the end of its tiles,
+// or when one of its own waits runs out), publishes in shared memory how
+// many tiles it issued; the warp waits for that, then for every issued tile
+// it has not consumed.  Those waits have their own, much longer limit
+// (kDrainNs: issued copies land in microseconds), and if one of them runs
+// out too, OPT_FLAG_DRAIN_TIMEOUT is set as well.  The host reads the flags
+// with opt_plan_status.
+//
+// A wait drill (a.drill, OPT_STEP_WAIT_DRILL) makes the waits run out on
+// purpose, with no fault: each CTA's producer withholds its first tile --
+// no copy, no arrive, so nothing ever completes that stage's "full" phase --
+// and issues the next S - 1 as usual.  Every consumer warp's first wait then
+// runs out, the producer's wait for the withheld stage's release runs out
+// too, and the consumers drain the S - 1 issued tiles (never the withheld
+// one) before leaving.  No tile is processed: the step changes nothing.
 #pragma once
 
 #include "step_kernel.cuh"
@@ -38,7 +53,7 @@ constexpr int kSmemPerSm = 228 * 1024;                      // shared memory per
 constexpr int kSmemReservedPerCta = 1024;                   // the runtime's share of each CTA
 constexpr int kBulkConsumers = kStepThreads / 32;          // consumer warps
 constexpr int kBulkThreads = kStepThreads + 32;            // + the producer warp
-constexpr unsigned long long kWaitNs = 2000000000ull;      // 2 s
+constexpr unsigned long long kDrainNs = 10000000000ull;    // 10 s beyond the wait limits
 
 // Shared-memory layout: barriers, then S stages of {header, p, g, m, v};
 // every part a multiple of 16 bytes.  S is 4, or 5 for BF16 v with nearest
@@ -64,10 +79,12 @@ struct BulkLayout {
   static constexpr int V = VD == OPT_BF16 ? 2 * N : VD == OPT_E4M3 ? N : N / 2;
   static constexpr int OFF_P = HDR, OFF_G = OFF_P + P, OFF_M = OFF_G + G, OFF_V = OFF_M + M;
   static constexpr int STAGE = OFF_V + V;
-  static constexpr bool fits(int s) { return 2 * (16 * s + STAGE * s + kSmemReservedPerCta) <= kSmemPerSm; }
+  static constexpr int CTRL = 16;                          // producer's issued count, done flag
+  static constexpr bool fits(int s) { return 2 * (16 * s + CTRL + STAGE * s + kSmemReservedPerCta) <= kSmemPerSm; }
   static constexpr int S = (!SR && COMBO == SC_BF16_BF16 && fits(5)) ? 5 : 4;
   static_assert(fits(S), "two CTAs per SM");
-  static constexpr int BAR_BYTES = 16 * S;                  // full[S], then empty[S]
+  static constexpr int OFF_CTRL = 16 * S;
+  static constexpr int BAR_BYTES = 16 * S + CTRL;           // full[S], empty[S], control
   static constexpr int BYTES = BAR_BYTES + STAGE * S;
   static_assert(STAGE % 16 == 0 && BAR_BYTES % 16 == 0, "bulk copy alignment");
   static_assert(kStepThreads * 8 == N, "one tile per stage");
@@ -101,13 +118,21 @@ __device__ __forceinline__ unsigned long long global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Wait for the phase with the given parity to complete, at most kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete, at most limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (!mbar_try_wait(bar, parity))
-    if (global_ns() - t0 > kWaitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   return true;
+}
+__device__ __forceinline__ void sts_volatile_u64(uint32_t a, unsigned long long v) {
+  asm volatile("st.volatile.shared.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long lds_volatile_u64(uint32_t a) {
+  unsigned long long v;
+  asm volatile("ld.volatile.shared.u64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+  return v;
 }
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile(
@@ -142,6 +167,7 @@ step_bulk_kernel(const StepArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t full0 = sbase, empty0 = sbase + 8 * S;             // barrier of stage s: + 8 * s
+  const uint32_t issued_at = sbase + L::OFF_CTRL, done_at = issued_at + 8;
   const uint32_t stage0 = sbase + L::BAR_BYTES;                     // stage s: + s * STAGE
   const bool reset = a.reset != 0;
   if (threadIdx.x == 0) {
@@ -149,6 +175,8 @@ step_bulk_kernel(const StepArgs a) {
       mbar_init(full0 + 8 * st, 1);
       mbar_init(empty0 + 8 * st, kBulkConsumers);
     }
+    sts_volatile_u64(issued_at, 0ull);
+    sts_volatile_u64(done_at, 0ull);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -161,12 +189,14 @@ step_bulk_kernel(const StepArgs a) {
   if (warp == kBulkConsumers) {
     // ---------------------------------------------------------- producer
     if (lane != 0) return;
-    for (int64_t k = 0; k < ntiles; ++k) {
+    int64_t k = 0;
+    for (; k < ntiles; ++k) {
       const int st = (int)(k % S);
-      if (k >= S && !mbar_wait(empty0 + 8 * st, (uint32_t)(k / S - 1) & 1u)) {
-        atomicOr(a.err, 1);
-        return;
+      if (k >= S && !mbar_wait(empty0 + 8 * st, (uint32_t)(k / S - 1) & 1u, a.wait_ns)) {
+        atomicOr(a.err, OPT_FLAG_WAIT_TIMEOUT);
+        break;
       }
+      if (k == 0 && a.drill) continue;     // withheld: no copy, no arrive
       BulkHeader h;
       h.tl = a.tiles[first + k * stride];
       h.td = a.tensors[h.tl.tensor];
@@ -186,6 +216,12 @@ step_bulk_kernel(const StepArgs a) {
         mbar_arrive(bar);     // a short tile: nothing copied, the consumers load it directly
       }
     }
+    // Tiles 0 .. k-1 are issued and no more will be: say so, for a consumer
+    // warp that stopped early and must let those copies land before it
+    // leaves (read only on that path).
+    sts_volatile_u64(issued_at, (unsigned long long)k);
+    __threadfence_block();
+    sts_volatile_u64(done_at, 1ull);
     return;
   }
 
@@ -200,7 +236,10 @@ step_bulk_kernel(const StepArgs a) {
   for (; k < ntiles; ++k) {
     const int st = (int)(k % S);
     // one verdict for the warp, so that its lanes never part ways
-    if (!__all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * st, (uint32_t)(k / S) & 1u))) { ok = false; break; }
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8 * st, (uint32_t)(k / S) & 1u, a.wait_ns))) {
+      ok = false;
+      break;
+    }
     const unsigned char* stage = smem + L::BAR_BYTES + st * L::STAGE;
     const BulkHeader h = *reinterpret_cast<const BulkHeader*>(stage);
     const int64_t e0 = h.tl.start + off;
@@ -245,11 +284,24 @@ step_bulk_kernel(const StepArgs a) {
                                                       a.seed_hi, a.step32, count);
   }
   if (!ok) {
-    // a wait ran out: flag it and let the copies possibly still in flight
-    // land (each wait bounded again) before leaving
-    if (lane == 0) atomicOr(a.err, 1);
-    for (int64_t q = k; q < ntiles && q < k + S; ++q)
-      mbar_wait(full0 + 8 * (int)(q % S), (uint32_t)(q / S) & 1u);
+    // A wait ran out: flag it, then let every copy that may still target a
+    // stage land before leaving.  This warp released tiles 0 .. k-1 only, so
+    // the producer issued at most tiles up to k + S - 1 (each needs every
+    // warp's release of the tile S before it): one pending phase per stage.
+    // Its own waits are bounded by wait_ns each, at most S + 1 of them after
+    // this warp's last release.
+    if (lane == 0) atomicOr(a.err, OPT_FLAG_WAIT_TIMEOUT);
+    const unsigned long long t0 = global_ns();
+    bool drained;
+    while (!(drained = lds_volatile_u64(done_at) != 0ull))
+      if (global_ns() - t0 > (unsigned long long)(S + 1) * a.wait_ns + kDrainNs) break;
+    if (drained) {
+      __threadfence_block();
+      const int64_t issued = (int64_t)lds_volatile_u64(issued_at);
+      for (int64_t q = (a.drill && k == 0) ? 1 : k; q < issued && drained; ++q)
+        drained = mbar_wait(full0 + 8 * (int)(q % S), (uint32_t)(q / S) & 1u, kDrainNs);
+    }
+    if (!drained && lane == 0) atomicOr(a.err, OPT_FLAG_DRAIN_TIMEOUT);
     return;
   }
   if (count) {

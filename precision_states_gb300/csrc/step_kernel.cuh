@@ -71,7 +71,7 @@ struct StepShape {
   static constexpr int kMinBlocks =
       (GT == OPT_BF16 && !SR && (COMBO == SC_BF16_E4M3 || COMBO == SC_BF16_E2M2)) ? 3 : 2;
   static constexpr bool kPersistent = ALGO != ALGO_ADEMAMIX;
-  static constexpr bool kBulk = COMBO != SC_F32 && ALGO == ALGO_ADAMW && (SR || COMBO == SC_BF16_BF16);
+  static constexpr bool kBulk = ALGO == ALGO_ADAMW && step_is_staged(COMBO, SR);
   static constexpr bool kLookahead = kPersistent && kMinBlocks == 2;
 };
 

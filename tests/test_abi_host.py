@@ -197,7 +197,13 @@ def test_plan_status_null_arguments():
     L = ps.lib()
     out = ctypes.c_int32()
     assert L.opt_plan_status(None, ctypes.byref(out), None) == ps.OPT_EINVAL
-    assert ps.OPT_FLAG_WAIT_TIMEOUT == 1
+    assert ps.OPT_FLAG_WAIT_TIMEOUT == 1 and ps.OPT_FLAG_DRAIN_TIMEOUT == 2
+
+
+def test_set_wait_limit_rejects_a_missing_plan():
+    assert ps.lib().opt_plan_set_wait_limit(None, 0) == ps.OPT_EINVAL
+    assert ps.lib().opt_plan_set_wait_limit(None, 2_000_000_000) == ps.OPT_EINVAL
+    assert ps.OPT_STEP_WAIT_DRILL == 4 and ps.hparams(wait_drill=True).flags == 4
 
 
 def test_set_step_and_step_flags_on_the_host():
