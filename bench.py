@@ -81,7 +81,10 @@ def parse():
                     help="FP32 states: device step counter, norm and step replayed from CUDA graphs")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="cpu_baseline: time oracle steps over the sample for at least this long")
+    ap.add_argument("--oracle-sample-elems", type=int, default=120_000_000,
+                    help="elements of the fixed tensor sample the oracle steps (both arms)")
     ap.add_argument("--stall-curve", action="store_true",
                     help="instead of timing: the fraction of v codes left unchanged per step, every state "
                          "mode, over the low-precision workload's steps (one JSON line per mode)")
@@ -93,6 +96,68 @@ def parse():
                          "format and rounding mode beside torch's builtin RNE casts (one JSON line per mode)")
     ap.add_argument("--cast-elems", type=int, default=(1 << 28) + 12)
     return ap.parse_args()
+
+
+def apply_overrides(w, args):
+    """The state dtypes and the algorithm the flags select, on workload w."""
+    if args.v_dtype:
+        w.m_dtype, w.v_dtype = ("f32", "f32") if args.v_dtype == "f32" else ("bf16", args.v_dtype)
+    if args.lamb is not None:
+        w.algo = "lamb"
+    return w
+
+
+def sample_indices(w, max_elems: int):
+    """The oracle's tensor sample, from sizes alone: tensors in list order,
+    those above 50M elements (embedding, head, MLP matrices) last, while they
+    fit in max_elems (at least one)."""
+    order = sorted(range(len(w.sizes)), key=lambda i: (w.sizes[i] > 50_000_000, i))
+    idx, total = [], 0
+    for i in order:
+        if total + w.sizes[i] > max_elems and idx:
+            break
+        idx.append(i)
+        total += w.sizes[i]
+    return idx, total
+
+
+def run_config(w, args, replicas: int) -> dict:
+    """The benchmark's configuration, identical in both arms: the workload,
+    the timing protocol of the GPU arm, and the oracle's tensor sample."""
+    clip = w.max_norm > 0
+    per_step = (step_bytes_per_param(w) + (ELEM_BYTES[w.grad_dtype] if clip else 0)) * w.numel
+    idx, total = sample_indices(w, args.oracle_sample_elems)
+    return {"workload": w.name, "tensors": len(w.sizes), "params_per_gpu": w.numel,
+            "grad_dtype": w.grad_dtype, "m_dtype": w.m_dtype, "v_dtype": w.v_dtype,
+            "rounding": args.rounding, "algo": w.algo, "clip_max_norm": w.max_norm,
+            "parallelism": f"replicas{replicas}",
+            "launch": "cuda-graph replay, device step counter" if args.graph else "direct",
+            "l2": ("L2 flushed before every timed step (256 MiB written, 256 MiB read); steps "
+                   "timed by their own events; e2e steps not flushed" if needs_l2_flush(w) else
+                   "inputs larger than L2 (%.0f GB streamed per step)" % (per_step / 1e9)),
+            "oracle_sample": {"tensors": len(idx), "params": total,
+                              "rule": "list order, tensors above 50M elements last, up to %d elements"
+                                      % args.oracle_sample_elems}}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
 
 
 def dist_env():
@@ -180,36 +245,16 @@ def traffic_for(kernel_key: str, params: int):
 # ----------------------------------------------------------- cpu baseline
 class OracleSample:
     """A bounded, deterministic sample of the workload for the CPU oracle:
-    tensors in list order (the embedding and head last), as many as fit a
-    budget of about `seconds` of single-threaded oracle time per step."""
+    the tensors sample_indices picks, from sizes alone, so that both arms
+    (and every box) time the oracle on the same tensors."""
 
-    def __init__(self, w, seconds: float, stochastic: bool = False, max_unorm: float = 0.0):
-        import numpy as np
-
+    def __init__(self, w, max_elems: int, stochastic: bool = False, max_unorm: float = 0.0):
         import oracle
         import workloads as W
 
         self.w = w
         self.ohp = oracle.hparams(**{**dict(beta1=0.9, beta2=0.999), **w.hp})
-        order = sorted(range(len(w.sizes)), key=lambda i: (w.sizes[i] > 50_000_000, i))
-        # calibrate: oracle time per element on a probe tensor
-        n_probe = min(2_000_000, max(w.sizes))
-        pw = W.Workload("probe", [n_probe], w.grad_dtype)
-        g = W.to_numpy_codes(W.make_grads(pw, "cpu", 1, 0)[0])
-        p = np.zeros(n_probe, np.float32)
-        t0 = time.perf_counter()
-        oracle.grad_norm([g], w.max_norm)
-        oracle.adam_tensor(oracle.ADAMW, p, g, np.zeros(n_probe, np.float32), np.zeros(n_probe, np.float32),
-                           self.ohp, 1)
-        per_elem = (time.perf_counter() - t0) / n_probe
-        budget = max(1, int(seconds / max(per_elem, 1e-10)))
-        self.idx, total = [], 0
-        for i in order:
-            if total + w.sizes[i] > budget and self.idx:
-                break
-            self.idx.append(i)
-            total += w.sizes[i]
-        self.numel = total
+        self.idx, self.numel = sample_indices(w, max_elems)
         self.grads = [W.to_numpy_codes(t) for t in W.make_grads(w, "cpu", 1, 0, self.idx)]
         self.params = [W.to_numpy_codes(t) for t in W.make_params(w, "cpu", 0, self.idx)]
         self.m = [W.to_numpy_codes(W.state_storage(w.m_dtype, w.sizes[i], "cpu")) for i in self.idx]
@@ -240,19 +285,25 @@ class OracleSample:
                                tensor_index=self.idx[k])
         return time.perf_counter() - t0
 
-    def describe(self, dt: float) -> str:
+    def describe(self, dt: float, steps: int) -> str:
         return (f"{len(self.idx)} of {len(self.w.sizes)} tensors ({self.numel:,} params, "
                 f"{self.numel / self.w.numel:.2%} of the list): norm + one step per timed step, "
-                f"single-threaded C oracle, {dt:.2f} s per step")
+                f"{steps} timed steps, single-threaded C oracle, {dt:.2f} s per step")
 
 
-def cpu_baseline(w, seconds: float, stochastic: bool = False, max_unorm: float = 0.0):
+def cpu_baseline(w, args):
     """The CPU oracle as it stands, timed on the machine's host cores (one
-    thread) over a bounded sample of the same workload."""
-    smp = OracleSample(w, seconds, stochastic, max_unorm)
-    dt = smp.step()
-    return {"value": smp.numel / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": smp.describe(dt)}
+    thread) over the fixed sample of the same workload: steps until at
+    least --cpu-seconds have passed (two at least), after one untimed."""
+    smp = OracleSample(w, args.oracle_sample_elems, args.rounding == "stochastic",
+                       args.lamb if args.lamb is not None else 0.0)
+    smp.step()
+    times = []
+    while len(times) < 2 or sum(times) < args.cpu_seconds:
+        times.append(smp.step())
+    dt = sum(times) / len(times)
+    return {"value": smp.numel / dt / 1e9, "unit": UNIT, "cores": 1, "cpu_model": cpu_model(),
+            "kind": "oracle", "sample": smp.describe(dt, len(times))}
 
 
 # ---------------------------------------------------------------- our arm
@@ -270,9 +321,7 @@ def run_ours(args, rank, local_rank, world):
         dist.init_process_group("nccl", device_id=dev)
         pg = dist
 
-    w = W.workload(args.workload)
-    if args.v_dtype:
-        w.m_dtype, w.v_dtype = ("f32", "f32") if args.v_dtype == "f32" else ("bf16", args.v_dtype)
+    w = apply_overrides(W.workload(args.workload), args)
     params = W.make_params(w, dev, seed=rank)
     grads = W.make_grads(w, dev, step=1, seed=rank)
     m = [W.state_storage(w.m_dtype, n, dev) for n in w.sizes]
@@ -285,7 +334,6 @@ def run_ours(args, rank, local_rank, world):
     d_norm = plan.norm_buffer() if clip else None
     step_fn = plan.ademamix_step if w.algo == "ademamix" else plan.adamw_step
     if args.lamb is not None:
-        w.algo = "lamb"
         step_fn = lambda hp_, t_, dn_, stream=None: plan.lamb_step(hp_, t_, args.lamb, dn_, stream=stream)
     # the norm is one launch per gradient dtype (one here; its last CTA
     # finishes), the step one launch (LAMB: three passes); with --graph the
@@ -520,21 +568,13 @@ def run_ours(args, rank, local_rank, world):
         del params, grads, m, v, m2
         plan.close()
         torch.cuda.empty_cache()
-        cpu = cpu_baseline(w, args.cpu_sample_seconds, args.rounding == "stochastic",
-                           args.lamb if args.lamb is not None else 0.0)
+        cpu = cpu_baseline(w, args)
 
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
-            "config": {"workload": w.name, "tensors": len(w.sizes), "params_per_gpu": params_per_step,
-                       "grad_dtype": w.grad_dtype, "m_dtype": w.m_dtype, "v_dtype": w.v_dtype,
-                       "rounding": args.rounding, "algo": w.algo,
-                       "clip_max_norm": w.max_norm, "parallelism": f"replicas{world}",
-                       "launch": "cuda-graph replay, device step counter" if args.graph else "direct",
-                       "l2": ("L2 flushed before every timed step (256 MiB written, 256 MiB read); steps "
-                              "timed by their own events; e2e steps not flushed" if flush else
-                              "inputs larger than L2 (%.0f GB streamed per step)" % ((step_bytes + norm_bytes) / 1e9))},
+            "config": run_config(w, args, world),
             "hbm_gbs": round((step_bytes + norm_bytes) / (total_ms / args.steps / 1e3) / 1e9, 1),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
             "gpu_launches": launches_per_step * args.steps,
@@ -549,31 +589,29 @@ def run_ours(args, rank, local_rank, world):
 # ---------------------------------------------------------- reference arm
 def run_reference(args, rank, world):
     """The CPU oracle as the reference arm: each step is the oracle's norm +
-    step over a bounded sample of the workload (rank 0 only)."""
+    step over the same fixed sample of the workload as the GPU arm's
+    cpu_baseline.  Rank 0 alone runs it, so its line reports one replica
+    (parallelism replicas1, oracle_rank 0) whatever the launch's world size;
+    the other ranks exit without work."""
     if rank != 0:
         return
     import workloads as W
-    w = W.workload(args.workload)
-    if args.v_dtype:
-        w.m_dtype, w.v_dtype = ("f32", "f32") if args.v_dtype == "f32" else ("bf16", args.v_dtype)
-    per_step = max(0.5, min(5.0, 120.0 / max(1, args.steps + args.warmup)))
-    smp = OracleSample(w, per_step, args.rounding == "stochastic")
+    w = apply_overrides(W.workload(args.workload), args)
+    smp = OracleSample(w, args.oracle_sample_elems, args.rounding == "stochastic",
+                       args.lamb if args.lamb is not None else 0.0)
     for _ in range(args.warmup):
         smp.step()
     times = [smp.step() for _ in range(args.steps)]
     total = sum(times)
     value = smp.numel * args.steps / total / 1e9
-    cb = {"value": round(value, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
-          "sample": smp.describe(total / args.steps)}
+    cb = {"value": round(value, 6), "unit": UNIT, "cores": 1, "cpu_model": cpu_model(), "kind": "oracle",
+          "sample": smp.describe(total / args.steps, args.steps)}
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+            "oracle_rank": 0,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": w.name, "tensors": len(w.sizes), "params_per_gpu": w.numel,
-                       "grad_dtype": w.grad_dtype, "m_dtype": w.m_dtype, "v_dtype": w.v_dtype,
-                       "rounding": args.rounding, "algo": w.algo,
-                       "clip_max_norm": w.max_norm, "parallelism": f"replicas{world}",
-                       "sampled_params_per_step": smp.numel},
+            "config": run_config(w, args, 1),
             "cpu_baseline": cb,
             "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

@@ -45,7 +45,57 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1, r.stdout
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
-    assert d["config"]["parallelism"] == "replicas2"
+    # rank 0 alone ran the oracle: one replica, whatever the launch's size
+    assert d["config"]["parallelism"] == "replicas1" and d["oracle_rank"] == 0
+
+
+def run_reference_line(*extra):
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0", *extra],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    return json.loads([l for l in r.stdout.splitlines() if l.strip()][-1])
+
+
+def test_both_arms_share_config_and_oracle_sample():
+    """The reference arm's config is the GPU arm's, key for key (the GPU
+    arm's is built by the same run_config for one replica), and both time
+    the oracle on one sample fixed by the tensor sizes alone."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    argv = ["--workload", "sweep", "--v-dtype", "e4m3", "--rounding", "stochastic",
+            "--oracle-sample-elems", "200000"]
+    d = run_reference_line(*argv)
+    old = sys.argv
+    try:
+        sys.argv = ["bench.py", "--steps", "1", "--warmup", "0", *argv]
+        args = bench.parse()
+    finally:
+        sys.argv = old
+    w = bench.apply_overrides(W.workload("sweep"), args)
+    assert d["config"] == json.loads(json.dumps(bench.run_config(w, args, 1)))
+    idx, total = bench.sample_indices(w, 200000)
+    assert d["config"]["oracle_sample"]["tensors"] == len(idx)
+    assert d["config"]["oracle_sample"]["params"] == total
+    assert total <= 200000 and idx == sorted(idx)
+    smp = bench.OracleSample(w, 200000, True)
+    assert smp.idx == idx and smp.numel == total
+    assert d["cpu_baseline"]["cpu_model"] and d["cpu_baseline"]["cores"] == 1
+
+
+def test_oracle_sample_is_fixed_by_sizes():
+    """Llama-3-8B list: the sample is the same set every time and on every
+    box (no timing calibration), the attention and norm tensors of the first
+    layers, the matrices above 50M elements left for last."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import workloads as W
+    w = W.workload("llama3_8b")
+    a = bench.sample_indices(w, 120_000_000)
+    assert a == bench.sample_indices(w, 120_000_000)
+    idx, total = a
+    assert all(w.sizes[i] <= 50_000_000 for i in idx) and 100_000_000 < total <= 120_000_000
 
 
 def test_l2_flush_only_for_lists_that_fit():
