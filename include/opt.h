@@ -319,7 +319,7 @@ int opt_decode(const void* d_in, float* d_out, int64_t n, int32_t dtype, void* s
  * cudaMalloc, cudaFree or allocating library routine, and no host heap.  The
  * pages describe no such variant; it has no counterpart there.
  *
- * Scratch: one fixed device array inside the library (4,534,528 bytes, held
+ * Scratch: one fixed device array inside the library (4,515,072 bytes, held
  * by every GPU that loads the library until the process exits), large enough
  * for OPT_NOALLOC_MAX_TENSORS tensors and OPT_NOALLOC_MAX_CHUNKS chunks of
  * OPT_CHUNK_ELEMS elements (about 8.6e9 elements).  Larger lists are rejected
@@ -351,7 +351,7 @@ int opt_grad_norm_noalloc(int32_t n, const int64_t* numel, const void* const* gr
 /* Elements per chunk of the chunk table. */
 #define OPT_CHUNK_ELEMS 32768
 /* Number of fixed partial-sum slots per gradient-dtype bucket. */
-#define OPT_NORM_SLOTS 1216
+#define OPT_NORM_SLOTS 912
 
 typedef struct opt_chunk {
   uint32_t tensor;   /* index into the list */

@@ -27,7 +27,7 @@ OPT_STEP_DEVICE_COUNTER = 2
 OPT_STEP_WAIT_DRILL = 4
 OPT_FLAG_WAIT_TIMEOUT, OPT_FLAG_DRAIN_TIMEOUT = 1, 2
 OPT_CHUNK_ELEMS = 32768
-OPT_NORM_SLOTS = 1216
+OPT_NORM_SLOTS = 912
 
 DTYPES = {"f32": OPT_F32, "bf16": OPT_BF16, "e4m3": OPT_E4M3, "e2m2": OPT_E2M2}
 

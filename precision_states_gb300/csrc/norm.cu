@@ -41,22 +41,28 @@
 namespace psopt {
 namespace {
 
-// 128 threads and 8 CTAs per SM: the 1216 slots are one wave, and each
-// thread may hold 64 registers -- enough for four 16-byte loads in flight
-// that rotate (each register refilled as soon as its vector is summed) and
-// two float-float chains (alternate vectors), so that the additions of one
-// vector need not wait for the previous vector's.  Measured on GB300 against
-// 256 threads at the 32-register cap with four loads issued together and
-// then summed into one chain: 2.5 % faster on the Llama-3-8B list, 4 % on
-// the 740-tensor list.  (Six rotating loads and one chain gained 1.6 and
-// 2 %; a packed magnitude max that cut a tenth of the instructions gained
-// nothing; eight 16-byte cp.async copies in flight per thread into its own
-// shared-memory slots, pipelined within each chunk, were 3 % slower on the
-// Llama-3-8B list and 12 % on the 740-tensor list; 32-byte loads read no
-// faster than 16-byte ones in a probe of this access order.)  Plain reads
-// in the same order reach 7.44 TB/s on GB300.
+// 128 threads and 6 CTAs per SM: the 912 slots are one wave on GB300's 152
+// SMs, and each thread may hold 85 registers -- enough for eight 16-byte
+// loads in flight that rotate (each register refilled as soon as its vector
+// is summed) and two float-float chains (alternate vectors), so that the
+// additions of one vector need not wait for the previous vector's.  Per-CTA
+// timestamps on GB300 showed the pass bound by each SM's throughput (every
+// SM finishing at the same time however the work was split), so the lever
+// is bytes in flight per SM, not balance.  Measured against 8 CTAs per SM
+// with four loads each (in a loop with the AdamW step between norms):
+// Llama-3-8B list 2.453 -> 2.380 ms, 740-tensor list 0.0850 -> 0.0818 ms;
+// with L2 clean before the norm, 0.0773 -> 0.0746 ms.  (Also measured: 608
+// CTAs of 256 threads with six loads, 456 of 256 with eight -- close
+// behind; a ring of 16 KB stages filled by one producer lane's bulk copies,
+// 1 to 3 CTAs per SM -- 3-27 % slower on the 740-tensor list; chunks of 16K
+// or 8K elements -- within 1.5 %; a finish that issues all its slot loads
+// up front -- no change: its time is a chain of latencies.  Earlier, against
+// 256 threads at the 32-register cap with four loads issued together: eight
+// cp.async copies per thread into shared-memory slots were 3 and 12 %
+// slower; 32-byte loads read no faster than 16-byte ones in this order.)
+// Plain reads in the same order reach 7.44 TB/s on GB300.
 constexpr int kNormThreads = 128;
-constexpr int kDepth = 4;            // 16-byte loads in flight per thread
+constexpr int kDepth = 8;            // 16-byte loads in flight per thread
 
 // Two float-float accumulators (lane x, lane y): value = hi + lo per lane.
 struct FF2 {
@@ -253,7 +259,7 @@ __device__ __forceinline__ void finish_slots(const NormSlot* __restrict__ slots,
 }
 
 template <int GT>
-__global__ void __launch_bounds__(kNormThreads, 8)
+__global__ void __launch_bounds__(kNormThreads, 6)
 norm_partials_kernel(const NormChunk* __restrict__ chunks, int64_t cbegin, int64_t cend,
                      NormSlot* __restrict__ slots, NormFinish fin) {
   using T = GradTraits<GT>;

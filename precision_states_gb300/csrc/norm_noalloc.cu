@@ -51,7 +51,7 @@ constexpr int64_t kOffSlots = align256(kOffChunks + 16 * kMaxChunks);      // No
 constexpr int64_t kOffDone = align256(kOffSlots + 32 * 2 * OPT_NORM_SLOTS);    // uint32: completion counter
 constexpr int64_t kScratchBytes = align256(kOffDone + 4);
 
-static_assert(kScratchBytes == 4534528, "scratch size stated in opt.h");
+static_assert(kScratchBytes == 4515072, "scratch size stated in opt.h");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 // Device address of g_noalloc_scratch per device, looked up once per device.
