@@ -321,8 +321,8 @@ static int do_step(opt_plan* P, const opt_hparams* hp, int64_t step, const opt_n
   if (st != OPT_OK) return st;
   a.tensors = P->d_tensors;
   a.tiles = P->d_tiles;
-  a.seed_lo = (uint32_t)hp->seed;
-  a.seed_hi = (uint32_t)(hp->seed >> 32);
+  philox_round_keys(hp->seed, a.rk);
+  a.neg_zero2 = kNegZero2;
   a.step32 = (uint32_t)step;
   a.d_norm = d_norm;
   a.unchanged = hp->count_unchanged ? P->d_unchanged : nullptr;

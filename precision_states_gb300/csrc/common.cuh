@@ -55,7 +55,9 @@ struct StepArgs {
   const opt_chunk* tiles;             // the step's work table (kTileElems per entry)
   int64_t tile_begin, tile_end;       // this bucket's range of it
   opt_step_scalars sc;
-  uint32_t seed_lo, seed_hi, step32;
+  uint32_t step32;
+  uint32_t rk[20];                    // Philox round keys of the seed (philox_round_keys)
+  unsigned long long neg_zero2;       // -0.0 in both f32 lanes (kNegZero2), for mulr2
   const opt_norm_result* d_norm;      // NULL: no clipping
   unsigned long long* unchanged;      // NULL: do not count
   int reset;                          // nonzero: start from zero moments
@@ -104,6 +106,23 @@ __device__ __forceinline__ f2_t fma2(f2_t a, f2_t b, f2_t c) {
   return r;
 }
 
+// The rounded products a*b of both lanes, written as fma(a, b, z) with z
+// -0.0 in both lanes: adding -0 changes no bit (the sign of a zero product
+// included), and the result of a fused multiply-add cannot be fused again.
+// For products that feed an addition whose result must be the definition's
+// bits.  Measured on GB300: a packed mul.rn.f32x2 used once, by an
+// add.rn.f32x2, was fused into it in spite of the .rn (and of --fmad=false),
+// so that about half of the sums b1 m + (1 - b1) g of BF16 inputs came out
+// 1 ulp or more off.  z must come from outside the compiler's view (a kernel
+// argument): with a literal -0 the fma was turned back into a multiply
+// and fused all the same.
+constexpr unsigned long long kNegZero2 = 0x8000000080000000ull;
+__device__ __forceinline__ f2_t mulr2(f2_t a, f2_t b, unsigned long long z) {
+  f2_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(z));
+  return r;
+}
+
 // ------------------------------------------------------------------ Philox
 // Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, "Parallel Random
 // Numbers: As Easy as 1, 2, 3", SC'11, sec. 3).  A round multiplies counter
@@ -125,6 +144,34 @@ __device__ __forceinline__ uint4 philox10(uint4 c, uint32_t k0, uint32_t k1) {
 __device__ __forceinline__ uint4 draw_words(uint64_t q, uint32_t tensor, uint32_t step32,
                                             uint32_t seed_lo, uint32_t seed_hi) {
   return philox10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), tensor, step32), seed_lo, seed_hi);
+}
+
+// The same generator with its ten round keys given: rk[2r], rk[2r+1] are
+// the key words of round r (the seed advanced r times by the Weyl
+// increments).  They depend on the seed alone, so a kernel receives them
+// formed once (philox_round_keys on the host) in its arguments, where each
+// round reads them as operands instead of recomputing them per call.
+__device__ __forceinline__ uint4 philox10_rk(uint4 c, const uint32_t* rk) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ rk[2 * r], lo1, hi0 ^ c.w ^ rk[2 * r + 1], lo0);
+  }
+  return c;
+}
+__device__ __forceinline__ uint4 draw_words_rk(uint64_t q, uint32_t tensor, uint32_t step32, const uint32_t* rk) {
+  return philox10_rk(make_uint4((uint32_t)q, (uint32_t)(q >> 32), tensor, step32), rk);
+}
+
+// Round keys of Philox4x32-10 for a 64-bit seed (host side).
+inline void philox_round_keys(uint64_t seed, uint32_t rk[20]) {
+  uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+  for (int r = 0; r < 10; ++r) {
+    if (r) { k0 += 0x9E3779B9u; k1 += 0xBB67AE85u; }
+    rk[2 * r] = k0;
+    rk[2 * r + 1] = k1;
+  }
 }
 
 // -------------------------------------------------------------- BF16 codec

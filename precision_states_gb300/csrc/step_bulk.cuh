@@ -280,8 +280,8 @@ step_bulk_kernel(const StepArgs a) {
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * st);
     if (cnt > 0)
-      same += update_store<GT, COMBO, ALGO_ADAMW, SR>(h.td, e0, cnt, f, coef, a.sc, h.tl.tensor, a.seed_lo,
-                                                      a.seed_hi, a.step32, count);
+      same += update_store<GT, COMBO, ALGO_ADAMW, SR>(h.td, e0, cnt, f, coef, a.sc, h.tl.tensor, a.rk, a.step32,
+                                                      count, a.neg_zero2);
   }
   if (!ok) {
     // A wait ran out: flag it, then let every copy that may still target a

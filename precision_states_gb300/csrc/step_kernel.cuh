@@ -36,7 +36,7 @@
 //
 // Stochastic-rounding draws: two Philox4x32-10 calls per group (counters
 // q = e0/4 and e0/4 + 1), so each draw depends only on (seed, step, tensor,
-// element).
+// element); the round keys come formed in the kernel arguments.
 #pragma once
 
 #include "common.cuh"
@@ -218,8 +218,8 @@ template <int GT, int COMBO, int ALGO, bool SR>
 __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e0, int cnt,
                                                  const Frag<GT, COMBO, ALGO>& f, float coef,
                                                  const opt_step_scalars& sc, uint32_t tensor,
-                                                 uint32_t seed_lo, uint32_t seed_hi, uint32_t step32,
-                                                 bool count) {
+                                                 const uint32_t* rk, uint32_t step32, bool count,
+                                                 unsigned long long neg_zero2) {
   using F = Frag<GT, COMBO, ALGO>;
   constexpr int MD = F::MD, VD = F::VD;
   constexpr bool LOWP = COMBO != SC_F32;
@@ -227,8 +227,8 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
 
   uint32_t words[8];
   if constexpr (LOWP && SR) {
-    const uint4 d0 = draw_words((uint64_t)e0 >> 2, tensor, step32, seed_lo, seed_hi);
-    const uint4 d1 = draw_words(((uint64_t)e0 >> 2) + 1, tensor, step32, seed_lo, seed_hi);
+    const uint4 d0 = draw_words_rk((uint64_t)e0 >> 2, tensor, step32, rk);
+    const uint4 d1 = draw_words_rk(((uint64_t)e0 >> 2) + 1, tensor, step32, rk);
     words[0] = d0.x; words[1] = d0.y; words[2] = d0.z; words[3] = d0.w;
     words[4] = d1.x; words[5] = d1.y; words[6] = d1.z; words[7] = d1.w;
   }
@@ -256,45 +256,62 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
     for (int k = 0; k < 4; ++k)
       e2m2x2_dec_q(__byte_perm(even, odd, (uint32_t)k | ((uint32_t)(4 + k) << 4)), v[2 * k], v[2 * k + 1]);
   }
-  // a low-precision v code holds v / v_scale (a power of two: exact; for
-  // E2M2 the decoded quarter value times 4 v_scale, also a power of two)
-  if constexpr (VD != OPT_F32) {
-    const float vsc = VD == OPT_E2M2 ? __fmul_rn(td.v_scale, 4.0f) : td.v_scale;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], vsc);
-  }
-  // the moments: scalar IEEE fp32 operations in the order of the definition
-  // (no contraction), so the values before rounding match bit for bit
-  float pn[8], mnv[8], vnv[8], m2n[8];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float ge = __fmul_rn(g[j], coef);
-    mnv[j] = __fadd_rn(__fmul_rn(sc.beta1, m[j]), __fmul_rn(sc.omb1, ge));
-    vnv[j] = __fadd_rn(__fmul_rn(sc.beta2, v[j]), __fmul_rn(sc.omb2, __fmul_rn(ge, ge)));
-    if constexpr (ALGO == ALGO_ADEMAMIX)
-      m2n[j] = __fadd_rn(__fmul_rn(sc.beta3, u2f(f.m2[j])), __fmul_rn(sc.omb3, ge));
-  }
-  // the update term (not a stored code)
+  float pn[8], mnv[8], vnv[8], m2n[8], vs[8];
   if constexpr (StepShape<GT, COMBO, ALGO, SR>::kBulk && COMBO != SC_BF16_BF16) {
-    // stochastic E4M3 / E2M2 v, where the issue slots are the scarce
-    // resource: two elements per packed f32x2 instruction,
-    // p' = fma(-lr, u, p decay).  Measured on GB300 (GPT-2 list, A/B/A/B):
-    // stochastic E2M2 0.938-0.940 -> 0.954-0.956 of the measured copy
-    // bandwidth, E4M3 0.974 -> 0.979-0.981; BF16 v lost 0.15-0.35 % and the
-    // 3-CTA/SM nearest E4M3 / E2M2 kernels spill with it, so they keep the
-    // scalar form.
+    // Stochastic E4M3 / E2M2 v, where the issue slots are the scarce
+    // resource: everything from the decoded values to the value the v code
+    // stores runs two elements per packed f32x2 instruction.  The moments
+    // keep the scalar path's operations and order, each lane rounding as
+    // the scalar operation does, so their bits are the definition's; the
+    // products that feed an addition are mulr2, which no compiler fusion
+    // can merge into it.  The update term is
+    // p' = fma(-lr, u, p decay) with a reciprocal then a multiply for the
+    // division.  Measured on GB300 (GPT-2 list, A/B/A/B), the packed update
+    // term alone took stochastic E2M2 from 0.938-0.940 to 0.954-0.956 of
+    // the measured copy bandwidth and E4M3 from 0.974 to 0.979-0.981; BF16 v
+    // lost 0.15-0.35 % with it and the 3-CTA/SM nearest E4M3 / E2M2 kernels
+    // spill with it, so they keep the scalar form.
+    const float vsc = VD == OPT_E2M2 ? __fmul_rn(td.v_scale, 4.0f) : td.v_scale;
+    const float vinv = VD == OPT_E2M2 ? __fmul_rn(td.v_inv_scale, 0.25f) : td.v_inv_scale;
+    const f2_t vsc2 = pk(vsc, vsc), vinv2 = pk(vinv, vinv), c2 = pk(coef, coef);
+    const f2_t b1p = pk(sc.beta1, sc.beta1), o1p = pk(sc.omb1, sc.omb1);
+    const f2_t b2p = pk(sc.beta2, sc.beta2), o2p = pk(sc.omb2, sc.omb2);
     const f2_t ib1 = pk(sc.inv_bc1, sc.inv_bc1), ib2 = pk(sc.inv_bc2, sc.inv_bc2);
     const f2_t eps2 = pk(sc.eps, sc.eps), dec2 = pk(sc.decay, sc.decay), nlr2 = pk(-sc.lr, -sc.lr);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const f2_t num = mul2(pk(mnv[2 * k], mnv[2 * k + 1]), ib1);
+      const f2_t ge = mul2(pk(g[2 * k], g[2 * k + 1]), c2);
+      const f2_t mp = add2(mulr2(b1p, pk(m[2 * k], m[2 * k + 1]), neg_zero2), mulr2(o1p, ge, neg_zero2));
+      const f2_t vp = add2(mulr2(b2p, mul2(pk(v[2 * k], v[2 * k + 1]), vsc2), neg_zero2),
+                           mulr2(o2p, mul2(ge, ge), neg_zero2));
+      unpk(mp, mnv[2 * k], mnv[2 * k + 1]);
+      unpk(mul2(vp, vinv2), vs[2 * k], vs[2 * k + 1]);
       float a0, a1, d0, d1;
-      unpk(mul2(pk(vnv[2 * k], vnv[2 * k + 1]), ib2), a0, a1);
+      unpk(mul2(vp, ib2), a0, a1);
       unpk(add2(pk(sqrt_approx(a0), sqrt_approx(a1)), eps2), d0, d1);
-      const f2_t u = mul2(num, pk(rcp_approx(d0), rcp_approx(d1)));
+      const f2_t u = mul2(mul2(mp, ib1), pk(rcp_approx(d0), rcp_approx(d1)));
       unpk(fma2(nlr2, u, mul2(pk(u2f(f.p[2 * k]), u2f(f.p[2 * k + 1])), dec2)), pn[2 * k], pn[2 * k + 1]);
     }
   } else {
+    // a low-precision v code holds v / v_scale (a power of two: exact; for
+    // E2M2 the decoded quarter value times 4 v_scale, also a power of two)
+    if constexpr (VD != OPT_F32) {
+      const float vsc = VD == OPT_E2M2 ? __fmul_rn(td.v_scale, 4.0f) : td.v_scale;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = __fmul_rn(v[j], vsc);
+    }
+    // the moments: scalar IEEE fp32 operations in the order of the
+    // definition (no contraction), so the values before rounding match bit
+    // for bit
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float ge = __fmul_rn(g[j], coef);
+      mnv[j] = __fadd_rn(__fmul_rn(sc.beta1, m[j]), __fmul_rn(sc.omb1, ge));
+      vnv[j] = __fadd_rn(__fmul_rn(sc.beta2, v[j]), __fmul_rn(sc.omb2, __fmul_rn(ge, ge)));
+      if constexpr (ALGO == ALGO_ADEMAMIX)
+        m2n[j] = __fadd_rn(__fmul_rn(sc.beta3, u2f(f.m2[j])), __fmul_rn(sc.omb3, ge));
+    }
+    // the update term (not a stored code)
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       float num = __fmul_rn(mnv[j], sc.inv_bc1);
@@ -303,13 +320,12 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
       const float u = COMBO == SC_BF16_BF16 ? div_full(num, den) : div_approx(num, den);
       pn[j] = __fsub_rn(__fmul_rn(u2f(f.p[j]), sc.decay), __fmul_rn(sc.lr, u));
     }
-  }
-  // the value the v code stores: v / v_scale, exact (E2M2: a quarter of it,
-  // the converters' E3M2 grid, in the same one multiplication)
-  float vs[8];
-  const float vinv = VD == OPT_E2M2 ? __fmul_rn(td.v_inv_scale, 0.25f) : td.v_inv_scale;
+    // the value the v code stores: v / v_scale, exact (E2M2: a quarter of
+    // it, the converters' E3M2 grid, in the same one multiplication)
+    const float vinv = VD == OPT_E2M2 ? __fmul_rn(td.v_inv_scale, 0.25f) : td.v_inv_scale;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) vs[j] = VD == OPT_F32 ? vnv[j] : __fmul_rn(vnv[j], vinv);
+    for (int j = 0; j < 8; ++j) vs[j] = VD == OPT_F32 ? vnv[j] : __fmul_rn(vnv[j], vinv);
+  }
   // encode, two elements per converter instruction: pair k holds elements
   // 2k (low half / low byte) and 2k+1.  Element j's m draw is the low half
   // of draw word j and its v draw the high half, so the random-bits operand
@@ -480,8 +496,8 @@ step_kernel(const StepArgs a) {
       if (ncnt == 8) load_full(ntd, ne0, reset, nxt);
       else load_partial(ntd, ne0, ncnt, reset, nxt);
     }
-    same += update_store<GT, COMBO, ALGO, SR>(ctd, ce0, ccnt, cur, coef, sc, ctensor, a.seed_lo,
-                                              a.seed_hi, a.step32, count);
+    same += update_store<GT, COMBO, ALGO, SR>(ctd, ce0, ccnt, cur, coef, sc, ctensor, a.rk, a.step32, count,
+                                              a.neg_zero2);
     cur = nxt;
     ctd = ntd;
     ce0 = ne0;
