@@ -368,6 +368,17 @@ __device__ __forceinline__ uint32_t e4m3x2_sr(float lo, float hi, uint32_t rbits
   if (__builtin_expect(lo != lo || hi != hi, 0)) pair = e4m3x2_sr_soft(lo, hi, rbits);
   return pair;
 }
+// The same, as the converter leaves it: lo in byte 0, hi in byte 2, so that
+// the step can gather eight codes with two byte permutes (one per 4-element
+// word) instead of one per pair and the shifts.  Bytes 1 and 3 come from
+// the lanes fed zeros and are never read.
+__device__ __forceinline__ uint32_t e4m3x2_sr_wide(float lo, float hi, uint32_t rbits) {
+  uint32_t d;
+  asm("cvt.rs.satfinite.e4m3x4.f32 %0, {%1, %2, %3, %4}, %5;"
+      : "=r"(d) : "f"(0.0f), "f"(hi), "f"(0.0f), "f"(lo), "r"(rbits));
+  if (__builtin_expect(lo != lo || hi != hi, 0)) d = __byte_perm(e4m3x2_sr_soft(lo, hi, rbits), 0u, 0x4140);
+  return d;
+}
 
 // Unsigned E2M2, stochastic: the E3M2 grid of the quarter values (as in
 // e2m2x2_rn_q), after the clamp (7/4 lies on the grid, so no draw moves a
@@ -379,6 +390,16 @@ __device__ __forceinline__ uint32_t e2m2x2_sr_q(float lo4, float hi4, uint32_t r
       : "=r"(d)
       : "f"(0.0f), "f"(e2m2_clamp_q<NONNEG>(hi4)), "f"(0.0f), "f"(e2m2_clamp_q<NONNEG>(lo4)), "r"(rbits));
   return __byte_perm(d, 0u, 0x4420);
+}
+// The same, as the converter leaves it: lo in byte 0, hi in byte 2 (bytes 1
+// and 3, from the lanes fed zeros, are never read).
+template <bool NONNEG = false>
+__device__ __forceinline__ uint32_t e2m2x2_sr_wide_q(float lo4, float hi4, uint32_t rbits) {
+  uint32_t d;
+  asm("cvt.rs.satfinite.e3m2x4.f32 %0, {%1, %2, %3, %4}, %5;"
+      : "=r"(d)
+      : "f"(0.0f), "f"(e2m2_clamp_q<NONNEG>(hi4)), "f"(0.0f), "f"(e2m2_clamp_q<NONNEG>(lo4)), "r"(rbits));
+  return d;
 }
 
 // ------------------------------------------ arithmetic for the update term

@@ -327,9 +327,13 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
     for (int j = 0; j < 8; ++j) vs[j] = VD == OPT_F32 ? vnv[j] : __fmul_rn(vnv[j], vinv);
   }
   // encode, two elements per converter instruction: pair k holds elements
-  // 2k (low half / low byte) and 2k+1.  Element j's m draw is the low half
-  // of draw word j and its v draw the high half, so the random-bits operand
-  // of pair k gathers those halves of words 2k and 2k+1.
+  // 2k (low half / low byte) and 2k+1 -- for stochastic E4M3 / E2M2 v in
+  // bytes 0 and 2, as the four-lane converter leaves them (WIDE), so that
+  // the store gathers them with a few byte permutes.  Element j's m draw is
+  // the low half of draw word j and its v draw the high half, so the
+  // random-bits operand of pair k gathers those halves of words 2k and 2k+1.
+  constexpr bool WIDE = SR && (VD == OPT_E4M3 || VD == OPT_E2M2);
+  constexpr int HI = WIDE ? 16 : 8;            // bit position of element 2k+1 in an 8-bit-code pair
   uint32_t mpair[4], vpair[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
@@ -338,14 +342,14 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
     const float v0 = vs[2 * k], v1 = vs[2 * k + 1];
     if constexpr (MD == OPT_BF16) mpair[k] = bf16x2_enc<SR>(mnv[2 * k], mnv[2 * k + 1], rm);
     if constexpr (VD == OPT_BF16) vpair[k] = bf16x2_enc<SR>(v0, v1, rv);
-    if constexpr (VD == OPT_E4M3) vpair[k] = SR ? e4m3x2_sr(v0, v1, rv) : e4m3x2_rn(v0, v1);
-    if constexpr (VD == OPT_E2M2) vpair[k] = SR ? e2m2x2_sr_q<true>(v0, v1, rv) : e2m2x2_rn_q<true>(v0, v1);
+    if constexpr (VD == OPT_E4M3) vpair[k] = SR ? e4m3x2_sr_wide(v0, v1, rv) : e4m3x2_rn(v0, v1);
+    if constexpr (VD == OPT_E2M2) vpair[k] = SR ? e2m2x2_sr_wide_q<true>(v0, v1, rv) : e2m2x2_rn_q<true>(v0, v1);
   }
   // code of element j in the pair words
   auto vcode_at = [&](int j) -> uint32_t {
     if constexpr (VD == OPT_F32) return f2u(vnv[j]);
     else if constexpr (VD == OPT_BF16) return (vpair[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-    else return (vpair[j >> 1] >> (8 * (j & 1))) & 0xFFu;
+    else return (vpair[j >> 1] >> (HI * (j & 1))) & 0xFFu;
   };
   uint32_t same = 0;
   if (count) {
@@ -371,13 +375,25 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
     } else if constexpr (VD == OPT_BF16) {
       st_cs_u4(static_cast<uint16_t*>(td.v) + e0, make_uint4(vpair[0], vpair[1], vpair[2], vpair[3]));
     } else if constexpr (VD == OPT_E4M3) {
-      st_cs_u2(static_cast<uint8_t*>(td.v) + e0,
-               make_uint2(vpair[0] | (vpair[1] << 16), vpair[2] | (vpair[3] << 16)));
+      if constexpr (WIDE)
+        st_cs_u2(static_cast<uint8_t*>(td.v) + e0,
+                 make_uint2(__byte_perm(vpair[0], vpair[1], 0x6420), __byte_perm(vpair[2], vpair[3], 0x6420)));
+      else
+        st_cs_u2(static_cast<uint8_t*>(td.v) + e0,
+                 make_uint2(vpair[0] | (vpair[1] << 16), vpair[2] | (vpair[3] << 16)));
     } else {
-      // byte k: the pair's two codes as nibbles (even element low)
-      uint32_t w = 0;
+      // byte k holds element 2k in its low nibble and 2k+1 in its high one:
+      // gather the eight codes into a word of even elements and one of odd
+      // elements (one code per byte), then w = even | odd << 4
+      uint32_t w;
+      if constexpr (WIDE) {
+        const uint32_t p01 = __byte_perm(vpair[0], vpair[1], 0x6240), p23 = __byte_perm(vpair[2], vpair[3], 0x6240);
+        w = __byte_perm(p01, p23, 0x5410) | (__byte_perm(p01, p23, 0x7632) << 4);
+      } else {
+        w = 0;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) w |= ((vpair[k] | (vpair[k] >> 4)) & 0xFFu) << (8 * k);
+        for (int k = 0; k < 4; ++k) w |= ((vpair[k] | (vpair[k] >> 4)) & 0xFFu) << (8 * k);
+      }
       st_cs_u1(static_cast<uint8_t*>(td.v) + (e0 >> 1), w);
     }
     if constexpr (ALGO == ALGO_ADEMAMIX) {
