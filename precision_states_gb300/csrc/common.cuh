@@ -396,9 +396,20 @@ __device__ __forceinline__ uint32_t e2m2x2_sr_q(float lo4, float hi4, uint32_t r
 template <bool NONNEG = false>
 __device__ __forceinline__ uint32_t e2m2x2_sr_wide_q(float lo4, float hi4, uint32_t rbits) {
   uint32_t d;
-  asm("cvt.rs.satfinite.e3m2x4.f32 %0, {%1, %2, %3, %4}, %5;"
-      : "=r"(d)
-      : "f"(0.0f), "f"(e2m2_clamp_q<NONNEG>(hi4)), "f"(0.0f), "f"(e2m2_clamp_q<NONNEG>(lo4)), "r"(rbits));
+  if constexpr (NONNEG) {
+    // v >= 0 (or NaN): convert unclamped and clamp the codes instead, both
+    // at once as 16-bit lanes (each lane holds one code, its upper byte from
+    // a lane fed zero).  The converter saturates at the E3M2 maximum, above
+    // 7/4, and a stochastic rounding of a value at or above 7/4 lands on a
+    // code of 7/4 or above: min(code, 15) is the code of the clamped value.
+    asm("cvt.rs.satfinite.e3m2x4.f32 %0, {%1, %2, %3, %4}, %5;"
+        : "=r"(d) : "f"(0.0f), "f"(hi4), "f"(0.0f), "f"(lo4), "r"(rbits));
+    asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(d), "r"(0x000F000Fu));
+  } else {
+    asm("cvt.rs.satfinite.e3m2x4.f32 %0, {%1, %2, %3, %4}, %5;"
+        : "=r"(d)
+        : "f"(0.0f), "f"(e2m2_clamp_q<NONNEG>(hi4)), "f"(0.0f), "f"(e2m2_clamp_q<NONNEG>(lo4)), "r"(rbits));
+  }
   return d;
 }
 

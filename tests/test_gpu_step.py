@@ -69,6 +69,51 @@ def test_nonfinite_norm_skips_step():
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("v_dtype", ["bf16", "e4m3", "e2m2"])
+@pytest.mark.parametrize("rounding", ["nearest", "stochastic"])
+def test_lowp_nonfinite_grads_without_clip(v_dtype, rounding):
+    """Without clipping, NaN and +-Inf gradients go into the states as the
+    codecs define (reading: plain AdamW propagates them): BF16 keeps NaN
+    and Inf, E4M3 stores NaN as 0x7F and saturates Inf to 448, E2M2 stores
+    NaN and Inf as its largest code; p becomes NaN there.  Two steps, so the
+    second decodes the non-finite codes the first wrote.  Every tensor of the
+    size sweep gets a NaN, a +Inf and a -Inf.  NaN codes are compared as a
+    class: IEEE fixes neither the sign nor the payload of a NaN that
+    arithmetic produces (the GPU returns its canonical NaN, an x86 host a
+    negative one), so every BF16 NaN code, and every E4M3 S.1111.111, is
+    mapped to one code on both sides first."""
+    w = W.workload("sweep", m_dtype="bf16", v_dtype=v_dtype, hp=dict(lr=1e-3, weight_decay=0.1))
+    w.max_norm = 0.0
+    gpu = GpuSide(w, seed=7)
+    orc = OracleSide(gpu, range(len(w.sizes)))
+    ghp, ohp = hp_for(w, rounding=rounding, seed=31)
+    for t in (1, 2):
+        W.fill_grads(w, gpu.grads, t, 7)
+        W.inject_nonfinite(gpu.grads, seed=40 + t, frac=1.0)
+        g_np = orc.grads(gpu.grads)
+        gpu.step(t, ghp, clip=False)
+        orc.step(t, g_np, ohp, 1.0, rounding == "stochastic", 31)
+    torch.cuda.synchronize()
+
+    def canon(arr, dtype):
+        """NaN codes to one code, in place (numpy array or torch tensor)."""
+        if dtype == "bf16":
+            a = arr.view(np.uint16) if isinstance(arr, np.ndarray) else arr.view(torch.int16)
+            mask = 0x7F80
+            nan = ((a & mask) == mask) & ((a & 0x7F) != 0)
+            a[nan] = 0x7FC0
+        elif dtype == "e4m3":
+            nan = (arr & 0x7F) == 0x7F
+            arr[nan] = 0x7F
+
+    for k, i in enumerate(range(len(w.sizes))):
+        for dt, g_t, o_a in (("bf16", gpu.m[i], orc.m[k]), (v_dtype, gpu.v[i], orc.v[k])):
+            canon(g_t, dt)
+            canon(o_a, dt)
+    orc.compare(gpu, 1e-5, rounding == "stochastic", steps=2)
+    assert gpu.plan.status() == 0
+
+
 def test_bf16_v_never_moves_with_zero_grad():
     """"When Small Updates Disappear" sec. 2.2 on the GPU: b2 = 0.999,
     nearest rounding, g = 0 -> every BF16 v code stays put."""
