@@ -518,13 +518,58 @@ def run_ours(args, rank, local_rank, world):
 
         _, t, _, _ = e2e_loop(2, t)                     # untimed: both buffers and plans warm
         torch.cuda.synchronize()
-        # the host link's own rate on this machine: one upload with nothing else running
-        u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        u0.record(copy_stream)
-        plans[0].grads_upload(host, stream=copy_stream)
-        u1.record(copy_stream)
+
+        def uploads_alone(n):
+            """Mean ms of n uploads with nothing else on the GPU."""
+            out = []
+            for _ in range(n):
+                u0, u1 = timing_event(), timing_event()
+                u0.record(copy_stream)
+                plans[0].grads_upload(host, stream=copy_stream)
+                u1.record(copy_stream)
+                torch.cuda.synchronize()
+                out.append(u0.elapsed_time(u1))
+            return sum(out) / len(out)
+
+        def uploads_beside_copies(n):
+            """Mean ms of n uploads while the compute stream runs plain device
+            copies that keep HBM busy for the whole upload (no optimizer work)."""
+            out = []
+            for _ in range(n):
+                u0, u1 = timing_event(), timing_event()
+                done = torch.cuda.Event()
+                u0.record(copy_stream)
+                plans[0].grads_upload(host, stream=copy_stream)
+                u1.record(copy_stream)
+                done.record(copy_stream)
+                while not done.query():
+                    for _ in range(16):
+                        hbm_b.copy_(hbm_a)
+                torch.cuda.synchronize()
+                out.append(u0.elapsed_time(u1))
+            return sum(out) / len(out)
+
+        # A/B/C, interleaved three times: uploads alone (A), the overlapped
+        # loop (B: its uploads, its compute, its time per step), uploads
+        # beside HBM-saturating copies (C).  Whether the loop's uploads run
+        # slower than uploads alone, and whether plain HBM traffic does the
+        # same to them, separates the link's own variation from contention
+        # with the compute.
+        hbm_a = torch.empty(2 << 30, dtype=torch.uint8, device=dev)
+        hbm_b = torch.empty_like(hbm_a)
+        ab = {"upload_alone_ms": [], "loop_upload_ms": [], "loop_compute_ms": [], "loop_ms_per_step": [],
+              "upload_beside_hbm_copies_ms": []}
+        kab = max(3, min(5, ke))
+        for _ in range(3):
+            ab["upload_alone_ms"].append(round(uploads_alone(2), 3))
+            l_ms, t, l_up, l_comp = e2e_loop(kab, t)
+            ab["loop_upload_ms"].append(round(l_up, 3))
+            ab["loop_compute_ms"].append(round(l_comp, 3))
+            ab["loop_ms_per_step"].append(round(l_ms / kab, 3))
+            ab["upload_beside_hbm_copies_ms"].append(round(uploads_beside_copies(2), 3))
+        del hbm_a, hbm_b
         torch.cuda.synchronize()
-        upload_alone_ms = u0.elapsed_time(u1)
+        upload_alone_ms = sum(ab["upload_alone_ms"]) / len(ab["upload_alone_ms"])
         if pg:
             pg.barrier()
         torch.cuda.synchronize()
@@ -541,6 +586,9 @@ def run_ours(args, rank, local_rank, world):
                "h2d_gbs_alone": round(h2d / (upload_alone_ms / 1e3) / 1e9, 1),
                "upload_ms_in_loop": round(upload_ms, 3), "compute_ms_in_loop": round(compute_ms, 3),
                "h2d_gbs_in_loop": round(h2d / (upload_ms / 1e3) / 1e9, 1),
+               "ab": {**ab, "steps_per_loop": kab,
+                      "how": "three rounds of: two uploads alone; the overlapped loop (uploads, norm + "
+                             "step); two uploads beside device copies that keep HBM busy"},
                "note": "per step: opt_grads_upload of the step's gradients from pinned host memory (one "
                        "cudaMemcpyAsync per tensor, copy stream, double-buffered), opt_grad_norm, the step, "
                        "and a copy of the 48-byte norm result to pinned host memory"}
