@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libpsopt.so")
 
-CU_SOURCES = ["api.cu", "norm.cu", "step_f32.cu", "step_lowp.cu", "codec.cu", "norm_noalloc.cu", "lamb.cu"]
+CU_SOURCES = ["api.cu", "norm.cu", "step_f32.cu", "step_lowp.cu", "step_small.cu", "codec.cu", "norm_noalloc.cu",
+              "lamb.cu"]
 CPP_SOURCES = ["host.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-I", INCLUDE, "-Xcompiler", "-fPIC",

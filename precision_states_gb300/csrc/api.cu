@@ -31,6 +31,10 @@ struct opt_plan {
   int32_t m_dtype = OPT_F32, v_dtype = OPT_F32;
   int combo = SC_F32;
   bool has_m2 = false;
+  // per gradient-dtype bucket: the whole bucket as kernel parameters, when
+  // it is short enough for the short-list step (small_ok)
+  SmallList small[2];
+  bool small_ok[2] = {false, false};
   std::vector<void*> grad_dev;          // per tensor, for opt_grads_upload
   std::vector<int64_t> grad_bytes;
   // one device allocation: tensors | norm chunks | tiles | slots | result | counter | flags |
@@ -196,6 +200,25 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
     P->grad_bytes[(size_t)i] = state_bytes(L->grad_dtype[i], L->numel[i]);
   }
 
+  // short buckets for the short-list step: at most kSmallMaxTensors
+  // non-empty tensors and kSmallMaxTiles tiles, in list order
+  for (int b = 0; b < 2; ++b) {
+    SmallList& sl = P->small[b];
+    std::memset(&sl, 0, sizeof sl);
+    int64_t tiles = 0;
+    bool ok = true;
+    for (int32_t i = 0; i < L->n && ok; ++i) {
+      if (L->numel[i] == 0 || (L->grad_dtype[i] == OPT_BF16 ? 1 : 0) != b) continue;
+      if (sl.n == kSmallMaxTensors) { ok = false; break; }
+      tiles += (L->numel[i] + kTileElems - 1) / kTileElems;
+      sl.tensor[sl.n] = (uint32_t)i;
+      sl.tile_end[sl.n] = tiles;
+      sl.td[sl.n] = tds[(size_t)i];
+      sl.n += 1;
+    }
+    P->small_ok[b] = ok && sl.n > 0 && tiles <= kSmallMaxTiles;
+  }
+
   // the norm's table: each chunk's first gradient element, resolved
   std::vector<NormChunk> nchunks((size_t)nch);
   for (int64_t k = 0; k < nch; ++k) {
@@ -344,9 +367,10 @@ static int do_step(opt_plan* P, const opt_hparams* hp, int64_t step, const opt_n
     a.tile_end = P->tile_begin[b + 1];
     if (a.tile_end <= a.tile_begin) continue;
     const int dt = b == 0 ? OPT_F32 : OPT_BF16;
-    if (P->combo == SC_F32) e = launch_step_fp32_states(dt, algo, a, P->sm_count, s);
-    else e = launch_step_lowp_states(dt, P->combo, hp->rounding == OPT_ROUND_STOCHASTIC, a,
-                                     P->sm_count, s);
+    const bool sr = hp->rounding == OPT_ROUND_STOCHASTIC;
+    if (P->small_ok[b] && !dev_step && !drill) e = launch_step_small(dt, P->combo, algo, sr, a, P->small[b], s);
+    else if (P->combo == SC_F32) e = launch_step_fp32_states(dt, algo, a, P->sm_count, s);
+    else e = launch_step_lowp_states(dt, P->combo, sr, a, P->sm_count, s);
   }
   return cuda_status(e);
 }

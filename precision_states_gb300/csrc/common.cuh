@@ -67,6 +67,19 @@ struct StepArgs {
   int drill;                          // nonzero: the staged step's waits run out on purpose
 };
 
+// A short bucket passed whole in a kernel's parameters (the short-list step,
+// step_small.cu): at most kSmallMaxTensors non-empty tensors in list order,
+// each with its descriptor, its index in the plan's list and the end of its
+// tiles in the bucket (tiles of kTileElems; an inclusive prefix sum).
+constexpr int kSmallMaxTensors = 8;
+constexpr int64_t kSmallMaxTiles = 4096;
+struct SmallList {
+  int n;
+  uint32_t tensor[kSmallMaxTensors];
+  int64_t tile_end[kSmallMaxTensors];
+  TensorDesc td[kSmallMaxTensors];
+};
+
 // ------------------------------------------------------------- bit views
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }

@@ -14,6 +14,7 @@ struct TensorDesc;
 struct NormSlot;
 struct NormChunk;
 struct StepArgs;
+struct SmallList;
 
 // Resident CTAs per SM of one kernel, cached per device and safe to fill
 // from several host threads.  The value is a property of the kernel and the
@@ -76,6 +77,10 @@ cudaError_t launch_step_scalars(const opt_step_scalars& base, int64_t* counter, 
 cudaError_t launch_set_step(int64_t* counter, int64_t value, cudaStream_t s);
 cudaError_t launch_step_lowp_states(int grad_dtype, int combo, int stochastic, const StepArgs& args,
                                     int sm_count, cudaStream_t s);
+// fused step for a short bucket (SmallList): one CTA per tile, descriptors
+// in the kernel parameters; every state combination and algorithm
+cudaError_t launch_step_small(int grad_dtype, int combo, int algo, int stochastic, const StepArgs& args,
+                              const SmallList& list, cudaStream_t s);
 
 // update-norm clipping (LAMB / max_unorm): phase 0 = per-tile sums (one
 // bucket), 1 = per-tensor ratios (all tensors), 2 = apply (one bucket)

@@ -98,6 +98,26 @@ def test_step_writes_stay_inside(v_dtype, rounding):
     plan.close()
 
 
+@pytest.mark.parametrize("v_dtype,rounding", [("f32", "nearest"), ("bf16", "stochastic"), ("e4m3", "nearest"),
+                                              ("e2m2", "stochastic")])
+def test_short_list_step_writes_stay_inside(v_dtype, rounding):
+    """The short-list launch shape (at most eight tensors): ragged sizes."""
+    g = Guarded()
+    sizes = [1, 3, 2047, 2049, 4097, 32769, 70001]
+    m_dtype = "f32" if v_dtype == "f32" else "bf16"
+    plan = guarded_plan(g, sizes, ["bf16"] * len(sizes), m_dtype, v_dtype)
+    d_res = g.make(48, torch.uint8)
+    hp = ps.hparams(lr=1e-2, weight_decay=0.1, rounding=rounding, seed=3, count_unchanged=v_dtype != "f32")
+    for t in range(1, 4):
+        plan.grad_norm(1.0, d_out=d_res.data_ptr(), sync=False)
+        plan.adamw_step(hp, t, d_res.data_ptr())
+    if v_dtype != "f32":
+        plan.unchanged_count()
+    assert plan.status() == 0
+    g.check(f"short list {v_dtype} {rounding}")
+    plan.close()
+
+
 def test_ademamix_and_lamb_writes_stay_inside():
     g = Guarded()
     plan = guarded_plan(g, SIZES, mixed(SIZES), "f32", "f32", m2=True)

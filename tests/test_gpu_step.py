@@ -55,6 +55,52 @@ def test_lowp_states_codes(v_dtype, rounding, gdt):
     run_parity(w, 12, 1e-6, rounding=rounding, count=True, check_every=4)
 
 
+SHORT = [1, 3, 2049, 4097, 70001, 300001]     # six tensors: the short-list launch shape
+
+
+@pytest.mark.parametrize("v_dtype,rounding", [("f32", "nearest"), ("bf16", "nearest"), ("bf16", "stochastic"),
+                                              ("e4m3", "nearest"), ("e4m3", "stochastic"),
+                                              ("e2m2", "nearest"), ("e2m2", "stochastic")])
+@pytest.mark.parametrize("gdt", ["bf16", "f32"])
+def test_short_list_path(v_dtype, rounding, gdt):
+    """A bucket of at most eight tensors and 4096 tiles takes the short-list
+    launch shape (descriptors in the kernel parameters, one CTA per tile):
+    parity with the oracle, clipped, with unchanged counts."""
+    m_dtype = "f32" if v_dtype == "f32" else "bf16"
+    w = W.workload("sweep", sizes=SHORT, grad_dtype=gdt, m_dtype=m_dtype, v_dtype=v_dtype,
+                   hp=dict(lr=1e-3, weight_decay=0.1, beta2=0.999), sigma_decay_steps=6)
+    run_parity(w, 6, 1e-5, rounding=rounding, count=v_dtype != "f32", check_every=3)
+
+
+def test_short_list_path_ademamix():
+    w = W.workload("sweep", sizes=SHORT, algo="ademamix", hp=dict(lr=1e-2, weight_decay=0.1))
+    run_parity(w, 1, 1e-6)
+    run_parity(w, 5, 1e-5)
+
+
+@pytest.mark.parametrize("v_dtype,rounding", [("f32", "nearest"), ("bf16", "stochastic"), ("e4m3", "nearest"),
+                                              ("e2m2", "stochastic")])
+def test_short_and_persistent_shapes_agree_bitwise(v_dtype, rounding):
+    """The same six tensors stepped alone (short-list shape) and with three
+    one-element tensors appended (nine tensors: the persistent kernel) end
+    with the same bits in p, m and v (no clipping: the extra tensors would
+    change the norm)."""
+    m_dtype = "f32" if v_dtype == "f32" else "bf16"
+    out = []
+    for sizes in (SHORT, SHORT + [1, 1, 1]):
+        w = W.workload("sweep", sizes=sizes, m_dtype=m_dtype, v_dtype=v_dtype,
+                       hp=dict(lr=1e-3, weight_decay=0.1), sigma_decay_steps=4)
+        gpu = GpuSide(w, seed=11)
+        ghp, _ = hp_for(w, rounding=rounding, seed=5)
+        for t in range(1, 5):
+            W.fill_grads(w, gpu.grads, t, 11)
+            gpu.step(t, ghp, clip=False)
+        torch.cuda.synchronize()
+        out.append([x.clone() for x in gpu.params[:6] + gpu.m[:6] + gpu.v[:6]])
+    for a, b in zip(*out):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
 def test_nonfinite_norm_skips_step():
     w = W.workload("clip_740")
     gpu = GpuSide(w, seed=3)
