@@ -22,8 +22,12 @@
  *
  * Parity pins: every function here is pinned by tests/test_oracle_*.py
  * against closed forms, brute force, library routines or values printed on
- * the pages.  The Philox generator is pinned only by its published
- * known-answer vector and by structural properties (see the test).
+ * the pages: the codecs against torch's casts, brute force over every code
+ * and the carry rule; the norm against exact rational arithmetic; the step,
+ * FP32 and low-precision states alike, against the one-step closed form and
+ * torch.optim.AdamW in float64, with planted mistakes (the `mutation` bits)
+ * shown to fail those pins; the Philox generator against cuRAND's host-side
+ * Philox4_32_10 generator.
  */
 #ifndef PS_ORACLE_H
 #define PS_ORACLE_H
