@@ -81,6 +81,9 @@ def parse():
                     help="FP32 states: device step counter, norm and step replayed from CUDA graphs")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-companions", action="store_true",
+                    help="default run only: skip the short device-timed runs of the other workloads")
+    ap.add_argument("--companion-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="cpu_baseline: time oracle steps over the sample for at least this long")
     ap.add_argument("--oracle-sample-elems", type=int, default=120_000_000,
@@ -171,12 +174,12 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, tag: str = ""):
         self.idx = gpu_index
         self.proc = None
         # the raw samples, beside the summary the JSON line carries
         out_dir = os.environ.get("BENCH_OUT_DIR", os.path.join(ROOT, "bench_out"))
-        self.path = os.path.join(out_dir, f"clocks_rank{gpu_index}.csv")
+        self.path = os.path.join(out_dir, f"clocks{tag}_rank{gpu_index}.csv")
 
     def start(self):
         try:
@@ -307,6 +310,122 @@ def cpu_baseline(w, args):
 
 
 # ---------------------------------------------------------------- our arm
+class Case:
+    """One workload on one device: its seeded tensors, the plan over them,
+    the hyperparameters and the step call the flags select."""
+
+    def __init__(self, w, rounding: str, lamb, dev, seed: int):
+        import torch
+
+        import precision_states_gb300 as ps
+        import workloads as W
+
+        self.w, self.lamb, self.dev = w, lamb, dev
+        self.params = W.make_params(w, dev, seed=seed)
+        self.grads = W.make_grads(w, dev, step=1, seed=seed)
+        self.m = [W.state_storage(w.m_dtype, n, dev) for n in w.sizes]
+        self.v = [W.state_storage(w.v_dtype, n, dev) for n in w.sizes]
+        self.m2 = [W.state_storage(w.m_dtype, n, dev) for n in w.sizes] if w.algo == "ademamix" else None
+        self.plan = ps.Plan(self.params, self.grads, self.m, self.v, self.m2, m_dtype=w.m_dtype,
+                            v_dtype=w.v_dtype)
+        self.hp = ps.hparams(rounding=rounding, seed=1234, **{**dict(beta1=0.9, beta2=0.999), **w.hp})
+        self.clip = w.max_norm > 0
+        self.d_norm = self.plan.norm_buffer() if self.clip else None
+        self.step_fn = self.stepper(self.plan)
+        # The timed steps must not find their inputs in L2 (129 MB on GB300).
+        # A list whose per-step bytes are under four times that is flushed
+        # before every step: a 256 MiB buffer is written, then another 256 MiB
+        # read, so that L2 holds neither the step's data nor dirty lines of
+        # the flush.  Such steps are timed by their own events (norm start to
+        # step end), so the flush stays out of the figure.
+        self.flush = needs_l2_flush(w)
+        if self.flush:
+            self.flush_w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+            self.flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def stepper(self, pl):
+        """The step call on plan pl: AdamW, AdEMAMix, or LAMB with the bound."""
+        if self.lamb is not None:
+            return lambda hp_, t_, dn_, stream=None: pl.lamb_step(hp_, t_, self.lamb, dn_, stream=stream)
+        return pl.ademamix_step if self.w.algo == "ademamix" else pl.adamw_step
+
+    def launches_per_step(self) -> int:
+        """The norm is one launch per gradient dtype (one here; its last CTA
+        finishes), the step one launch (LAMB: three passes)."""
+        return (1 if self.clip else 0) + (3 if self.lamb is not None else 1)
+
+    def one_step(self, t, hp, stream, ev=None, graphs=None):
+        """Norm + step number t on stream; ev = three events (start, after
+        the norm, after the step) or None; graphs replace the launches."""
+        graphs = graphs or {}
+        if self.flush:
+            self.flush_w.fill_(float(t))
+            self.flush_r.sum()
+        if ev is not None:
+            ev[0].record(stream)
+        if self.clip:
+            if "norm" in graphs:
+                graphs["norm"].replay()
+            else:
+                self.plan.grad_norm(self.w.max_norm, sync=False, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        if "step" in graphs:
+            graphs["step"].replay()
+        else:
+            self.step_fn(hp, t, self.d_norm, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    def time_steps(self, hp, stream, t, steps, graphs=None, step_arg=None):
+        """steps timed steps after step t: (last t, per-step event triples,
+        total ms).  A flushed list's total is the sum of its steps' own
+        intervals; otherwise the span of the loop."""
+        import torch
+
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for k in range(steps):
+            t += 1
+            self.one_step(t if step_arg is None else step_arg, hp, stream, evs[k], graphs)
+        end.record(stream)
+        torch.cuda.synchronize()
+        total = start.elapsed_time(end)
+        if self.flush:
+            total = sum(e[0].elapsed_time(e[2]) for e in evs)
+        return t, evs, total
+
+    def norm_clean_ms(self, stream, n: int) -> float:
+        """The norm alone with L2 clean: in the step loop each norm follows a
+        step, and the write-back of the step's dirty L2 lines lands in the
+        norm's interval.  Here a 512 MiB read (untimed) evicts them first, so
+        the norm's events time the kernel's own traffic."""
+        import torch
+
+        rd = torch.ones(2 * FLUSH_BYTES // 4, dtype=torch.float32, device=self.dev)
+        cl = []
+        for k in range(n + 2):
+            rd.sum()
+            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a0.record(stream)
+            self.plan.grad_norm(self.w.max_norm, sync=False, stream=stream)
+            a1.record(stream)
+            torch.cuda.synchronize()
+            if k >= 2:
+                cl.append(a0.elapsed_time(a1))
+        del rd
+        return sum(cl) / len(cl)
+
+    def close(self):
+        import torch
+
+        self.plan.close()
+        for k in ("plan", "d_norm", "step_fn", "params", "grads", "m", "v", "m2", "flush_w", "flush_r"):
+            self.__dict__.pop(k, None)
+        torch.cuda.empty_cache()
+
+
 def run_ours(args, rank, local_rank, world):
     import torch
 
@@ -322,23 +441,12 @@ def run_ours(args, rank, local_rank, world):
         pg = dist
 
     w = apply_overrides(W.workload(args.workload), args)
-    params = W.make_params(w, dev, seed=rank)
-    grads = W.make_grads(w, dev, step=1, seed=rank)
-    m = [W.state_storage(w.m_dtype, n, dev) for n in w.sizes]
-    v = [W.state_storage(w.v_dtype, n, dev) for n in w.sizes]
-    m2 = [W.state_storage(w.m_dtype, n, dev) for n in w.sizes] if w.algo == "ademamix" else None
-    plan = ps.Plan(params, grads, m, v, m2, m_dtype=w.m_dtype, v_dtype=w.v_dtype)
-    hp = ps.hparams(rounding=args.rounding, seed=1234, **{**dict(beta1=0.9, beta2=0.999), **w.hp})
+    case = Case(w, args.rounding, args.lamb, dev, seed=rank)
+    params, grads, m, v, m2 = case.params, case.grads, case.m, case.v, case.m2
+    plan, hp, clip, d_norm = case.plan, case.hp, case.clip, case.d_norm
     stream = torch.cuda.current_stream(dev)
-    clip = w.max_norm > 0
-    d_norm = plan.norm_buffer() if clip else None
-    step_fn = plan.ademamix_step if w.algo == "ademamix" else plan.adamw_step
-    if args.lamb is not None:
-        step_fn = lambda hp_, t_, dn_, stream=None: plan.lamb_step(hp_, t_, args.lamb, dn_, stream=stream)
-    # the norm is one launch per gradient dtype (one here; its last CTA
-    # finishes), the step one launch (LAMB: three passes); with --graph the
-    # device step counter adds one launch
-    launches_per_step = (1 if clip else 0) + (3 if args.lamb is not None else 1) + (1 if args.graph else 0)
+    # with --graph the device step counter adds one launch
+    launches_per_step = case.launches_per_step() + (1 if args.graph else 0)
     if args.graph and (w.m_dtype != "f32" or args.lamb is not None):
         raise SystemExit("--graph needs FP32 states and the AdamW or AdEMAMix step")
     hp_step = hp
@@ -346,42 +454,12 @@ def run_ours(args, rank, local_rank, world):
         hp_step = ps.opt_hparams.from_buffer_copy(hp)
         hp_step.flags |= ps.OPT_STEP_DEVICE_COUNTER
     graphs = {}
-
-    # The timed steps must not find their inputs in L2 (129 MB on GB300).  A
-    # list whose per-step bytes are under four times that is flushed before
-    # every step: a 256 MiB buffer is written, then another 256 MiB read, so
-    # that L2 holds neither the step's data nor dirty lines of the flush.
-    # Such steps are timed by their own events (norm start to step end), so
-    # the flush stays out of the figure.
-    flush = needs_l2_flush(w)
-    if flush:
-        flush_w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-        flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-
-    def one_step(t, ev=None):
-        if flush:
-            flush_w.fill_(float(t))
-            flush_r.sum()
-        if ev is not None:
-            ev[0].record(stream)
-        if clip:
-            if "norm" in graphs:
-                graphs["norm"].replay()
-            else:
-                plan.grad_norm(w.max_norm, sync=False, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        if "step" in graphs:
-            graphs["step"].replay()
-        else:
-            step_fn(hp_step, 0 if args.graph else t, d_norm, stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
+    step_arg = 0 if args.graph else None
 
     t = 0
     for _ in range(args.warmup):
         t += 1
-        one_step(t)
+        case.one_step(t if step_arg is None else step_arg, hp_step, stream)
     torch.cuda.synchronize()
     if args.graph:
         # capture once (nothing runs); each replay is the counter's next step
@@ -392,55 +470,26 @@ def run_ours(args, rank, local_rank, world):
                 plan.grad_norm(w.max_norm, sync=False, stream=side)
         graphs["step"] = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graphs["step"], stream=side):
-            step_fn(hp_step, 0, d_norm, stream=side)
+            case.step_fn(hp_step, 0, d_norm, stream=side)
         torch.cuda.synchronize()
     if pg:
         pg.barrier()
     torch.cuda.synchronize()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
-    start.record(stream)
-    for k in range(args.steps):
-        t += 1
-        one_step(t, evs[k])
-    end.record(stream)
-    torch.cuda.synchronize()
+    t, evs, total_ms = case.time_steps(hp_step, stream, t, args.steps, graphs, step_arg)
     clk = clocks.stop()
-    total_ms = start.elapsed_time(end)
     norm_ms = [e[0].elapsed_time(e[1]) for e in evs]
     step_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    if flush:
-        total_ms = sum(e[0].elapsed_time(e[2]) for e in evs)
     if pg:
         tt = torch.tensor([total_ms], device=dev)
         pg.all_reduce(tt, op=pg.ReduceOp.MAX)
         total_ms = float(tt.item())
     params_per_step = w.numel
     value = params_per_step * world * args.steps / (total_ms / 1e3) / 1e9
-
-    # The norm alone with L2 clean: in the loop above each norm follows a
-    # step, and the write-back of the step's dirty L2 lines lands in the
-    # norm's interval.  Here a 512 MiB read (untimed) evicts them first, so
-    # the norm's events time the kernel's own traffic.
-    norm_clean_ms = None
-    if clip:
-        rd = torch.ones(2 * FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-        cl = []
-        for k in range(min(args.steps, 20) + 2):
-            rd.sum()
-            a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a0.record(stream)
-            plan.grad_norm(w.max_norm, sync=False, stream=stream)
-            a1.record(stream)
-            torch.cuda.synchronize()
-            if k >= 2:
-                cl.append(a0.elapsed_time(a1))
-        norm_clean_ms = sum(cl) / len(cl)
-        del rd
+    norm_clean_ms = case.norm_clean_ms(stream, min(args.steps, 20)) if clip else None
 
     # end-to-end through the C ABI with host buffers.  Every step copies its
     # gradients from pinned host memory (opt_grads_upload) and reads its norm
@@ -456,11 +505,7 @@ def run_ours(args, rank, local_rank, world):
         grads_b = [torch.empty_like(g) for g in grads]
         plan_b = ps.Plan(params, grads_b, m, v, m2, m_dtype=w.m_dtype, v_dtype=w.v_dtype)
         plans = [plan, plan_b]
-        def stepper(pl):
-            if args.lamb is not None:
-                return lambda hp_, t_, dn_, stream=None: pl.lamb_step(hp_, t_, args.lamb, dn_, stream=stream)
-            return pl.ademamix_step if w.algo == "ademamix" else pl.adamw_step
-        steps_of = [stepper(plan), stepper(plan_b)]
+        steps_of = [case.stepper(plan), case.stepper(plan_b)]
         copy_stream = torch.cuda.Stream(dev)
         res_dev = torch.zeros((max(ke, 2), 6), dtype=torch.float64, device=dev)   # 48 B per step
         res_host = torch.zeros((max(ke, 2), 6), dtype=torch.float64, pin_memory=True)
@@ -637,11 +682,15 @@ def run_ours(args, rank, local_rank, world):
                                                 "step's dirty L2 lines (in the loop, their write-back lands "
                                                 "in the norm's interval)"}}
 
+    # the main list's tensors are not needed past this point
+    del params, grads, m, v, m2, plan, d_norm
+    case.close()
+    companions = None
+    if companions_wanted(args, world):
+        companions = run_companions(args, dev, stream, peak)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        del params, grads, m, v, m2
-        plan.close()
-        torch.cuda.empty_cache()
         cpu = cpu_baseline(w, args)
 
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
@@ -653,11 +702,89 @@ def run_ours(args, rank, local_rank, world):
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
             "gpu_launches": launches_per_step * args.steps,
             "per_step_ms": per_step_stats}
+    if companions is not None:
+        line["companions"] = companions
     if rank == 0:
         print(json.dumps(line), flush=True)
     if pg:
         pg.barrier()
         pg.destroy_process_group()
+
+
+# ------------------------------------------------------------- companions
+# The default run also times, briefly and by device events only, every other
+# workload the benchmark covers, so that one invocation records them all:
+# (workload, state override as for --v-dtype, rounding, LAMB bound).
+COMPANIONS = (
+    ("adamw_1m", None, "nearest", None),
+    ("clip_740", None, "nearest", None),
+    ("ademamix_gpt2", None, "nearest", None),
+    ("lowp_gpt2", "f32", "nearest", None),
+    ("lowp_gpt2", "bf16", "nearest", None),
+    ("lowp_gpt2", "bf16", "stochastic", None),
+    ("lowp_gpt2", "e4m3", "nearest", None),
+    ("lowp_gpt2", "e4m3", "stochastic", None),
+    ("lowp_gpt2", "e2m2", "nearest", None),
+    ("lowp_gpt2", "e2m2", "stochastic", None),
+    ("llama3_8b", None, "nearest", 1.0),
+)
+
+
+def companions_wanted(args, world: int) -> bool:
+    """Only the default invocation on one GPU: the Llama-3-8B list with its
+    own states, AdamW, direct launches."""
+    return (world == 1 and not args.no_companions and args.workload == "llama3_8b" and args.v_dtype is None
+            and args.lamb is None and not args.graph)
+
+
+def run_companions(args, dev, stream, peak) -> dict:
+    """Each COMPANIONS entry: a fresh seeded list, --warmup untimed steps,
+    --companion-steps timed ones (events as in the main loop, L2 flushed
+    where the list is small), then freed; plus the standalone cast in every
+    format and rounding.  One clock record covers all of them."""
+    import torch
+
+    import workloads as W
+
+    clocks = ClockSampler(dev.index, tag="_companions")
+    clocks.start()
+    time.sleep(0.3)
+    runs = []
+    for name, vdt, rnd, lamb in COMPANIONS:
+        w = apply_overrides(W.workload(name), argparse.Namespace(v_dtype=vdt, lamb=lamb))
+        case = Case(w, rnd, lamb, dev, seed=0)
+        t = 0
+        for _ in range(args.warmup):
+            t += 1
+            case.one_step(t, case.hp, stream)
+        torch.cuda.synchronize()
+        t, evs, total = case.time_steps(case.hp, stream, t, args.companion_steps)
+        k = len(evs)
+        step_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / k
+        step_bytes = step_bytes_per_param(w) * w.numel
+        rec = {"workload": name, "tensors": len(w.sizes), "params": w.numel, "grad_dtype": w.grad_dtype,
+               "m_dtype": w.m_dtype, "v_dtype": w.v_dtype, "rounding": rnd, "algo": w.algo,
+               "value": round(w.numel * k / (total / 1e3) / 1e9, 3), "ms_per_step": round(total / k, 4),
+               "step_kernel": {"ms_per_launch": round(step_ms, 4), "bytes_per_launch": int(step_bytes),
+                               "frac": round(step_bytes / (step_ms / 1e3) / 1e9 / peak, 4)},
+               "l2": "flushed before every step" if case.flush else "inputs larger than L2"}
+        if lamb is not None:
+            rec["lamb_max_unorm"] = lamb
+        if case.clip:
+            nb = ELEM_BYTES[w.grad_dtype] * w.numel
+            norm_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / k
+            clean = case.norm_clean_ms(stream, k)
+            rec["norm"] = {"ms": round(norm_ms, 4), "frac": round(nb / (norm_ms / 1e3) / 1e9 / peak, 4),
+                           "clean_l2_ms": round(clean, 4),
+                           "clean_l2_frac": round(nb / (clean / 1e3) / 1e9 / peak, 4)}
+        runs.append(rec)
+        case.close()
+        del case
+    casts = cast_rows(args.cast_elems, 50, args.warmup, dev, stream, peak)
+    clk = clocks.stop()
+    return {"how": "each workload seeded afresh, %d warm-up and %d timed steps, CUDA events on the launching "
+                   "stream; fractions of the measured copy bandwidth" % (args.warmup, args.companion_steps),
+            "runs": runs, "cast": casts, "clocks": clk}
 
 
 # ---------------------------------------------------------- reference arm
@@ -742,24 +869,21 @@ def run_stall_curve(args):
                           "model_stationary": model}), flush=True)
 
 
-def run_cast(args):
+def cast_rows(n: int, launches: int, warmup: int, dev, stream, peak, clocks=None) -> list:
     """The standalone cast ("When Small Updates Disappear", sec. 6-8: an fp32
     tensor rounded to BF16, nearest or stochastic, one read and one write
     per element) for BF16, E4M3 and E2M2 through opt_encode, timed with CUDA
-    events over --steps launches after --warmup, beside torch's builtin
+    events over `launches` launches after `warmup`, beside torch's builtin
     round-to-nearest conversions (copy_ into a preallocated BF16 / E4M3
     tensor), which are the hardware-cast yardstick.  The input (4 B per
-    element) is larger than L2, so every launch streams from HBM."""
+    element) is larger than L2, so every launch streams from HBM.  With a
+    ClockSampler, each row carries the clocks of its own launches."""
     import torch
 
     import precision_states_gb300 as ps
 
-    dev = torch.device("cuda", 0)
-    n = args.cast_elems
     gen = torch.Generator(device=dev).manual_seed(7)
     x = torch.randn(n, generator=gen, device=dev, dtype=torch.float32) * 1e-3
-    peak, peak_src = measured_peak()
-    stream = torch.cuda.current_stream(dev)
     out_bytes = {"bf16": 2, "e4m3": 1, "e2m2": 0.5}
     outs = {"bf16": torch.empty(n, dtype=torch.int16, device=dev),
             "e4m3": torch.empty(n, dtype=torch.uint8, device=dev),
@@ -768,10 +892,8 @@ def run_cast(args):
     if hasattr(torch, "float8_e4m3fn"):
         builtin["e4m3"] = torch.empty(n, dtype=torch.float8_e4m3fn, device=dev)
 
-    launches = max(args.steps, 100)       # ~0.2 ms each: enough launches for a stable mean
-
     def timed(fn):
-        for _ in range(max(3, args.warmup)):
+        for _ in range(max(3, warmup)):
             fn()
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -783,25 +905,43 @@ def run_cast(args):
         return e0.elapsed_time(e1) / launches
 
     ref_ms = {dt: timed(lambda t=t: t.copy_(x)) for dt, t in builtin.items()}
-    clocks = ClockSampler(0)
+    rows = []
     for dt in ("bf16", "e4m3", "e2m2"):
         for rnd in ("nearest", "stochastic"):
-            clocks.start()
-            time.sleep(0.2)
+            if clocks is not None:
+                clocks.start()
+                time.sleep(0.2)
             ms = timed(lambda: ps.opt_encode(x, outs[dt], dt, rnd, seed=11, tensor_index=0, step=1,
                                              stream=stream))
-            clk = clocks.stop()
             nbytes = n * (4 + out_bytes[dt])
             gbs = nbytes / (ms / 1e3) / 1e9
-            line = {"report": "standalone cast", "elements": n, "format": dt, "rounding": rnd,
-                    "ms_per_launch": round(ms, 4), "gelem_per_s": round(n / (ms / 1e3) / 1e9, 2),
-                    "hbm_gbs": round(gbs, 1), "frac": round(gbs / peak, 4), "peak_gbs": peak, "peak_source": peak_src,
-                    "bytes_per_elem": 4 + out_bytes[dt], "launches": launches, "warmup": max(3, args.warmup),
-                    "l2": "input larger than L2 (%.2f GB)" % (4 * n / 1e9), "clocks": clk}
+            row = {"elements": n, "format": dt, "rounding": rnd, "ms_per_launch": round(ms, 4),
+                   "gelem_per_s": round(n / (ms / 1e3) / 1e9, 2), "hbm_gbs": round(gbs, 1),
+                   "frac": round(gbs / peak, 4), "bytes_per_elem": 4 + out_bytes[dt], "launches": launches}
+            if clocks is not None:
+                row["clocks"] = clocks.stop()
             if dt in ref_ms:
-                line["builtin_rne_ms"] = round(ref_ms[dt], 4)
-                line["vs_builtin_rne"] = round(ref_ms[dt] / ms, 4)
-            print(json.dumps(line), flush=True)
+                row["builtin_rne_ms"] = round(ref_ms[dt], 4)
+                row["vs_builtin_rne"] = round(ref_ms[dt] / ms, 4)
+            rows.append(row)
+    del x, outs, builtin
+    torch.cuda.empty_cache()
+    return rows
+
+
+def run_cast(args):
+    """One JSON line per format and rounding of the standalone cast."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    peak, peak_src = measured_peak()
+    launches = max(args.steps, 100)       # ~0.2 ms each: enough launches for a stable mean
+    rows = cast_rows(args.cast_elems, launches, args.warmup, dev, torch.cuda.current_stream(dev), peak,
+                     clocks=ClockSampler(0))
+    for row in rows:
+        line = {"report": "standalone cast", **row, "peak_gbs": peak, "peak_source": peak_src,
+                "warmup": max(3, args.warmup), "l2": "input larger than L2 (%.2f GB)" % (4 * row["elements"] / 1e9)}
+        print(json.dumps(line), flush=True)
 
 
 def main():

@@ -247,6 +247,7 @@ class Plan:
         if getattr(self, "handle", None):
             lib().opt_plan_destroy(self.handle)
             self.handle = None
+        self._keep = None          # the tensors are free to go with the plan
 
     def __del__(self):
         try:
