@@ -44,10 +44,21 @@ lamb_stats_kernel(const StepArgs a, TileSums* __restrict__ sums) {
     if (a.d_norm->status != OPT_OK) return;
     coef = a.d_norm->clip_coef;
   }
-  __shared__ float s_u[kLambThreads / 32], s_p[kLambThreads / 32];
+  // the warps' partial sums, double-buffered by tile parity: thread 0 reads
+  // tile k's after the tile's barrier, and the warps write tile k + 2's only
+  // after tile k + 1's barrier, which thread 0 reaches after its reads.  One
+  // barrier per tile instead of two (the second guarded a single buffer)
+  // took the three passes from 0.961 to 0.994-0.996 of the measured copy
+  // bandwidth on the Llama-3-8B list and from 0.973 to 1.026-1.029 on the
+  // 740-tensor list (GB300, A/B/A), with bit-identical results.  No barrier
+  // at all (per-warp slots, the slices summed by the ratio pass) was faster
+  // on the 740-tensor list but made this pass 7 % slower on the Llama-3-8B
+  // list: there the warps of a CTA gain from reading a tile together.
+  __shared__ float s_u[2][kLambThreads / 32], s_p[2][kLambThreads / 32];
   const int off = threadIdx.x * 8;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int64_t i = a.tile_begin + blockIdx.x; i < a.tile_end; i += gridDim.x) {
+  int par = 0;
+  for (int64_t i = a.tile_begin + blockIdx.x; i < a.tile_end; i += gridDim.x, par ^= 1) {
     const opt_chunk tl = a.tiles[i];
     float su = 0.0f, sp = 0.0f;
     if (off < (int)tl.len) {
@@ -90,17 +101,16 @@ lamb_stats_kernel(const StepArgs a, TileSums* __restrict__ sums) {
       su = __fadd_rn(su, __shfl_xor_sync(0xFFFFFFFFu, su, o));
       sp = __fadd_rn(sp, __shfl_xor_sync(0xFFFFFFFFu, sp, o));
     }
-    if (lane == 0) { s_u[warp] = su; s_p[warp] = sp; }
+    if (lane == 0) { s_u[par][warp] = su; s_p[par][warp] = sp; }
     __syncthreads();
     if (threadIdx.x == 0) {
       double tu = 0.0, tp = 0.0;
-      for (int w = 0; w < kLambThreads / 32; ++w) { tu += (double)s_u[w]; tp += (double)s_p[w]; }
+      for (int w = 0; w < kLambThreads / 32; ++w) { tu += (double)s_u[par][w]; tp += (double)s_p[par][w]; }
       TileSums r;
       r.su = tu;
       r.sp = tp;
       sums[i] = r;
     }
-    __syncthreads();
   }
 }
 
