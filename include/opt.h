@@ -30,7 +30,7 @@
  *  - Pointers named d_* or held in an opt_tensor_list are DEVICE pointers on
  *    the device that was current when the plan was created; everything else
  *    is host memory.  The caller owns every tensor; a plan owns only its
- *    chunk table and a small workspace (about 16 bytes per 32768 elements).
+ *    chunk table and a small workspace (about 16 bytes per 2048 elements).
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Calls are stream-ordered and never synchronise, except where
  *    a host output (h_*) is requested.
@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define OPT_ABI_VERSION 1
+#define OPT_ABI_VERSION 2
 
 /* ---- status codes --------------------------------------------------- */
 #define OPT_OK            0
@@ -61,7 +61,7 @@ extern "C" {
 #define OPT_EALIGN       -3   /* a device pointer not 16-byte aligned */
 #define OPT_ECUDA        -4   /* a CUDA runtime call failed */
 #define OPT_ENOMEM       -5   /* workspace allocation failed */
-#define OPT_ELIMIT       -6   /* list exceeds opt_grad_norm_noalloc's fixed limits */
+#define OPT_ELIMIT       -6   /* list exceeds a fixed limit of the norm (see OPT_NORM_MAX_PART, opt_grad_norm_noalloc) */
 
 /* ---- storage types ----------------------------------------------------
  * OPT_F32   IEEE binary32.
@@ -319,11 +319,11 @@ int opt_decode(const void* d_in, float* d_out, int64_t n, int32_t dtype, void* s
  * cudaMalloc, cudaFree or allocating library routine, and no host heap.  The
  * pages describe no such variant; it has no counterpart there.
  *
- * Scratch: one fixed device array inside the library (4,515,072 bytes, held
+ * Scratch: one fixed device array inside the library (4,466,432 bytes, held
  * by every GPU that loads the library until the process exits), large enough
  * for OPT_NOALLOC_MAX_TENSORS tensors and OPT_NOALLOC_MAX_CHUNKS chunks of
- * OPT_CHUNK_ELEMS elements (about 8.6e9 elements).  Larger lists are rejected
- * with OPT_ELIMIT before any GPU work.
+ * the norm's table (about 8.6e9 elements at OPT_CHUNK_ELEMS per chunk).
+ * Larger lists are rejected with OPT_ELIMIT before any GPU work.
  *
  * Inputs: n tensors; numel, grad (device pointers, 16-byte aligned) and
  * grad_dtype (OPT_F32 or OPT_BF16) are HOST arrays, copied into the scratch
@@ -348,23 +348,40 @@ int opt_grad_norm_noalloc(int32_t n, const int64_t* numel, const void* const* gr
 
 /* ---- host-only helpers (no GPU needed) ----------------------------------- */
 
-/* Elements per chunk of the chunk table. */
+/* The norm's chunks.  A gradient-dtype bucket of E elements is cut into
+ * chunks of OPT_NORM_CHUNK_MIN elements when E < 2^29, 2 OPT_NORM_CHUNK_MIN
+ * when E < 2^31, OPT_CHUNK_ELEMS otherwise -- doubled while any of the
+ * bucket's OPT_NORM_SLOTS slots would own more than OPT_NORM_MAX_PART chunks
+ * (slot s owns chunks s, s + OPT_NORM_SLOTS, ...).  A small list then gives
+ * every slot's warps many chunks to share, a large one fewer per-chunk costs.
+ * The size depends on the sizes alone, so the result stays bit-identical run
+ * to run; a bucket whose tensors alone exceed the bound (more than
+ * OPT_NORM_SLOTS * OPT_NORM_MAX_PART of them) returns OPT_ELIMIT. */
+#define OPT_NORM_CHUNK_MIN 8192
 #define OPT_CHUNK_ELEMS 32768
-/* Number of fixed partial-sum slots per gradient-dtype bucket. */
-#define OPT_NORM_SLOTS 912
+/* Fixed partial-sum slots per gradient-dtype bucket: one CTA of 24 warps each
+ * (one per SM of a GB300). */
+#define OPT_NORM_SLOTS 152
+#define OPT_NORM_MAX_PART 4096
 
 typedef struct opt_chunk {
   uint32_t tensor;   /* index into the list */
-  uint32_t len;      /* 1..OPT_CHUNK_ELEMS */
-  int64_t start;     /* element offset in the tensor, multiple of OPT_CHUNK_ELEMS */
+  uint32_t len;      /* 1..chunk size of its bucket */
+  int64_t start;     /* element offset in the tensor, a multiple of that size */
 } opt_chunk;
 
-/* Chunk table from sizes and gradient dtypes only: bucket 0 (FP32 grads)
- * first, then bucket 1 (BF16 grads); within a bucket, tensors in list order
- * and chunks in element order.  Writes up to `cap` entries to `out` (may be
- * NULL to count) and the bucket boundaries to bucket_begin[0..2] (chunks of
- * bucket b are [bucket_begin[b], bucket_begin[b+1])).  Returns the chunk
- * count, or a negative status. */
+/* Chunk size of gradient-dtype bucket `bucket` (0: FP32 gradients, 1: BF16)
+ * of a list, by the rule above; a positive power of two, or a negative
+ * status. */
+int64_t opt_norm_chunk_elems(int32_t n, const int64_t* numel, const int32_t* grad_dtype, int32_t bucket);
+
+/* The norm's chunk table, from sizes and gradient dtypes only: bucket 0
+ * (FP32 grads) first, then bucket 1 (BF16 grads), each in chunks of its
+ * opt_norm_chunk_elems; within a bucket, tensors in list order and chunks in
+ * element order.  Writes up to `cap` entries to `out` (may be NULL to count)
+ * and the bucket boundaries to bucket_begin[0..2] (chunks of bucket b are
+ * [bucket_begin[b], bucket_begin[b+1])).  Returns the chunk count, or a
+ * negative status. */
 int64_t opt_chunk_table(int32_t n, const int64_t* numel, const int32_t* grad_dtype,
                         opt_chunk* out, int64_t cap, int64_t bucket_begin[3]);
 

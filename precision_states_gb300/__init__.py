@@ -26,8 +26,8 @@ OPT_STEP_RESET_STATES = 1
 OPT_STEP_DEVICE_COUNTER = 2
 OPT_STEP_WAIT_DRILL = 4
 OPT_FLAG_WAIT_TIMEOUT, OPT_FLAG_DRAIN_TIMEOUT = 1, 2
-OPT_CHUNK_ELEMS = 32768
-OPT_NORM_SLOTS = 912
+OPT_NORM_CHUNK_MIN, OPT_CHUNK_ELEMS = 8192, 32768
+OPT_NORM_SLOTS, OPT_NORM_MAX_PART = 152, 4096
 
 DTYPES = {"f32": OPT_F32, "bf16": OPT_BF16, "e4m3": OPT_E4M3, "e2m2": OPT_E2M2}
 
@@ -93,6 +93,8 @@ _SIGS = {
     "opt_decode": (_c.c_int, [_vp, _vp, _c.c_int64, _c.c_int32, _vp]),
     "opt_chunk_table": (_c.c_int64, [_c.c_int32, _c.POINTER(_c.c_int64), _c.POINTER(_c.c_int32),
                                      _c.POINTER(opt_chunk), _c.c_int64, _c.POINTER(_c.c_int64)]),
+    "opt_norm_chunk_elems": (_c.c_int64, [_c.c_int32, _c.POINTER(_c.c_int64), _c.POINTER(_c.c_int32),
+                                          _c.c_int32]),
     "opt_step_scalars_compute": (_c.c_int, [_c.POINTER(opt_hparams), _c.c_int64,
                                             _c.POINTER(opt_step_scalars)]),
     "opt_norm_combine": (_c.c_int, [_c.POINTER(opt_norm_result), _c.c_int32, _c.c_double,
@@ -164,6 +166,14 @@ def opt_chunk_table(numel, grad_dtype):
     out = (opt_chunk * max(cnt, 1))()
     lib().opt_chunk_table(n, ne, gd, out, cnt, bb)
     return [(out[i].tensor, out[i].len, out[i].start) for i in range(cnt)], list(bb)
+
+
+def opt_norm_chunk_elems(numel, grad_dtype, bucket: int) -> int:
+    """Host-only: the norm's chunk size for gradient-dtype bucket 0 (FP32) or 1 (BF16)."""
+    n = len(numel)
+    ne = (_c.c_int64 * max(n, 1))(*numel)
+    gd = (_c.c_int32 * max(n, 1))(*grad_dtype)
+    return _check(lib().opt_norm_chunk_elems(n, ne, gd, bucket), "opt_norm_chunk_elems")
 
 
 def opt_step_scalars_compute(hp: opt_hparams, step: int) -> dict:

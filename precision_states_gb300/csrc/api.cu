@@ -165,9 +165,10 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
   std::vector<opt_chunk> chunks((size_t)nch);
   opt_chunk_table(L->n, L->numel, L->grad_dtype, chunks.data(), nch, P->bucket_begin);
   P->n_chunks = nch;
-  const int64_t ntl = build_table(L->n, L->numel, L->grad_dtype, kTileElems, nullptr, 0, P->tile_begin);
+  const int64_t tile_elems[2] = {kTileElems, kTileElems};
+  const int64_t ntl = build_table(L->n, L->numel, L->grad_dtype, tile_elems, nullptr, 0, P->tile_begin);
   std::vector<opt_chunk> tiles((size_t)ntl);
-  build_table(L->n, L->numel, L->grad_dtype, kTileElems, tiles.data(), ntl, P->tile_begin);
+  build_table(L->n, L->numel, L->grad_dtype, tile_elems, tiles.data(), ntl, P->tile_begin);
   P->n_tiles = ntl;
   P->tile_first.assign((size_t)L->n, 0);
   P->tile_count.assign((size_t)L->n, 0);

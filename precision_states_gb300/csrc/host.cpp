@@ -20,7 +20,7 @@ const char* opt_strerror(int status) {
     case OPT_EALIGN: return "device pointer not 16-byte aligned";
     case OPT_ECUDA: return "CUDA runtime error";
     case OPT_ENOMEM: return "out of device memory";
-    case OPT_ELIMIT: return "list exceeds the no-allocation norm's fixed limits";
+    case OPT_ELIMIT: return "list exceeds a fixed limit of the norm";
     default: return "unknown status";
   }
 }
@@ -33,7 +33,7 @@ namespace psopt {
 // 'Correctness properties': host-side decomposition from sizes, no atomics;
 // 'What': one launch per dtype bucket).  FP32-gradient tensors first, then
 // BF16; list order within a bucket; element order within a tensor.
-int64_t build_table(int32_t n, const int64_t* numel, const int32_t* grad_dtype, int64_t elems,
+int64_t build_table(int32_t n, const int64_t* numel, const int32_t* grad_dtype, const int64_t elems[2],
                     opt_chunk* out, int64_t cap, int64_t bucket_begin[3]) {
   if (n < 0 || (n > 0 && (numel == nullptr || grad_dtype == nullptr))) return OPT_EINVAL;
   for (int32_t i = 0; i < n; ++i) {
@@ -46,11 +46,11 @@ int64_t build_table(int32_t n, const int64_t* numel, const int32_t* grad_dtype, 
     if (bucket_begin) bucket_begin[b] = count;
     for (int32_t i = 0; i < n; ++i) {
       if (grad_dtype[i] != buckets[b]) continue;
-      for (int64_t start = 0; start < numel[i]; start += elems) {
+      for (int64_t start = 0; start < numel[i]; start += elems[b]) {
         if (out != nullptr && count < cap) {
           const int64_t left = numel[i] - start;
           out[count].tensor = (uint32_t)i;
-          out[count].len = (uint32_t)(left < elems ? left : elems);
+          out[count].len = (uint32_t)(left < elems[b] ? left : elems[b]);
           out[count].start = start;
         }
         ++count;
@@ -60,13 +60,48 @@ int64_t build_table(int32_t n, const int64_t* numel, const int32_t* grad_dtype, 
   if (bucket_begin) bucket_begin[2] = count;
   return count;
 }
+
+// The norm's chunk size for one dtype bucket (the rule stated at
+// OPT_NORM_CHUNK_MIN in opt.h).  Measured on GB300 with the norm's
+// one-CTA-per-SM kernel: 8K-element chunks were fastest on the 740-tensor
+// list (197M elements; 16K and 4K 3 % slower), 32K on the Llama-3-8B list
+// (8.03e9; 16K 1 % slower).
+int64_t norm_chunk_elems(int32_t n, const int64_t* numel, const int32_t* grad_dtype, int bucket) {
+  if (n < 0 || (n > 0 && (numel == nullptr || grad_dtype == nullptr)) || bucket < 0 || bucket > 1)
+    return OPT_EINVAL;
+  const int want = bucket == 0 ? OPT_F32 : OPT_BF16;
+  int64_t elems = 0;
+  for (int32_t i = 0; i < n; ++i) {
+    if (numel[i] < 0) return OPT_EINVAL;
+    if (grad_dtype[i] != OPT_F32 && grad_dtype[i] != OPT_BF16) return OPT_EUNSUPPORTED;
+    if (grad_dtype[i] == want) elems += numel[i];
+  }
+  int64_t ce = elems < (int64_t(1) << 29) ? OPT_NORM_CHUNK_MIN
+             : elems < (int64_t(1) << 31) ? 2 * OPT_NORM_CHUNK_MIN : OPT_CHUNK_ELEMS;
+  for (; ce <= (int64_t(1) << 31); ce *= 2) {
+    int64_t chunks = 0;
+    for (int32_t i = 0; i < n; ++i)
+      if (grad_dtype[i] == want) chunks += (numel[i] + ce - 1) / ce;
+    if ((chunks + OPT_NORM_SLOTS - 1) / OPT_NORM_SLOTS <= OPT_NORM_MAX_PART) return ce;
+  }
+  return OPT_ELIMIT;     // more tensors than the slots can hold chunks
+}
 }  // namespace psopt
 
 extern "C" {
 
 int64_t opt_chunk_table(int32_t n, const int64_t* numel, const int32_t* grad_dtype,
                         opt_chunk* out, int64_t cap, int64_t bucket_begin[3]) {
-  return psopt::build_table(n, numel, grad_dtype, OPT_CHUNK_ELEMS, out, cap, bucket_begin);
+  int64_t ce[2];
+  for (int b = 0; b < 2; ++b) {
+    ce[b] = psopt::norm_chunk_elems(n, numel, grad_dtype, b);
+    if (ce[b] < 0) return ce[b];
+  }
+  return psopt::build_table(n, numel, grad_dtype, ce, out, cap, bucket_begin);
+}
+
+int64_t opt_norm_chunk_elems(int32_t n, const int64_t* numel, const int32_t* grad_dtype, int32_t bucket) {
+  return psopt::norm_chunk_elems(n, numel, grad_dtype, bucket);
 }
 
 // Per-step scalars, formed in double and rounded once ("Investigate SM103

@@ -55,10 +55,12 @@ __host__ __device__ constexpr inline bool step_is_staged(int combo, bool stochas
 // of the step kernel's 256 threads.
 constexpr int64_t kTileElems = 2048;
 
-// Table of pieces of at most `elems` elements (the norm's chunks, the step's
-// tiles), bucketed by gradient dtype; see opt_chunk_table.
-int64_t build_table(int32_t n, const int64_t* numel, const int32_t* grad_dtype, int64_t elems,
+// Table of pieces of at most elems[b] elements in bucket b (the norm's
+// chunks, the step's tiles), bucketed by gradient dtype; see opt_chunk_table.
+int64_t build_table(int32_t n, const int64_t* numel, const int32_t* grad_dtype, const int64_t elems[2],
                     opt_chunk* out, int64_t cap, int64_t bucket_begin[3]);
+// the norm's chunk size for a dtype bucket (see OPT_NORM_CHUNK_MIN)
+int64_t norm_chunk_elems(int32_t n, const int64_t* numel, const int32_t* grad_dtype, int bucket);
 
 // The gradient norm: one pass-1 launch per non-empty dtype bucket b (chunks
 // [bucket_begin[b], bucket_begin[b + 1]) into slots[b * OPT_NORM_SLOTS ...]),

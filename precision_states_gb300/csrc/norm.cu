@@ -19,49 +19,43 @@
 // [2^-40, 2^40] (where fp32 squares could overflow or lose bits) re-reads
 // those elements and accumulates them in double -- a rare, exact slow path.
 //
-// Pass 1 runs OPT_NORM_SLOTS CTAs per dtype bucket; slot s sums chunks
-// s, s + OPT_NORM_SLOTS, ... of the bucket in that order, each chunk's
-// first element resolved to an address in the table.  (Giving each slot one
-// contiguous, equal span of the bucket instead balanced the slots exactly
-// but measured 2-4 % slower on GB300: in this order all CTAs stream one
-// window of memory together.)  Pass 2, the finish, reduces all slots in a
-// fixed order and derives norm2, the inf-norm, the NaN/Inf status and the
-// clip coefficient.  It runs in whichever CTA of the last pass-1 launch
-// completes last: every CTA publishes its slot, then takes a ticket from a
-// completion counter; the CTA holding the last ticket finishes and resets
-// the counter.  Which CTA that is varies from run to run, but the order of
-// the reduction does not, so neither do the bits of the result.  Fusing the
-// finish into pass 1 saves a launch and the gap before it: 2.5 % of the
-// norm on the 740-tensor list, where the finish is a visible share; on the
-// Llama-3-8B list it measured 0.2 % slower, with one counter or with
-// sixteen (so not from contention on the counter).
+// Pass 1 runs OPT_NORM_SLOTS CTAs per dtype bucket, one per SM of a GB300,
+// each of 24 warps.  Slot s owns chunks s, s + OPT_NORM_SLOTS, ... of the
+// bucket (chunks of 8K-32K elements, the size from the bucket's size, each
+// chunk's first element resolved to an address in the table); the slot's
+// warps take its chunks one at a time from a counter in shared memory, and
+// each chunk's sum, reduced by the warp that read it in a fixed shuffle
+// tree, goes to the chunk's own place in shared memory.  The slot's total is
+// those sums in chunk order.  Which warp read a chunk varies from run to run,
+// but no value depends on it, so the norm is bit-identical run to run.
+// (Against 912 CTAs of 128 threads, each summing a fixed set of chunks,
+// 6 per SM: the CTAs of one SM ended a median 16 us apart on the 740-tensor
+// list and 265 us apart on the Llama-3-8B list, because co-resident CTAs get
+// unequal shares of the SM's bandwidth, however equal their work; with the
+// warps of a whole SM sharing its chunks they end within about 20 us, and
+// the Llama-3-8B norm fell from 2.377 to 2.215 ms.)  Pass 2, the finish,
+// reduces all slots in a fixed order and derives norm2, the inf-norm, the
+// NaN/Inf status and the clip coefficient.  It runs in whichever CTA of the
+// last pass-1 launch completes last: every CTA publishes its slot, then
+// takes a ticket from a completion counter; the CTA holding the last ticket
+// finishes and resets the counter.  Fusing the finish into pass 1 saves a
+// launch and the gap before it.
 #include "common.cuh"
 #include "internal.h"
 
 namespace psopt {
 namespace {
 
-// 128 threads and 6 CTAs per SM: the 912 slots are one wave on GB300's 152
-// SMs, and each thread may hold 85 registers -- enough for eight 16-byte
-// loads in flight that rotate (each register refilled as soon as its vector
-// is summed) and two float-float chains (alternate vectors), so that the
-// additions of one vector need not wait for the previous vector's.  Per-CTA
-// timestamps on GB300 showed the pass bound by each SM's throughput (every
-// SM finishing at the same time however the work was split), so the lever
-// is bytes in flight per SM, not balance.  Measured against 8 CTAs per SM
-// with four loads each (in a loop with the AdamW step between norms):
-// Llama-3-8B list 2.453 -> 2.380 ms, 740-tensor list 0.0850 -> 0.0818 ms;
-// with L2 clean before the norm, 0.0773 -> 0.0746 ms.  (Also measured: 608
-// CTAs of 256 threads with six loads, 456 of 256 with eight -- close
-// behind; a ring of 16 KB stages filled by one producer lane's bulk copies,
-// 1 to 3 CTAs per SM -- 3-27 % slower on the 740-tensor list; chunks of 16K
-// or 8K elements -- within 1.5 %; a finish that issues all its slot loads
-// up front -- no change: its time is a chain of latencies.  Earlier, against
-// 256 threads at the 32-register cap with four loads issued together: eight
-// cp.async copies per thread into shared-memory slots were 3 and 12 %
-// slower; 32-byte loads read no faster than 16-byte ones in this order.)
-// Plain reads in the same order reach 7.44 TB/s on GB300.
-constexpr int kNormThreads = 128;
+// 24 warps per CTA, one CTA per SM: each thread may hold 85 registers --
+// eight 16-byte loads in flight that rotate (each register refilled as soon
+// as its vector is summed) and two float-float chains (alternate vectors),
+// so that the additions of one vector need not wait for the previous
+// vector's.  The SM's 768 threads keep 96 KB in flight, as the 6 CTAs of
+// 128 threads before them did.  (Measured in the same probe loop, with the
+// AdamW step between norms: 16 warps of eight loads or 32 of six were
+// 2-4 % slower.)
+constexpr int kNormWarps = 24;
+constexpr int kNormThreads = 32 * kNormWarps;
 constexpr int kDepth = 8;            // 16-byte loads in flight per thread
 
 // Two float-float accumulators (lane x, lane y): value = hi + lo per lane.
@@ -148,34 +142,6 @@ __device__ __forceinline__ uint32_t acc_vec<OPT_F32>(FF2& a, uint4 w) {
   return max(max(w.x & 0x7FFFFFFFu, w.y & 0x7FFFFFFFu), max(w.z & 0x7FFFFFFFu, w.w & 0x7FFFFFFFu));
 }
 
-// Exact slow path over one thread's own elements of a chunk (rare: only
-// when they hold a NaN, an Inf or an extreme magnitude).  Its accumulators
-// live in shared memory, one per thread, so that they hold no registers on
-// the fast path.
-struct SlowAcc {
-  double sum;
-  unsigned long long nans, infs;
-  uint32_t mxbits;
-  uint32_t pad;
-};
-
-template <int GT>
-__device__ __noinline__ void slow_chunk(const char* g, int nvec, int rem, int tid, bool owns_tail,
-                                        SlowAcc& a) {
-  using T = GradTraits<GT>;
-  constexpr int V = T::kVec;
-  auto visit = [&](float x) {
-    if (x != x) { ++a.nans; return; }
-    if (fabsf(x) == __int_as_float(0x7F800000)) { ++a.infs; return; }
-    a.sum += (double)x * (double)x;
-    a.mxbits = max(a.mxbits, f2u(fabsf(x)));
-  };
-  for (int vv = tid; vv < nvec; vv += kNormThreads)
-    for (int j = 0; j < V; ++j) visit(T::elem(g, (int64_t)vv * V + j));
-  if (owns_tail)
-    for (int j = 0; j < rem; ++j) visit(T::elem(g, (int64_t)nvec * V + j));
-}
-
 // What the finish needs, passed to every pass-1 launch of one norm.
 struct NormFinish {
   const NormSlot* all;     // the slots it reduces, in this order
@@ -186,21 +152,17 @@ struct NormFinish {
   opt_norm_result* out;
 };
 
-// One CTA reduces n slots in a fixed order (a strided sum per thread, then
-// fixed shuffle and shared-memory trees) and writes the result.  The slots
-// are read through L2, where the other CTAs' stores landed.
+// One warp reduces n slots in a fixed order (lane l: slots l, l + 32, ... in
+// order; then a butterfly, after which every lane holds the same values) and
+// lane 0 writes the result.  The slots are read through L2, where the other
+// CTAs' stores landed.
 __device__ __forceinline__ void finish_slots(const NormSlot* __restrict__ slots, int n, double max_norm,
                                              opt_norm_result* __restrict__ out) {
-  constexpr int kWarps = kNormThreads / 32;
-  __shared__ double s_sum[kWarps];
-  __shared__ unsigned long long s_nan[kWarps], s_inf[kWarps];
-  __shared__ float s_max[kWarps];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lane = threadIdx.x & 31;
   double sum = 0.0;
   unsigned long long nans = 0, infs = 0;
   float mx = 0.0f;
-#pragma unroll 4
-  for (int i = tid; i < n; i += kNormThreads) {
+  for (int i = lane; i < n; i += 32) {
     const uint4* q = reinterpret_cast<const uint4*>(slots + i);
     const uint4 a = __ldcg(q), b = __ldcg(q + 1);
     sum += __hiloint2double((int)a.y, (int)a.x);
@@ -215,23 +177,7 @@ __device__ __forceinline__ void finish_slots(const NormSlot* __restrict__ slots,
     infs += __shfl_xor_sync(0xFFFFFFFFu, infs, o);
     mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
   }
-  if (lane == 0) {
-    s_sum[warp] = sum;
-    s_nan[warp] = nans;
-    s_inf[warp] = infs;
-    s_max[warp] = mx;
-  }
-  __syncthreads();
-  if (tid != 0) return;
-  sum = 0.0;
-  nans = infs = 0;
-  mx = 0.0f;
-  for (int w = 0; w < kWarps; ++w) {
-    sum += s_sum[w];
-    nans += s_nan[w];
-    infs += s_inf[w];
-    mx = fmaxf(mx, s_max[w]);
-  }
+  if (lane != 0) return;
   opt_norm_result r;
   r.nan_count = nans;
   r.inf_count = infs;
@@ -258,126 +204,181 @@ __device__ __forceinline__ void finish_slots(const NormSlot* __restrict__ slots,
   *out = r;
 }
 
+// One chunk, read and summed by one warp: lane l takes vectors l, l + 32,
+// ... (kDepth loads in flight, rotating, into two float-float chains), the
+// lane owning vector nvec loads the ragged tail element-wise.  Returns the
+// chunk's sum of squares (the lanes' float-float sums merged in a fixed
+// shuffle tree, lane 0's value), and adds its max |g| (fp32 bits) and NaN /
+// Inf counts to the CTA's.  A chunk holding a NaN, an Inf or a magnitude
+// outside [2^-40, 2^40] in any lane (fp32 squares could overflow or lose
+// bits) is read again by all lanes and summed exactly in double: rare.
 template <int GT>
-__global__ void __launch_bounds__(kNormThreads, 6)
-norm_partials_kernel(const NormChunk* __restrict__ chunks, int64_t cbegin, int64_t cend,
-                     NormSlot* __restrict__ slots, NormFinish fin) {
+__device__ __forceinline__ double chunk_sum(const char* __restrict__ g, uint32_t len, int lane,
+                                            unsigned int* s_max, unsigned long long* s_nan,
+                                            unsigned long long* s_inf) {
   using T = GradTraits<GT>;
   constexpr int V = T::kVec;
-  const int tid = threadIdx.x;
+  const int nvec = (int)(len / V);
+  const int rem = (int)(len % V);
+  FF2 acc = {0ull, 0ull};
+  uint32_t cmax = 0;
+  int left = nvec > lane ? (nvec - lane + 31) / 32 : 0;
+  const char* q = g + lane * 16;
+  constexpr int kStep = 32 * 16;
+  if (left >= kDepth) {
+    uint4 w[kDepth];
+    FF2 acc2 = {0ull, 0ull};     // a second chain: odd vectors of a round
+#pragma unroll
+    for (int d = 0; d < kDepth; ++d) w[d] = ld_nc_u4(q + d * kStep);
+    q += kDepth * kStep;
+    for (left -= kDepth; left >= kDepth; left -= kDepth, q += kDepth * kStep) {
+#pragma unroll
+      for (int d = 0; d < kDepth; ++d) {
+        cmax = max(cmax, acc_vec<GT>((d & 1) ? acc2 : acc, w[d]));
+        w[d] = ld_nc_u4(q + d * kStep);
+      }
+    }
+#pragma unroll
+    for (int d = 0; d < kDepth; ++d) cmax = max(cmax, acc_vec<GT>((d & 1) ? acc2 : acc, w[d]));
+    // fold the second chain in: float-float sum of the two, lane-wise
+    const f2_t s = add2(acc.hi, acc2.hi);
+    const f2_t bb = sub2(s, acc.hi);
+    const f2_t aa = sub2(s, bb);
+    const f2_t e = add2(sub2(acc.hi, aa), sub2(acc2.hi, bb));
+    acc.lo = add2(add2(acc.lo, acc2.lo), e);
+    acc.hi = s;
+  }
+  for (; left > 0; --left, q += kStep) cmax = max(cmax, acc_vec<GT>(acc, ld_nc_u4(q)));
+  const bool owns_tail = rem > 0 && (nvec % 32) == lane;
+  if (owns_tail) {
+    uint32_t wv[4] = {0u, 0u, 0u, 0u};
+    for (int j = 0; j < rem; ++j) {
+      const uint32_t bits = f2u(T::elem(g, (int64_t)nvec * V + j));
+      if (GT == OPT_BF16) wv[j >> 1] |= (bits >> 16) << (16 * (j & 1));
+      else                wv[j] = bits;
+    }
+    cmax = max(cmax, acc_vec<GT>(acc, make_uint4(wv[0], wv[1], wv[2], wv[3])));
+  }
+  const bool fast = cmax <= T::kHi && (cmax >= T::kLo || cmax == 0u);
+  if (__all_sync(0xFFFFFFFFu, fast)) {
+    float H = 0.0f, L = 0.0f, hx, hy, lx, ly;
+    unpk(acc.hi, hx, hy);
+    unpk(acc.lo, lx, ly);
+    ff_merge(H, L, hx, lx);
+    ff_merge(H, L, hy, ly);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float H2 = __shfl_xor_sync(0xFFFFFFFFu, H, o), L2 = __shfl_xor_sync(0xFFFFFFFFu, L, o);
+      ff_merge(H, L, H2, L2);
+    }
+    const uint32_t wmax = __reduce_max_sync(0xFFFFFFFFu, cmax);
+    if (lane == 0 && wmax) atomicMax(s_max, GT == OPT_BF16 ? (wmax << 16) : wmax);
+    return (double)H + (double)L;      // lane 0's is the one kept
+  }
+  // the exact slow path, out of the fast path's registers
+  double ds = 0.0;
+  unsigned long long nn = 0, ni = 0;
+  uint32_t mb = 0;
+  auto visit = [&](float x) {
+    if (x != x) { ++nn; return; }
+    if (fabsf(x) == __int_as_float(0x7F800000)) { ++ni; return; }
+    ds += (double)x * (double)x;
+    mb = max(mb, f2u(fabsf(x)));
+  };
+  for (int vv = lane; vv < nvec; vv += 32)
+    for (int j = 0; j < V; ++j) visit(T::elem(g, (int64_t)vv * V + j));
+  if (owns_tail)
+    for (int j = 0; j < rem; ++j) visit(T::elem(g, (int64_t)nvec * V + j));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ds += __shfl_xor_sync(0xFFFFFFFFu, ds, o);
+    nn += __shfl_xor_sync(0xFFFFFFFFu, nn, o);
+    ni += __shfl_xor_sync(0xFFFFFFFFu, ni, o);
+    mb = max(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, o));
+  }
+  if (lane == 0) {
+    if (nn) atomicAdd(s_nan, nn);
+    if (ni) atomicAdd(s_inf, ni);
+    if (mb) atomicMax(s_max, mb);
+  }
+  return ds;
+}
+
+template <int GT>
+__global__ void __launch_bounds__(kNormThreads, 1)
+norm_partials_kernel(const NormChunk* __restrict__ chunks, int64_t cbegin, int64_t cend,
+                     NormSlot* __restrict__ slots, NormFinish fin) {
+  __shared__ double s_part[OPT_NORM_MAX_PART];   // each chunk's sum, in chunk order
+  __shared__ int s_next;                         // the next chunk to take
+  __shared__ unsigned int s_max;                 // max |g|, fp32 bits (integer max: any order)
+  __shared__ unsigned long long s_nan, s_inf;    // counts (integer sums: any order)
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int slot = blockIdx.x;
-
-  __shared__ SlowAcc s_slow[kNormThreads];
-  s_slow[tid] = SlowAcc{0.0, 0ull, 0ull, 0u, 0u};
-  float AH = 0.0f, AL = 0.0f;      // fast-path float-float accumulator
-  uint32_t mxbits = 0;             // fast-path max |g|, fp32 bits
-
-  // The slot's chunks are c = cbegin + slot + k * OPT_NORM_SLOTS.  A table
-  // entry holds the chunk's resolved address, so a chunk starts after one
-  // 16-byte load.
-  for (int64_t c = cbegin + slot; c < cend; c += OPT_NORM_SLOTS) {
-    const NormChunk cur = chunks[c];
-    const char* g = static_cast<const char*>(cur.ptr);
-    const int nvec = (int)(cur.len / V);
-    const int rem = (int)(cur.len % V);
-
-    FF2 acc = {0ull, 0ull};
-    uint32_t cmax = 0;
-    // this thread's vectors tid, tid + T, ...: kDepth 16-byte loads in
-    // flight, rotating -- each register is refilled with the vector kDepth
-    // ahead as soon as it has been used -- and two summation chains
-    int left = nvec > tid ? (nvec - tid + kNormThreads - 1) / kNormThreads : 0;
-    const char* q = g + tid * 16;
-    constexpr int kStep = kNormThreads * 16;
-    if (left >= kDepth) {
-      uint4 w[kDepth];
-      FF2 acc2 = {0ull, 0ull};     // a second chain: odd vectors of a round
-#pragma unroll
-      for (int d = 0; d < kDepth; ++d) w[d] = ld_nc_u4(q + d * kStep);
-      q += kDepth * kStep;
-      for (left -= kDepth; left >= kDepth; left -= kDepth, q += kDepth * kStep) {
-#pragma unroll
-        for (int d = 0; d < kDepth; ++d) {
-          cmax = max(cmax, acc_vec<GT>((d & 1) ? acc2 : acc, w[d]));
-          w[d] = ld_nc_u4(q + d * kStep);
-        }
-      }
-#pragma unroll
-      for (int d = 0; d < kDepth; ++d) cmax = max(cmax, acc_vec<GT>((d & 1) ? acc2 : acc, w[d]));
-      // fold the second chain in: float-float sum of the two, lane-wise
-      const f2_t s = add2(acc.hi, acc2.hi);
-      const f2_t bb = sub2(s, acc.hi);
-      const f2_t aa = sub2(s, bb);
-      const f2_t e = add2(sub2(acc.hi, aa), sub2(acc2.hi, bb));
-      acc.lo = add2(add2(acc.lo, acc2.lo), e);
-      acc.hi = s;
-    }
-    for (; left > 0; --left, q += kStep) cmax = max(cmax, acc_vec<GT>(acc, ld_nc_u4(q)));
-    // ragged tail: the thread that would own vector nvec loads it element-wise
-    const bool owns_tail = rem > 0 && (nvec % kNormThreads) == tid;
-    if (owns_tail) {
-      uint32_t wv[4] = {0u, 0u, 0u, 0u};
-      for (int j = 0; j < rem; ++j) {
-        const uint32_t bits = f2u(T::elem(g, (int64_t)nvec * V + j));
-        if (GT == OPT_BF16) wv[j >> 1] |= (bits >> 16) << (16 * (j & 1));
-        else                wv[j] = bits;
-      }
-      cmax = max(cmax, acc_vec<GT>(acc, make_uint4(wv[0], wv[1], wv[2], wv[3])));
-    }
-
-    const bool fast = cmax <= T::kHi && (cmax >= T::kLo || cmax == 0u);
-    if (fast) {
-      float hx, hy, lx, ly;
-      unpk(acc.hi, hx, hy);
-      unpk(acc.lo, lx, ly);
-      ff_merge(AH, AL, hx, lx);
-      ff_merge(AH, AL, hy, ly);
-      mxbits = max(mxbits, GT == OPT_BF16 ? (cmax << 16) : cmax);
-    } else {
-      slow_chunk<GT>(g, nvec, rem, tid, owns_tail, s_slow[tid]);
-    }
-  }
-
-  // fixed-order CTA reduction in double
-  __shared__ double s_sum[kNormThreads];
-  __shared__ unsigned long long s_nan[kNormThreads], s_inf[kNormThreads];
-  __shared__ uint32_t s_max[kNormThreads];
-  const SlowAcc slow = s_slow[tid];
-  s_sum[tid] = ((double)AH + (double)AL) + slow.sum;
-  s_nan[tid] = slow.nans;
-  s_inf[tid] = slow.infs;
-  s_max[tid] = max(mxbits, slow.mxbits);
-  __syncthreads();
-  for (int w = kNormThreads / 2; w > 0; w >>= 1) {
-    if (tid < w) {
-      s_sum[tid] += s_sum[tid + w];
-      s_nan[tid] += s_nan[tid + w];
-      s_inf[tid] += s_inf[tid + w];
-      s_max[tid] = max(s_max[tid], s_max[tid + w]);
-    }
-    __syncthreads();
-  }
-  __shared__ unsigned int s_ticket;
+  // the slot's chunks: cbegin + slot + j * OPT_NORM_SLOTS, j < nj (at most
+  // OPT_NORM_MAX_PART by the table's chunk size; a slot with more would be
+  // a broken table: it reads nothing and reports a NaN, so that a step given
+  // this norm is skipped)
+  const int64_t first = cbegin + slot;
+  const int64_t nj64 = first < cend ? (cend - 1 - first) / OPT_NORM_SLOTS + 1 : 0;
+  const bool broken = nj64 > OPT_NORM_MAX_PART;
+  const int nj = broken ? 0 : (int)nj64;
   if (tid == 0) {
+    s_next = 0;
+    s_max = 0u;
+    s_nan = broken ? 1ull : 0ull;
+    s_inf = 0ull;
+  }
+  __syncthreads();
+
+  // Each warp takes a chunk, and takes the next one (and requests its table
+  // entry) before it reads the current one, so that the entry's latency
+  // hides behind the chunk.
+  int j = 0;
+  if (lane == 0) j = atomicAdd(&s_next, 1);
+  j = __shfl_sync(0xFFFFFFFFu, j, 0);
+  NormChunk cur = {nullptr, 0u, 0u};
+  if (j < nj) cur = chunks[first + (int64_t)j * OPT_NORM_SLOTS];
+  while (j < nj) {
+    int jn = 0;
+    if (lane == 0) jn = atomicAdd(&s_next, 1);
+    jn = __shfl_sync(0xFFFFFFFFu, jn, 0);
+    NormChunk nxt = {nullptr, 0u, 0u};
+    if (jn < nj) nxt = chunks[first + (int64_t)jn * OPT_NORM_SLOTS];
+    const double part = chunk_sum<GT>(static_cast<const char*>(cur.ptr), cur.len, lane, &s_max, &s_nan, &s_inf);
+    if (lane == 0) s_part[j] = part;
+    j = jn;
+    cur = nxt;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+
+  // warp 0: the slot's total, its chunks' sums in chunk order (lane l:
+  // chunks l, l + 32, ...; then a butterfly), published with a ticket
+  double sum = 0.0;
+  for (int k = lane; k < nj; k += 32) sum += s_part[k];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+  unsigned int ticket = 0;
+  if (lane == 0) {
     NormSlot r;
-    r.sum = s_sum[0];
-    r.nan_count = s_nan[0];
-    r.inf_count = s_inf[0];
-    r.maxabs = u2f(s_max[0]);
+    r.sum = sum;
+    r.nan_count = s_nan;
+    r.inf_count = s_inf;
+    r.maxabs = u2f(s_max);
     r.pad = 0;
     slots[slot] = r;
     __threadfence();                         // the slot is visible before the ticket
-    s_ticket = atomicAdd(fin.done, 1u);
+    ticket = atomicAdd(fin.done, 1u);
   }
-  __syncthreads();
-  if (s_ticket != fin.n_ctas - 1) return;
+  ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
+  if (ticket != fin.n_ctas - 1) return;
   __threadfence();                           // every other CTA's slot is visible now
   finish_slots(fin.all, fin.n_all, fin.max_norm, fin.out);
-  if (tid == 0) *fin.done = 0u;
+  if (lane == 0) *fin.done = 0u;
 }
 
 // The finish alone, for a norm over no elements (no pass-1 launch).
-__global__ void __launch_bounds__(kNormThreads)
+__global__ void __launch_bounds__(32)
 norm_finalize_kernel(const NormSlot* __restrict__ slots, int n, double max_norm,
                      opt_norm_result* __restrict__ out) {
   finish_slots(slots, n, max_norm, out);
@@ -391,7 +392,7 @@ cudaError_t launch_norm(const NormChunk* chunks, const int64_t bucket_begin[3], 
   for (int b = 0; b < 2; ++b)
     if (bucket_begin[b + 1] > bucket_begin[b]) used[nb++] = b;
   if (nb == 0) {
-    norm_finalize_kernel<<<1, kNormThreads, 0, s>>>(slots, 0, max_norm, out);
+    norm_finalize_kernel<<<1, 32, 0, s>>>(slots, 0, max_norm, out);
     return cudaGetLastError();
   }
   NormFinish fin;

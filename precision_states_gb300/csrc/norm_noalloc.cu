@@ -15,9 +15,10 @@
 // call on each device looks the address up with cudaGetSymbolAddress, with
 // that device current, and caches it.  Each call then copies the caller's
 // host arrays into the array (cudaMemcpyAsync, no staging buffer of ours),
-// builds the chunk table on the device in the same order opt_plan_create
-// builds it on the host, and runs the same norm kernels as opt_grad_norm --
-// so the result is the same, bit for bit.
+// builds the chunk table on the device in the same order and with the same
+// chunk sizes (chosen on the host from the sizes, as opt_chunk_table does)
+// as opt_plan_create builds it on the host, and runs the same norm kernels
+// as opt_grad_norm -- so the result is the same, bit for bit.
 //
 // Every call shares the array and overwrites the parts it reads before
 // reading them -- all but the norm's completion counter, which the
@@ -51,7 +52,7 @@ constexpr int64_t kOffSlots = align256(kOffChunks + 16 * kMaxChunks);      // No
 constexpr int64_t kOffDone = align256(kOffSlots + 32 * 2 * OPT_NORM_SLOTS);    // uint32: completion counter
 constexpr int64_t kScratchBytes = align256(kOffDone + 4);
 
-static_assert(kScratchBytes == 4515072, "scratch size stated in opt.h");
+static_assert(kScratchBytes == 4466432, "scratch size stated in opt.h");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 // Device address of g_noalloc_scratch per device, looked up once per device.
@@ -72,11 +73,12 @@ cudaError_t scratch_address(int device, unsigned char** out) {
   return cudaSuccess;
 }
 
-// One CTA: per-tensor chunk counts, a stable bucket-major order (FP32
-// gradients first, then BF16, list order within a bucket), and each
-// tensor's first chunk in that order.
+// One CTA: per-tensor chunk counts (chunks of ce0 elements in the FP32
+// bucket, ce1 in the BF16 one), a stable bucket-major order (FP32 gradients
+// first, then BF16, list order within a bucket), and each tensor's first
+// chunk in that order.
 __global__ void __launch_bounds__(kPrepThreads)
-noalloc_prep_kernel(unsigned char* scratch, int n) {
+noalloc_prep_kernel(unsigned char* scratch, int n, int64_t ce0, int64_t ce1) {
   const int64_t* numel = reinterpret_cast<const int64_t*>(scratch + kOffNumel);
   const int32_t* dtype = reinterpret_cast<const int32_t*>(scratch + kOffDtype);
   int32_t* order = reinterpret_cast<int32_t*>(scratch + kOffOrder);
@@ -92,7 +94,8 @@ noalloc_prep_kernel(unsigned char* scratch, int n) {
     const int t = t0 + k;
     if (t >= n) break;
     const int b = dtype[t] == OPT_BF16 ? 1 : 0;
-    ch[b] += (numel[t] + OPT_CHUNK_ELEMS - 1) / OPT_CHUNK_ELEMS;
+    const int64_t ce = b ? ce1 : ce0;
+    ch[b] += (numel[t] + ce - 1) / ce;
     cnt[b] += 1;
   }
   s_chunks[0][tid] = ch[0]; s_chunks[1][tid] = ch[1];
@@ -119,17 +122,18 @@ noalloc_prep_kernel(unsigned char* scratch, int n) {
     const int t = t0 + k;
     if (t >= n) break;
     const int b = dtype[t] == OPT_BF16 ? 1 : 0;
+    const int64_t ce = b ? ce1 : ce0;
     order[pos[b]] = t;
     base[pos[b]] = next[b];
     pos[b] += 1;
-    next[b] += (numel[t] + OPT_CHUNK_ELEMS - 1) / OPT_CHUNK_ELEMS;
+    next[b] += (numel[t] + ce - 1) / ce;
   }
 }
 
 // One thread per chunk: find its tensor (last position whose first chunk is
 // <= c, by binary search over the bucket-major order) and write the entry
 // with the chunk's first gradient element resolved.
-__global__ void noalloc_fill_kernel(unsigned char* scratch, int n, int64_t total) {
+__global__ void noalloc_fill_kernel(unsigned char* scratch, int n, int64_t total, int64_t ce0, int64_t ce1) {
   const void* const* grad = reinterpret_cast<const void* const*>(scratch + kOffGrad);
   const int64_t* numel = reinterpret_cast<const int64_t*>(scratch + kOffNumel);
   const int32_t* dtype = reinterpret_cast<const int32_t*>(scratch + kOffDtype);
@@ -145,11 +149,12 @@ __global__ void noalloc_fill_kernel(unsigned char* scratch, int n, int64_t total
       else hi = mid;
     }
     const int t = order[lo - 1];
-    const int64_t start = (c - base[lo - 1]) * OPT_CHUNK_ELEMS;
+    const int64_t ce = dtype[t] == OPT_BF16 ? ce1 : ce0;
+    const int64_t start = (c - base[lo - 1]) * ce;
     const int64_t left = numel[t] - start;
     NormChunk e;
     e.ptr = static_cast<const char*>(grad[t]) + start * (dtype[t] == OPT_BF16 ? 2 : 4);
-    e.len = (uint32_t)(left < OPT_CHUNK_ELEMS ? left : OPT_CHUNK_ELEMS);
+    e.len = (uint32_t)(left < ce ? left : ce);
     e.pad = 0;
     chunks[c] = e;
   }
@@ -173,13 +178,21 @@ extern "C" int opt_grad_norm_noalloc(int32_t n, const int64_t* numel, const void
   if ((uintptr_t)d_out & 7u) return OPT_EALIGN;
   if (n > kMaxTensors) return OPT_ELIMIT;
   if (n > 0 && (numel == nullptr || grad == nullptr || grad_dtype == nullptr)) return OPT_EINVAL;
-  int64_t bucket[2] = {0, 0};
   for (int32_t i = 0; i < n; ++i) {
     if (numel[i] < 0) return OPT_EINVAL;
     if (grad_dtype[i] != OPT_F32 && grad_dtype[i] != OPT_BF16) return OPT_EUNSUPPORTED;
     if (numel[i] > 0 && grad[i] == nullptr) return OPT_EINVAL;
     if (grad[i] != nullptr && ((uintptr_t)grad[i] & 15u)) return OPT_EALIGN;
-    bucket[grad_dtype[i] == OPT_BF16 ? 1 : 0] += (numel[i] + OPT_CHUNK_ELEMS - 1) / OPT_CHUNK_ELEMS;
+  }
+  int64_t ce[2];
+  for (int b = 0; b < 2; ++b) {
+    ce[b] = norm_chunk_elems(n, numel, grad_dtype, b);
+    if (ce[b] < 0) return (int)ce[b];
+  }
+  int64_t bucket[2] = {0, 0};
+  for (int32_t i = 0; i < n; ++i) {
+    const int b = grad_dtype[i] == OPT_BF16 ? 1 : 0;
+    bucket[b] += (numel[i] + ce[b] - 1) / ce[b];
     if (bucket[0] + bucket[1] > kMaxChunks) return OPT_ELIMIT;
   }
   const int64_t total = bucket[0] + bucket[1];
@@ -199,10 +212,10 @@ extern "C" int opt_grad_norm_noalloc(int32_t n, const int64_t* numel, const void
       e = cudaMemcpyAsync(scratch + kOffDtype, grad_dtype, sizeof(int32_t) * (size_t)n, cudaMemcpyHostToDevice,
                           s);
     if (e != cudaSuccess) return cuda_status(e);
-    noalloc_prep_kernel<<<1, kPrepThreads, 0, s>>>(scratch, n);
+    noalloc_prep_kernel<<<1, kPrepThreads, 0, s>>>(scratch, n, ce[0], ce[1]);
     if (total > 0) {
       const int64_t want = (total + 255) / 256;
-      noalloc_fill_kernel<<<(int)(want < 1024 ? want : 1024), 256, 0, s>>>(scratch, n, total);
+      noalloc_fill_kernel<<<(int)(want < 1024 ? want : 1024), 256, 0, s>>>(scratch, n, total, ce[0], ce[1]);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_status(e);

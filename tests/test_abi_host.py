@@ -41,7 +41,7 @@ def test_exports_via_nm():
 
 
 def test_version_and_strerror():
-    assert ps.opt_version() == 1
+    assert ps.opt_version() == 2
     for code in (0, 1, -1, -2, -3, -4, -5, 99):
         assert isinstance(ps.opt_strerror(code), str) and ps.opt_strerror(code)
 
@@ -59,24 +59,54 @@ def test_chunk_table_covers_each_tensor_once(seed):
     numel = [int(x) for x in rng.choice([0, 1, 7, 32767, 32768, 32769, 100000, 262144 + 5], 40)]
     gd = [int(x) for x in rng.choice([ps.OPT_F32, ps.OPT_BF16], 40)]
     table, bb = ps.opt_chunk_table(numel, gd)
-    CH = ps.OPT_CHUNK_ELEMS
+    ch = [ps.opt_norm_chunk_elems(numel, gd, b) for b in (0, 1)]
+    assert ch == [ps.OPT_NORM_CHUNK_MIN] * 2          # small buckets: the smallest chunks
+    CH = {ps.OPT_F32: ch[0], ps.OPT_BF16: ch[1]}
     assert bb[0] == 0 and bb[2] == len(table)
-    assert len(table) == sum((n + CH - 1) // CH for n in numel)
+    assert len(table) == sum((n + CH[d] - 1) // CH[d] for n, d in zip(numel, gd))
     for k, (t, ln, start) in enumerate(table):
         bucket = 0 if k < bb[1] else 1
         assert gd[t] == (ps.OPT_F32 if bucket == 0 else ps.OPT_BF16)
-        assert 1 <= ln <= CH and start % CH == 0 and start + ln <= numel[t]
+        c = CH[gd[t]]
+        assert 1 <= ln <= c and start % c == 0 and start + ln <= numel[t]
     covered = {}
     for t, ln, start in table:
         covered.setdefault(t, []).append((start, ln))
     for t, n in enumerate(numel):
         segs = covered.get(t, [])
-        assert [s for s, _ in segs] == list(range(0, n, CH))       # in element order
+        assert [s for s, _ in segs] == list(range(0, n, CH[gd[t]]))       # in element order
         assert sum(ln for _, ln in segs) == n
     # tensors appear in list order within a bucket
     for lo, hi in ((0, bb[1]), (bb[1], bb[2])):
         ts = [table[k][0] for k in range(lo, hi)]
         assert ts == sorted(ts)
+
+
+def test_norm_chunk_size_rule():
+    """The norm's chunk size comes from a bucket's size alone: 8K elements
+    below 2^29, 16K below 2^31, 32K above, doubled while a slot would own
+    more than OPT_NORM_MAX_PART chunks; the other bucket does not matter."""
+    f = ps.opt_norm_chunk_elems
+    B, F = ps.OPT_BF16, ps.OPT_F32
+    assert f([], [], 0) == f([], [], 1) == ps.OPT_NORM_CHUNK_MIN
+    assert f([(1 << 29) - 1], [B], 1) == 8192
+    assert f([1 << 29], [B], 1) == 16384
+    assert f([(1 << 31) - 1], [B], 1) == 16384
+    assert f([1 << 31], [B], 1) == 32768
+    assert f([8_030_261_248], [B], 1) == 32768             # the Llama-3-8B list's size
+    assert f([1 << 31, 5], [F, B], 1) == 8192              # buckets apart
+    assert f([1 << 31, 5], [F, B], 0) == 32768
+    # 32K chunks would give a slot more than OPT_NORM_MAX_PART: doubled
+    lim = ps.OPT_NORM_SLOTS * ps.OPT_NORM_MAX_PART * 32768
+    assert f([lim], [B], 1) == 32768
+    assert f([lim + 1], [B], 1) == 65536
+    # tensors beyond what the slots can hold, one chunk each at least
+    many = ps.OPT_NORM_SLOTS * ps.OPT_NORM_MAX_PART + 1
+    with pytest.raises(ps.OptError) as e:
+        f([1] * many, [B] * many, 1)
+    assert e.value.status == ps.OPT_ELIMIT
+    with pytest.raises(ps.OptError):
+        f([5], [B], 2)
 
 
 def test_chunk_table_errors():
