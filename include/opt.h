@@ -201,7 +201,10 @@ const char* opt_strerror(int status);  /* static string, never NULL */
 
 /* Validate `list`, build the chunk table (host, from sizes only), allocate
  * the workspace on the current device and upload the tables (synchronous).
- * On success *out owns the plan; destroy it with opt_plan_destroy. */
+ * On success *out owns the plan; destroy it with opt_plan_destroy.  Returns
+ * OPT_ELIMIT for a gradient-dtype bucket of more than
+ * OPT_NORM_SLOTS * OPT_NORM_MAX_PART (622,592) tensors, whose chunks the
+ * norm's slots cannot hold (see OPT_NORM_CHUNK_MIN). */
 int opt_plan_create(const opt_tensor_list* list, opt_plan** out);
 void opt_plan_destroy(opt_plan* plan);   /* NULL is a no-op; synchronises the device */
 /* Plan facts: chunks, elements, device workspace bytes (any may be NULL). */

@@ -190,7 +190,7 @@ def _noalloc_norm(grads, max_norm, d_out):
     return ps.opt_norm_result.from_buffer_copy(bytes(d_out.cpu().numpy()))
 
 
-@pytest.mark.parametrize("name", ["clip_740", "llama3_8b", "mixed"])
+@pytest.mark.parametrize("name", ["clip_740", "llama3_8b", "mixed", "mid"])
 def test_norm_counts_every_element_once(name):
     """Every gradient element enters the norm exactly once, over whole lists:
     with BF16 gradients all 1 and FP32 gradients all 2, the sum of squares is
@@ -201,6 +201,10 @@ def test_norm_counts_every_element_once(name):
     if name == "mixed":
         sizes = [32768 * 3 + 5, 1, 70001, 32768, 32767, 4097, 0, 9]
         dts = [torch.bfloat16 if i % 2 == 0 else torch.float32 for i in range(len(sizes))]
+    elif name == "mid":      # a BF16 bucket of 2^29 elements and more: 16K-element chunks
+        sizes = [(1 << 29) - 4099, 12345, 7, 4097]
+        dts = [torch.bfloat16] * len(sizes)
+        assert ps.opt_norm_chunk_elems(sizes, [ps.OPT_BF16] * 4, 1) == 16384
     else:
         w = W.workload(name)
         sizes = w.sizes
@@ -220,3 +224,27 @@ def test_norm_counts_every_element_once(name):
     d_out = torch.zeros(48, dtype=torch.uint8, device="cuda")
     na = _noalloc_norm(grads, 0.0, d_out)
     assert na.sumsq == want and na.norm_inf == got.norm_inf
+
+
+def test_mid_size_chunks_match_the_oracle():
+    """A BF16 bucket just over 2^29 elements takes the middle chunk size
+    (16,384): the norm of seeded values equals the oracle's within 1e-12,
+    repeats bit for bit, and the no-allocation path gives the same bits."""
+    sizes = [(1 << 28) + 3, (1 << 28) + 77, 5]
+    assert ps.opt_norm_chunk_elems(sizes, [ps.OPT_BF16] * 3, 1) == 16384
+    gen = torch.Generator(device="cuda").manual_seed(29)
+    grads = [(torch.randn(n, generator=gen, device="cuda") * s).to(torch.bfloat16)
+             for n, s in zip(sizes, (1e-3, 2.0, 1e4))]
+    plan = plan_for(grads)
+    got = plan.grad_norm(1.0)
+    again = plan.grad_norm(1.0)
+    assert again.as_dict() == got.as_dict()
+    want = oracle_norm_parallel(host(grads), 1.0, 16)
+    assert rel_err(got.norm2, want["norm2"]) <= TOL, (got.norm2, want["norm2"])
+    assert got.norm_inf == want["norm_inf"] and got.clip_coef == want["clip_coef"]
+    plan.close()
+    del plan
+    torch.cuda.empty_cache()
+    d_out = torch.zeros(48, dtype=torch.uint8, device="cuda")
+    na = _noalloc_norm(grads, 1.0, d_out)
+    assert na.sumsq == got.sumsq and na.norm2 == got.norm2 and na.clip_coef == got.clip_coef
