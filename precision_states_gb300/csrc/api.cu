@@ -55,10 +55,7 @@ struct opt_plan {
   // update-norm clipping (LAMB) workspace, allocated on first use
   std::vector<int64_t> tile_first, tile_count;   // per tensor, in the tile table
   void* d_lamb = nullptr;
-  void* d_lamb_sums = nullptr;
-  int64_t* d_tile_first = nullptr;
-  int64_t* d_tile_count = nullptr;
-  float* d_ratio = nullptr;
+  psopt::LambWork lamb{};
 };
 
 namespace psopt {
@@ -394,22 +391,61 @@ int opt_lamb_step(opt_plan* P, const opt_hparams* hp, int64_t step, float max_un
   if (!g.ok) return OPT_ECUDA;
   cudaError_t e = cudaSuccess;
   if (P->d_lamb == nullptr && P->n > 0) {
-    // per tile: two doubles; per tensor: first tile, tile count, ratio
-    const int64_t off_f = align_up(16 * P->n_tiles, 256);
-    const int64_t off_c = align_up(off_f + 8 * (int64_t)P->n, 256);
-    const int64_t off_r = align_up(off_c + 8 * (int64_t)P->n, 256);
+    // segments of at most kLambSegTiles tiles, each tensor at least one
+    std::vector<int32_t> seg_tensor, seg_count, tensor_seg0((size_t)P->n), tensor_nseg((size_t)P->n);
+    std::vector<int64_t> seg_first;
+    for (int32_t t = 0; t < P->n; ++t) {
+      const int64_t first = P->tile_first[(size_t)t], count = P->tile_count[(size_t)t];
+      const int64_t nseg = count > 0 ? (count + kLambSegTiles - 1) / kLambSegTiles : 1;
+      tensor_seg0[(size_t)t] = (int32_t)seg_tensor.size();
+      tensor_nseg[(size_t)t] = (int32_t)nseg;
+      for (int64_t j = 0; j < nseg; ++j) {
+        const int64_t left = count - j * kLambSegTiles;
+        seg_tensor.push_back(t);
+        seg_first.push_back(first + j * kLambSegTiles);
+        seg_count.push_back((int32_t)(left < kLambSegTiles ? (left > 0 ? left : 0) : kLambSegTiles));
+      }
+    }
+    const int64_t ns = (int64_t)seg_tensor.size();
+    // per tile: two doubles; per segment: tensor, first tile, count, two
+    // doubles; per tensor: first segment, segment count, ticket, ratio
+    const int64_t off_st = align_up(16 * P->n_tiles, 256);
+    const int64_t off_sf = align_up(off_st + 4 * ns, 256);
+    const int64_t off_sc = align_up(off_sf + 8 * ns, 256);
+    const int64_t off_ss = align_up(off_sc + 4 * ns, 256);
+    const int64_t off_t0 = align_up(off_ss + 16 * ns, 256);
+    const int64_t off_tn = align_up(off_t0 + 4 * (int64_t)P->n, 256);
+    const int64_t off_tk = align_up(off_tn + 4 * (int64_t)P->n, 256);
+    const int64_t off_r = align_up(off_tk + 4 * (int64_t)P->n, 256);
     const int64_t bytes = align_up(off_r + 4 * (int64_t)P->n, 256);
     e = cudaMalloc(&P->d_lamb, (size_t)bytes);
     if (e != cudaSuccess) { P->d_lamb = nullptr; return cuda_status(e); }
     char* base = static_cast<char*>(P->d_lamb);
-    P->d_lamb_sums = base;
-    P->d_tile_first = reinterpret_cast<int64_t*>(base + off_f);
-    P->d_tile_count = reinterpret_cast<int64_t*>(base + off_c);
-    P->d_ratio = reinterpret_cast<float*>(base + off_r);
-    e = cudaMemcpy(P->d_tile_first, P->tile_first.data(), 8 * (size_t)P->n, cudaMemcpyHostToDevice);
-    if (e == cudaSuccess)
-      e = cudaMemcpy(P->d_tile_count, P->tile_count.data(), 8 * (size_t)P->n, cudaMemcpyHostToDevice);
-    if (e != cudaSuccess) return cuda_status(e);
+    LambWork& w = P->lamb;
+    w.tile_sums = base;
+    w.seg_tensor = reinterpret_cast<const int32_t*>(base + off_st);
+    w.seg_first = reinterpret_cast<const int64_t*>(base + off_sf);
+    w.seg_count = reinterpret_cast<const int32_t*>(base + off_sc);
+    w.seg_sums = base + off_ss;
+    w.tensor_seg0 = reinterpret_cast<const int32_t*>(base + off_t0);
+    w.tensor_nseg = reinterpret_cast<const int32_t*>(base + off_tn);
+    w.tickets = reinterpret_cast<unsigned int*>(base + off_tk);
+    w.ratio = reinterpret_cast<float*>(base + off_r);
+    w.n_segs = (int)ns;
+    auto up = [&](int64_t off, const void* src, size_t n) {
+      return n == 0 ? cudaSuccess : cudaMemcpy(base + off, src, n, cudaMemcpyHostToDevice);
+    };
+    e = cudaMemset(base + off_tk, 0, 4 * (size_t)P->n);
+    if (e == cudaSuccess) e = up(off_st, seg_tensor.data(), 4 * (size_t)ns);
+    if (e == cudaSuccess) e = up(off_sf, seg_first.data(), 8 * (size_t)ns);
+    if (e == cudaSuccess) e = up(off_sc, seg_count.data(), 4 * (size_t)ns);
+    if (e == cudaSuccess) e = up(off_t0, tensor_seg0.data(), 4 * (size_t)P->n);
+    if (e == cudaSuccess) e = up(off_tn, tensor_nseg.data(), 4 * (size_t)P->n);
+    if (e != cudaSuccess) {
+      cudaFree(P->d_lamb);
+      P->d_lamb = nullptr;
+      return cuda_status(e);
+    }
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   for (int phase = 0; phase < 3 && e == cudaSuccess; ++phase) {
@@ -417,8 +453,7 @@ int opt_lamb_step(opt_plan* P, const opt_hparams* hp, int64_t step, float max_un
       if (phase == 1 && b == 1) break;               // the ratios cover every tensor at once
       a.tile_begin = P->tile_begin[b];
       a.tile_end = P->tile_begin[b + 1];
-      e = launch_lamb(b == 0 ? OPT_F32 : OPT_BF16, a, P->d_lamb_sums, P->d_tile_first, P->d_tile_count, P->n,
-                      max_unorm, P->d_ratio, P->sm_count, s, phase);
+      e = launch_lamb(b == 0 ? OPT_F32 : OPT_BF16, a, P->lamb, max_unorm, P->sm_count, s, phase);
     }
   }
   return cuda_status(e);

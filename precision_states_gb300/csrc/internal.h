@@ -84,10 +84,26 @@ cudaError_t launch_step_lowp_states(int grad_dtype, int combo, int stochastic, c
 cudaError_t launch_step_small(int grad_dtype, int combo, int algo, int stochastic, const StepArgs& args,
                               const SmallList& list, cudaStream_t s);
 
-// update-norm clipping (LAMB / max_unorm): phase 0 = per-tile sums (one
-// bucket), 1 = per-tensor ratios (all tensors), 2 = apply (one bucket)
-cudaError_t launch_lamb(int grad_dtype, const StepArgs& args, void* tile_sums, const int64_t* tile_first,
-                        const int64_t* tile_count, int n_tensors, float max_unorm, float* ratio,
+// update-norm clipping (LAMB / max_unorm): the workspace, device pointers.
+// A tensor's tiles are cut into segments of at most kLambSegTiles tiles;
+// each segment's sums are reduced by one CTA of the ratio pass, and the last
+// of a tensor's segments to finish (a per-tensor ticket) sums them in order.
+constexpr int64_t kLambSegTiles = 2048;
+struct LambWork {
+  void* tile_sums;                 // per tile: sums of u^2 and p^2
+  const int32_t* seg_tensor;       // per segment: its tensor
+  const int64_t* seg_first;        // per segment: first tile
+  const int32_t* seg_count;        // per segment: tiles (0 for an empty tensor)
+  void* seg_sums;                  // per segment: sums of u^2 and p^2
+  const int32_t* tensor_seg0;      // per tensor: first segment
+  const int32_t* tensor_nseg;      // per tensor: segments (at least 1)
+  unsigned int* tickets;           // per tensor: 0 between calls
+  float* ratio;                    // per tensor: the trust ratio
+  int n_segs;
+};
+// phase 0 = per-tile sums (one bucket), 1 = per-tensor ratios (all
+// tensors), 2 = apply (one bucket)
+cudaError_t launch_lamb(int grad_dtype, const StepArgs& args, const LambWork& w, float max_unorm,
                         int sm_count, cudaStream_t s, int phase);
 
 // standalone codecs
