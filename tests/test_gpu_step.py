@@ -584,3 +584,24 @@ def test_grads_upload_copies_every_tensor_exactly():
     with pytest.raises(ValueError):
         gpu.plan.grads_upload([host[0].float()] + host[1:])
     gpu.plan.close()
+
+
+@pytest.mark.parametrize("max_unorm", [0.3, 100.0])
+def test_lamb_tensors_over_several_segments_match_oracle(max_unorm):
+    """The ratio pass cuts a tensor's tiles into segments of 2,048 and forms
+    the ratio in the CTA that finishes the tensor's last segment: tensors of
+    4 segments (the last one ragged), of exactly 1, of 2 (the second one
+    tile), and a tiny one give the oracle's ratios and states after 3 steps,
+    and the same bits twice."""
+    seg = 2048 * 2048
+    sizes = [3 * seg + 777, seg, seg + 1, 5]
+    w = W.Workload("lamb_segments", sizes, "bf16", steps=3, max_norm=1.0, p_std=0.02, grad_std=1.0,
+                   hp=dict(lr=1e-2, weight_decay=0.1))
+    gpu, orc, ratios = _lamb_run(w, 9, max_unorm, 3)
+    flat = [r for rs in ratios for r in rs]
+    if max_unorm < 1.0:
+        assert all(r < 1.0 for r in flat)
+    orc.compare(gpu, 1e-5, False)
+    again, _, _ = _lamb_run(w, 9, max_unorm, 3, with_oracle=False)
+    for x, y in zip(gpu.params + gpu.m + gpu.v, again.params + again.m + again.v):
+        assert torch.equal(x, y)
