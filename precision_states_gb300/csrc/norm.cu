@@ -4,20 +4,23 @@
 // "perf(training): fused multi-tensor gradient-norm reduction" (NeMo
 // Automodel PR #3685), 'Correctness properties': values are widened in
 // registers (never squared in BF16), the decomposition into chunks comes from
-// sizes only and there are no atomics, so the norm is bit-identical run to
-// run; NaNs are counted because a max that ignores NaN would hide them.
+// sizes only and no floating-point value is accumulated in arrival order, so
+// the norm is bit-identical run to run; NaNs are counted because a max that
+// ignores NaN would hide them.  (The only atomics are on integers -- which
+// warp takes a chunk, the max of |g| as bits, the NaN and Inf counts, the
+// completion ticket -- none of which changes a bit of the result.)
 //
 // GB300 design.  Blackwell Ultra's FP64 rate is a small fraction of its FP32
 // rate, so one fp64 operation per element would make this streaming pass
-// compute-bound.  Instead each thread accumulates squares in error-free
+// compute-bound.  Instead each lane accumulates squares in error-free
 // float-float form (Knuth's TwoSum, exact; BF16 squares are exact in fp32 and
-// FP32 squares are split exactly with an FMA), two lanes at a time with the
-// packed f32x2 instructions.  The per-chunk float-float sums are merged into
-// a per-thread float-float accumulator, converted to double once per thread,
-// and reduced across the CTA in double in a fixed tree.  Only a thread whose
-// elements in a chunk hold a NaN, an Inf, or a magnitude outside
-// [2^-40, 2^40] (where fp32 squares could overflow or lose bits) re-reads
-// those elements and accumulates them in double -- a rare, exact slow path.
+// FP32 squares are split exactly with an FMA), two values at a time with the
+// packed f32x2 instructions.  A chunk is read by one warp; its lanes'
+// float-float sums are merged in a fixed shuffle tree and converted to
+// double once per chunk.  A chunk in which any lane's elements hold a NaN,
+// an Inf, or a magnitude outside [2^-40, 2^40] (where fp32 squares could
+// overflow or lose bits) is read again by the whole warp and summed in
+// double -- a rare, exact slow path.
 //
 // Pass 1 runs OPT_NORM_SLOTS CTAs per dtype bucket, one per SM of a GB300,
 // each of 24 warps.  Slot s owns chunks s, s + OPT_NORM_SLOTS, ... of the
