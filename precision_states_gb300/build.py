@@ -37,8 +37,8 @@ def _nvcc() -> str:
 
 
 # the sources that make up the fused step kernel (for the profile stamp)
-STEP_KERNEL_SOURCES = ["step_kernel.cuh", "common.cuh", "internal.h", "step_f32.cu", "step_lowp.cu",
-                       "../../include/opt.h"]
+STEP_KERNEL_SOURCES = ["step_kernel.cuh", "step_dyn.cuh", "common.cuh", "internal.h", "step_f32.cu",
+                       "step_lowp.cu", "../../include/opt.h"]
 
 
 def source_stamp(files) -> str:

@@ -52,6 +52,7 @@ struct opt_plan {
   unsigned int* d_done = nullptr;          // the norm's completion counter
   int64_t* d_step = nullptr;               // device step counter (last step taken)
   opt_step_scalars* d_sc = nullptr;        // its step's scalars
+  unsigned long long* d_dyn = nullptr;     // the warp-dynamic step's counters (0 between launches)
   // update-norm clipping (LAMB) workspace, allocated on first use
   std::vector<int64_t> tile_first, tile_count;   // per tensor, in the tile table
   void* d_lamb = nullptr;
@@ -243,7 +244,8 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
   const int64_t off_d = off_e + 8;
   const int64_t off_k = align_up(off_d + 8, 16);
   const int64_t off_q = off_k + 16;
-  P->d_bytes = align_up(off_q + (int64_t)sizeof(opt_step_scalars), 256);
+  const int64_t off_y = align_up(off_q + (int64_t)sizeof(opt_step_scalars), 16);
+  P->d_bytes = align_up(off_y + 16, 256);
   cudaError_t e = cudaMalloc(&P->d_mem, (size_t)P->d_bytes);
   if (e != cudaSuccess) { delete P; return cuda_status(e); }
   char* base = static_cast<char*>(P->d_mem);
@@ -257,6 +259,7 @@ int opt_plan_create(const opt_tensor_list* L, opt_plan** out) {
   P->d_done = reinterpret_cast<unsigned int*>(base + off_d);
   P->d_step = reinterpret_cast<int64_t*>(base + off_k);
   P->d_sc = reinterpret_cast<opt_step_scalars*>(base + off_q);
+  P->d_dyn = reinterpret_cast<unsigned long long*>(base + off_y);
 
   e = cudaMemset(P->d_mem, 0, (size_t)P->d_bytes);
   if (e == cudaSuccess && L->n > 0)
@@ -351,6 +354,7 @@ static int do_step(opt_plan* P, const opt_hparams* hp, int64_t step, const opt_n
   a.err = P->d_err;
   a.wait_ns = P->wait_ns;
   a.drill = drill ? 1 : 0;
+  a.dyn = P->d_dyn;
 
   DeviceGuard g(P->device);
   if (!g.ok) return OPT_ECUDA;

@@ -65,6 +65,8 @@ struct StepArgs {
   const opt_step_scalars* d_sc;       // non-NULL: use these scalars (device memory), not sc
   unsigned long long wait_ns;         // limit of each wait of the staged step (opt_plan_set_wait_limit)
   int drill;                          // nonzero: the staged step's waits run out on purpose
+  unsigned long long* dyn;            // the FP32 AdamW step's tile counter and finished-warp count
+                                      // (0 between launches: the last warp resets them)
 };
 
 // A short bucket passed whole in a kernel's parameters (the short-list step,

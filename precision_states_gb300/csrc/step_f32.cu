@@ -1,5 +1,6 @@
 // step_f32.cu -- fused step instantiations with FP32 m, v (and m2), and the
 // device step counter that lets a captured CUDA graph replay the step.
+#include "step_dyn.cuh"
 #include "step_kernel.cuh"
 
 namespace psopt {
@@ -27,8 +28,13 @@ __global__ void set_step_kernel(int64_t* counter, int64_t value) {
 
 template <int GT, int ALGO>
 cudaError_t launch_f32(const StepArgs& a, int sm_count, cudaStream_t s) {
-  if (a.d_sc != nullptr) return launch_one<GT, SC_F32, ALGO, false, true>(a, sm_count, s);
-  return launch_one<GT, SC_F32, ALGO, false>(a, sm_count, s);
+  if constexpr (ALGO == ALGO_ADAMW) {
+    if (a.d_sc != nullptr) return launch_dyn<GT, true>(a, sm_count, s);
+    return launch_dyn<GT, false>(a, sm_count, s);
+  } else {
+    if (a.d_sc != nullptr) return launch_one<GT, SC_F32, ALGO, false, true>(a, sm_count, s);
+    return launch_one<GT, SC_F32, ALGO, false>(a, sm_count, s);
+  }
 }
 
 }  // namespace
