@@ -220,6 +220,27 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def step_kernel_name(w, rounding: str) -> str:
+    """The step's kernel as the library dispatches it (the roofline's label
+    and the key of its traffic record): LAMB's three passes; the short-list
+    kernel for at most 8 tensors and 4,096 tiles of 2,048 elements; the
+    warp-dynamic kernel for FP32-state AdamW; the staged kernel for
+    low-precision states with stochastic rounding and for BF16 v; else the
+    register-pipelined kernel."""
+    args = f"{w.grad_dtype} grads, {w.m_dtype} m, {w.v_dtype} v, {w.algo}, {rounding}"
+    nonempty = [n for n in w.sizes if n > 0]
+    tiles = sum((n + 2047) // 2048 for n in nonempty)
+    if w.algo == "lamb":
+        return f"lamb_stats_kernel + lamb_ratio_kernel + lamb_apply_kernel<{args}>"
+    if len(nonempty) <= 8 and tiles <= 4096:
+        return f"step_small_kernel<{args}>"
+    if w.m_dtype == "f32" and w.algo == "adamw":
+        return f"step_dyn_kernel<{args}>"
+    if w.m_dtype != "f32" and w.algo == "adamw" and (rounding == "stochastic" or w.v_dtype == "bf16"):
+        return f"step_bulk_kernel<{args}>"
+    return f"step_kernel<{args}>"
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -665,7 +686,7 @@ def run_ours(args, rank, local_rank, world):
     step_avg = sum(step_ms) / len(step_ms)
     norm_avg = sum(norm_ms) / len(norm_ms)
     achieved = step_bytes / (step_avg / 1e3) / 1e9
-    kname = f"step_kernel<{w.grad_dtype} grads, {w.m_dtype} m, {w.v_dtype} v, {w.algo}, {args.rounding}>"
+    kname = step_kernel_name(w, args.rounding)
     roofline = {"bound": "hbm", "kernel": kname,
                 "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic_for(kname, params_per_step),
