@@ -28,13 +28,8 @@ __global__ void set_step_kernel(int64_t* counter, int64_t value) {
 
 template <int GT, int ALGO>
 cudaError_t launch_f32(const StepArgs& a, int sm_count, cudaStream_t s) {
-  if constexpr (ALGO == ALGO_ADAMW) {
-    if (a.d_sc != nullptr) return launch_dyn<GT, true>(a, sm_count, s);
-    return launch_dyn<GT, false>(a, sm_count, s);
-  } else {
-    if (a.d_sc != nullptr) return launch_one<GT, SC_F32, ALGO, false, true>(a, sm_count, s);
-    return launch_one<GT, SC_F32, ALGO, false>(a, sm_count, s);
-  }
+  if (a.d_sc != nullptr) return launch_dyn<GT, SC_F32, ALGO, false, true>(a, sm_count, s);
+  return launch_dyn<GT, SC_F32, ALGO, false, false>(a, sm_count, s);
 }
 
 }  // namespace
