@@ -391,6 +391,7 @@ int opt_lamb_step(opt_plan* P, const opt_hparams* hp, int64_t step, float max_un
   a.tiles = P->d_tiles;
   a.d_norm = d_norm;
   a.err = P->d_err;
+  a.dyn = P->d_dyn;
   DeviceGuard g(P->device);
   if (!g.ok) return OPT_ECUDA;
   cudaError_t e = cudaSuccess;

@@ -21,6 +21,7 @@
 //     (the same operations, so the same bits), p <- p (1 - lr wd) - lr ratio u.
 // Traffic: pass 1 reads p, g, m, v and writes m, v; pass 3 reads p, m, v and
 // writes p: 38 B per parameter with BF16 gradients.
+#include "step_dyn.cuh"
 #include "step_kernel.cuh"
 
 namespace psopt {
@@ -40,6 +41,43 @@ __device__ __forceinline__ float lamb_dir(float mn, float vn, const opt_step_sca
   return div_approx(num, den);
 }
 
+// The streaming passes take their tiles as warps free up: a warp takes whole
+// tiles from the plan's counter (one atomic per tile, a tile ahead) and
+// covers each in passes of 256 elements, lane l taking elements
+// base + 8 l .. + 7 of each pass.  body(td, e0, cnt) works on the lane's
+// group (cnt <= 0: none in this pass); tile_done(i) runs, warp-wide, after
+// tile i's last pass, so pass 1 reduces each tile within one warp and needs
+// no CTA barrier.  Measured on GB300 against fixed shares per CTA (pass 1
+// with one CTA barrier per tile), A/B/A/B: the LAMB step on the Llama-3-8B
+// list went from 45.40 to 42.40 ms (1.003 -> 1.074 of the measured copy
+// bandwidth), on the 740-tensor list from 1.028 to 1.022.
+template <typename Body, typename TileDone>
+__device__ __forceinline__ void warp_tiles(const StepArgs& a, int lane, Body body, TileDone tile_done) {
+  const int64_t n = a.tile_end - a.tile_begin;
+  unsigned long long* ctr = a.dyn;
+  int64_t u = dyn_take(ctr, lane);
+  if (u < n) {
+    opt_chunk tl = a.tiles[a.tile_begin + u];
+    int64_t un = dyn_take(ctr, lane);
+    opt_chunk tln{};
+    if (un < n) tln = a.tiles[a.tile_begin + un];
+    for (;;) {
+      const TensorDesc td = a.tensors[tl.tensor];
+      for (int base = 0; base < (int)tl.len; base += 256) {
+        const int o = base + lane * 8;
+        body(td, tl.tensor, tl.start + o, min(8, (int)tl.len - o));
+      }
+      tile_done(a.tile_begin + u);
+      if (un >= n) break;
+      u = un;
+      tl = tln;
+      un = dyn_take(ctr, lane);
+      if (un < n) tln = a.tiles[a.tile_begin + un];
+    }
+  }
+  dyn_done(ctr, lane);
+}
+
 template <int GT>
 __global__ void __launch_bounds__(kLambThreads, kLambMinBlocks)
 lamb_stats_kernel(const StepArgs a, TileSums* __restrict__ sums) {
@@ -48,74 +86,51 @@ lamb_stats_kernel(const StepArgs a, TileSums* __restrict__ sums) {
     if (a.d_norm->status != OPT_OK) return;
     coef = a.d_norm->clip_coef;
   }
-  // the warps' partial sums, double-buffered by tile parity: thread 0 reads
-  // tile k's after the tile's barrier, and the warps write tile k + 2's only
-  // after tile k + 1's barrier, which thread 0 reaches after its reads.  One
-  // barrier per tile instead of two (the second guarded a single buffer)
-  // took the three passes from 0.961 to 0.994-0.996 of the measured copy
-  // bandwidth on the Llama-3-8B list and from 0.973 to 1.026-1.029 on the
-  // 740-tensor list (GB300, A/B/A), with bit-identical results.  No barrier
-  // at all (per-warp slots, the slices summed by the ratio pass) was faster
-  // on the 740-tensor list but made this pass 7 % slower on the Llama-3-8B
-  // list: there the warps of a CTA gain from reading a tile together.
-  __shared__ float s_u[2][kLambThreads / 32], s_p[2][kLambThreads / 32];
-  const int off = threadIdx.x * 8;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int par = 0;
-  for (int64_t i = a.tile_begin + blockIdx.x; i < a.tile_end; i += gridDim.x, par ^= 1) {
-    const opt_chunk tl = a.tiles[i];
-    float su = 0.0f, sp = 0.0f;
-    if (off < (int)tl.len) {
-      const TensorDesc td = a.tensors[tl.tensor];
-      const int64_t e0 = tl.start + off;
-      const int cnt = min(8, (int)tl.len - off);
-      Frag<GT, SC_F32, ALGO_ADAMW> f;
-      if (cnt == 8) load_full(td, e0, false, f);
-      else load_partial(td, e0, cnt, false, f);
-      float mn[8], vn[8];
+  const int lane = threadIdx.x & 31;
+  float su = 0.0f, sp = 0.0f;          // this lane's sums over its groups of the tile
+  auto body = [&](const TensorDesc& td, uint32_t, int64_t e0, int cnt) {
+    if (cnt <= 0) return;
+    Frag<GT, SC_F32, ALGO_ADAMW> f;
+    if (cnt == 8) load_full(td, e0, false, f);
+    else load_partial(td, e0, cnt, false, f);
+    float mn[8], vn[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float g = GT == OPT_BF16 ? bf16_dec(code_at<16>(f.g, j)) : u2f(f.g[j]);
-        const float ge = __fmul_rn(g, coef);
-        mn[j] = __fadd_rn(__fmul_rn(a.sc.beta1, u2f(f.m[j])), __fmul_rn(a.sc.omb1, ge));
-        vn[j] = __fadd_rn(__fmul_rn(a.sc.beta2, u2f(f.v[j])), __fmul_rn(a.sc.omb2, __fmul_rn(ge, ge)));
-        if (j < cnt) {
-          const float u = lamb_dir(mn[j], vn[j], a.sc);
-          su = __fadd_rn(su, __fmul_rn(u, u));
-          sp = __fadd_rn(sp, __fmul_rn(u2f(f.p[j]), u2f(f.p[j])));
-        }
-      }
-      if (cnt == 8) {
-        st_cs_u4(static_cast<float*>(td.m) + e0, make_uint4(f2u(mn[0]), f2u(mn[1]), f2u(mn[2]), f2u(mn[3])));
-        st_cs_u4(static_cast<float*>(td.m) + e0 + 4,
-                 make_uint4(f2u(mn[4]), f2u(mn[5]), f2u(mn[6]), f2u(mn[7])));
-        st_cs_u4(static_cast<float*>(td.v) + e0, make_uint4(f2u(vn[0]), f2u(vn[1]), f2u(vn[2]), f2u(vn[3])));
-        st_cs_u4(static_cast<float*>(td.v) + e0 + 4,
-                 make_uint4(f2u(vn[4]), f2u(vn[5]), f2u(vn[6]), f2u(vn[7])));
-      } else {
-        for (int j = 0; j < cnt; ++j) {
-          static_cast<float*>(td.m)[e0 + j] = mn[j];
-          static_cast<float*>(td.v)[e0 + j] = vn[j];
-        }
+    for (int j = 0; j < 8; ++j) {
+      const float g = GT == OPT_BF16 ? bf16_dec(code_at<16>(f.g, j)) : u2f(f.g[j]);
+      const float ge = __fmul_rn(g, coef);
+      mn[j] = __fadd_rn(__fmul_rn(a.sc.beta1, u2f(f.m[j])), __fmul_rn(a.sc.omb1, ge));
+      vn[j] = __fadd_rn(__fmul_rn(a.sc.beta2, u2f(f.v[j])), __fmul_rn(a.sc.omb2, __fmul_rn(ge, ge)));
+      if (j < cnt) {
+        const float u = lamb_dir(mn[j], vn[j], a.sc);
+        su = __fadd_rn(su, __fmul_rn(u, u));
+        sp = __fadd_rn(sp, __fmul_rn(u2f(f.p[j]), u2f(f.p[j])));
       }
     }
-    // fixed-order reduction over the tile: warps, then the warp totals
+    if (cnt == 8) {
+      st_cs_u4(static_cast<float*>(td.m) + e0, make_uint4(f2u(mn[0]), f2u(mn[1]), f2u(mn[2]), f2u(mn[3])));
+      st_cs_u4(static_cast<float*>(td.m) + e0 + 4, make_uint4(f2u(mn[4]), f2u(mn[5]), f2u(mn[6]), f2u(mn[7])));
+      st_cs_u4(static_cast<float*>(td.v) + e0, make_uint4(f2u(vn[0]), f2u(vn[1]), f2u(vn[2]), f2u(vn[3])));
+      st_cs_u4(static_cast<float*>(td.v) + e0 + 4, make_uint4(f2u(vn[4]), f2u(vn[5]), f2u(vn[6]), f2u(vn[7])));
+    } else {
+      for (int j = 0; j < cnt; ++j) {
+        static_cast<float*>(td.m)[e0 + j] = mn[j];
+        static_cast<float*>(td.v)[e0 + j] = vn[j];
+      }
+    }
+  };
+  // the tile's sums: the lanes' fp32 sums in double, a fixed butterfly
+  auto tile_done = [&](int64_t i) {
+    double tu = (double)su, tp = (double)sp;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      su = __fadd_rn(su, __shfl_xor_sync(0xFFFFFFFFu, su, o));
-      sp = __fadd_rn(sp, __shfl_xor_sync(0xFFFFFFFFu, sp, o));
+      tu += __shfl_xor_sync(0xFFFFFFFFu, tu, o);
+      tp += __shfl_xor_sync(0xFFFFFFFFu, tp, o);
     }
-    if (lane == 0) { s_u[par][warp] = su; s_p[par][warp] = sp; }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      double tu = 0.0, tp = 0.0;
-      for (int w = 0; w < kLambThreads / 32; ++w) { tu += (double)s_u[par][w]; tp += (double)s_p[par][w]; }
-      TileSums r;
-      r.su = tu;
-      r.sp = tp;
-      sums[i] = r;
-    }
-  }
+    if (lane == 0) sums[i] = TileSums{tu, tp};
+    su = 0.0f;
+    sp = 0.0f;
+  };
+  warp_tiles(a, lane, body, tile_done);
 }
 
 // One CTA per segment (a tensor's tiles are contiguous in the table, its
@@ -187,14 +202,10 @@ template <int GT>
 __global__ void __launch_bounds__(kLambThreads, kLambMinBlocks)
 lamb_apply_kernel(const StepArgs a, const float* __restrict__ ratio) {
   if (a.d_norm != nullptr && a.d_norm->status != OPT_OK) return;
-  const int off = threadIdx.x * 8;
-  int64_t i = a.tile_begin + blockIdx.x;
-  opt_chunk tl;
-  while (next_tile(i, a, off, tl)) {
-    const TensorDesc td = a.tensors[tl.tensor];
-    const float r = ratio[tl.tensor];
-    const int64_t e0 = tl.start + off;
-    const int cnt = min(8, (int)tl.len - off);
+  const int lane = threadIdx.x & 31;
+  auto body = [&](const TensorDesc& td, uint32_t tensor, int64_t e0, int cnt) {
+    if (cnt <= 0) return;
+    const float r = ratio[tensor];
     float p[8], m[8], v[8];
     if (cnt == 8) {
       uint32_t w[8];
@@ -224,8 +235,8 @@ lamb_apply_kernel(const StepArgs a, const float* __restrict__ ratio) {
     } else {
       for (int j = 0; j < cnt; ++j) td.p[e0 + j] = pn[j];
     }
-    i += gridDim.x;
-  }
+  };
+  warp_tiles(a, lane, body, [](int64_t) {});
 }
 
 // Persistent grid: CTAs resident at once (occupancy cached per kernel
@@ -241,6 +252,7 @@ int grid_for_kernel(K k, OccupancyCache& occ, int sm_count, int64_t work) {
 cudaError_t launch_lamb(int grad_dtype, const StepArgs& a, const LambWork& w, float max_unorm, int sm_count,
                         cudaStream_t s, int phase) {
   const int64_t tiles = a.tile_end - a.tile_begin;
+  if (a.dyn == nullptr) return cudaErrorInvalidValue;     // the streaming passes need the counter
   TileSums* ts = static_cast<TileSums*>(w.tile_sums);
   float* ratio = w.ratio;
   // one occupancy slot per kernel instance

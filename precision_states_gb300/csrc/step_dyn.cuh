@@ -36,6 +36,20 @@ __device__ __forceinline__ int64_t dyn_take(unsigned long long* ctr, int lane) {
   return (int64_t)__shfl_sync(0xFFFFFFFFu, v, 0);
 }
 
+// A warp that has taken its last index (>= the tile count) counts itself;
+// once every warp of the launch has, no one reads the counter again, and the
+// last one returns both counts to 0.
+__device__ __forceinline__ void dyn_done(unsigned long long* ctr, int lane) {
+  if (lane != 0) return;
+  const unsigned long long warps = (unsigned long long)gridDim.x * (blockDim.x / 32);
+  __threadfence();                     // this warp's last take comes before its count
+  if (atomicAdd(ctr + 1, 1ull) == warps - 1) {
+    __threadfence();                   // and every warp's, before the reset
+    ctr[0] = 0ull;
+    ctr[1] = 0ull;
+  }
+}
+
 template <int GT, int COMBO, int ALGO, bool SR, bool DEVSC>
 __global__ void __launch_bounds__(kStepThreads, (StepShape<GT, COMBO, ALGO, SR>::kMinBlocks))
 step_dyn_kernel(const StepArgs a) {
@@ -114,18 +128,7 @@ step_dyn_kernel(const StepArgs a) {
     same = __reduce_add_sync(0xFFFFFFFFu, same);
     if (lane == 0 && same) atomicAdd(a.unchanged, (unsigned long long)same);
   }
-  // The warp took its last index (>= n) above, so once every warp of the
-  // launch has counted itself here no one reads the counter again: the last
-  // one returns both counts to 0.
-  if (lane == 0) {
-    const unsigned long long warps = (unsigned long long)gridDim.x * (kStepThreads / 32);
-    __threadfence();                   // this warp's last take comes before its count
-    if (atomicAdd(ctr + 1, 1ull) == warps - 1) {
-      __threadfence();                 // and every warp's, before the reset
-      ctr[0] = 0ull;
-      ctr[1] = 0ull;
-    }
-  }
+  dyn_done(ctr, lane);
 }
 
 // As many CTAs as are resident (occupancy cached), but no more than the
@@ -134,6 +137,7 @@ template <int GT, int COMBO, int ALGO, bool SR, bool DEVSC>
 cudaError_t launch_dyn(const StepArgs& a, int sm_count, cudaStream_t s) {
   const int64_t n = a.tile_end - a.tile_begin;
   if (n <= 0) return cudaSuccess;
+  if (a.dyn == nullptr) return cudaErrorInvalidValue;     // the kernel needs the counter
   auto k = step_dyn_kernel<GT, COMBO, ALGO, SR, DEVSC>;
   static OccupancyCache occ;
   const int per_sm = cached_occupancy(k, occ, kStepThreads, 0);
