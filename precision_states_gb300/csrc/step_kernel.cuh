@@ -53,9 +53,13 @@ constexpr int kStepThreads = 256;
 //   3 CTAs (<= 80 registers) without spilling, and the extra warps lift them
 //   from 0.93 / 0.90 to 1.00 of the measured copy bandwidth.  Every other
 //   instantiation spills at 3 CTAs and runs slower there.
-// - Grid: persistent (as many CTAs as are resident) except for AdEMAMix,
-//   whose five fp32 streams ran faster with one CTA per tile (0.993 against
-//   0.944 of measured).
+// - Grid: persistent (as many CTAs as are resident), CTA c taking tiles
+//   c, c + G, ... -- except for AdEMAMix, whose five fp32 streams ran faster
+//   with one CTA per tile here (0.993 against 0.944 of measured).  The
+//   FP32-state steps (AdamW and AdEMAMix) now run step_dyn_kernel
+//   (step_dyn.cuh) instead, whose warps take tiles from a counter; this
+//   kernel keeps the nearest E4M3 / E2M2 states (3 CTAs per SM) and the
+//   stochastic and BF16-v states where they are not staged.
 // - Staging: the low-precision AdamW instantiations with stochastic rounding,
 //   and BF16 v with nearest rounding, take their input tiles through shared
 //   memory from a producer warp's bulk copies (step_bulk.cuh): 0.956 / 0.917
