@@ -41,14 +41,41 @@ STEP_KERNEL_SOURCES = ["step_kernel.cuh", "step_dyn.cuh", "common.cuh", "interna
                        "step_lowp.cu", "../../include/opt.h"]
 
 
+def code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments, trailing spaces and blank
+    lines (string and character literals kept whole), so that a stamp over
+    it changes with the code and not with its comments."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = [ln.rstrip() for ln in "".join(out).splitlines()]
+    return "\n".join(ln for ln in lines if ln)
+
+
 def source_stamp(files) -> str:
-    """SHA-256 over the named sources (paths relative to csrc/) and the flags."""
+    """SHA-256 over the code of the named sources (paths relative to csrc/;
+    comments and blank lines left out) and the flags."""
     h = hashlib.sha256()
     for f in files:
         path = os.path.normpath(os.path.join(CSRC, f))
         h.update(f.encode())
-        with open(path, "rb") as fh:
-            h.update(fh.read())
+        with open(path, encoding="utf-8") as fh:
+            h.update(code_only(fh.read()).encode())
     # flags without machine-specific paths, so the stamp is the same wherever the tree sits
     h.update(" ".join(f for f in NVCC_FLAGS if not os.path.isabs(f)).encode())
     return h.hexdigest()
