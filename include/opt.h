@@ -38,7 +38,10 @@
  *    a negative status and launch nothing.  There is no CPU fallback.
  *  - Not thread-safe per plan: calls on one plan must not overlap in time on
  *    different host threads.  Concurrent device work on one plan (two streams)
- *    races on the plan's workspace.
+ *    races on the plan's workspace: the norm's slots and completion counter,
+ *    and the tile counter from which the FP32-state and LAMB steps' warps
+ *    take their tiles (two overlapping steps would split one step's tiles
+ *    between them).  Order one plan's calls on one stream, or with events.
  */
 #ifndef PS_OPT_H
 #define PS_OPT_H
