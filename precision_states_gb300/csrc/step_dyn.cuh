@@ -19,7 +19,8 @@
 //
 // Measured on GB300 against the fixed shares (A/B/A/B): Llama-3-8B AdamW
 // step 30.41 -> 29.76 ms (1.024 -> 1.047 of the measured copy bandwidth),
-// 740-tensor list 1.005 -> 1.024, AdEMAMix on the GPT-2 list 1.001 -> 1.012,
+// 740-tensor list 1.005 -> 1.024, AdEMAMix on the GPT-2 list 1.001 -> 1.012
+// (1.025-1.027 once it took its next tile at the switch, without spills),
 // FP32-state AdamW on the GPT-2 list 1.018 -> 1.013.  The nearest E4M3 /
 // E2M2 states keep step_kernel: at their 3 CTAs per SM this loop spills
 // (60-76 bytes) and ran at 0.88 / 0.96 against 1.00 / 1.01.
@@ -68,13 +69,17 @@ step_dyn_kernel(const StepArgs a) {
   const int64_t n = a.tile_end - a.tile_begin;
   unsigned long long* ctr = a.dyn;
   uint32_t same = 0;
+  // AHEAD: the next tile is taken, and its entry requested, a tile early.
+  // AdEMAMix, whose five streams fill the registers, takes it when it
+  // switches tiles instead, which keeps it from spilling.
+  constexpr bool AHEAD = ALGO != ALGO_ADEMAMIX;
 
   int64_t u = dyn_take(ctr, lane);
   if (u < n) {
     opt_chunk tl = a.tiles[a.tile_begin + u];
-    int64_t un = dyn_take(ctr, lane);              // the tile after, a tile ahead
+    int64_t un = AHEAD ? dyn_take(ctr, lane) : 0;
     opt_chunk tln{};
-    if (un < n) tln = a.tiles[a.tile_begin + un];
+    if (AHEAD && un < n) tln = a.tiles[a.tile_begin + un];
     TensorDesc ctd = a.tensors[tl.tensor];
     uint32_t ctensor = tl.tensor;
     int pass = 0;
@@ -96,12 +101,14 @@ step_dyn_kernel(const StepArgs a) {
         const int o = pass * 256 + lane * 8;
         ne0 = tl.start + o;
         ncnt = min(8, (int)tl.len - o);
-      } else if (un < n) {
-        tl = tln;
+      } else if (AHEAD ? un < n : (un = dyn_take(ctr, lane)) < n) {
+        tl = AHEAD ? tln : a.tiles[a.tile_begin + un];
         ntensor = tl.tensor;
         ntd = a.tensors[ntensor];   // (reusing ctd for the same tensor cost 2-6 % on FP32 paths)
-        un = dyn_take(ctr, lane);
-        if (un < n) tln = a.tiles[a.tile_begin + un];
+        if constexpr (AHEAD) {
+          un = dyn_take(ctr, lane);
+          if (un < n) tln = a.tiles[a.tile_begin + un];
+        }
         pass = 0;
         ne0 = tl.start + lane * 8;
         ncnt = min(8, (int)tl.len - lane * 8);
