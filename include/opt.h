@@ -355,15 +355,16 @@ int opt_grad_norm_noalloc(int32_t n, const int64_t* numel, const void* const* gr
 /* ---- host-only helpers (no GPU needed) ----------------------------------- */
 
 /* The norm's chunks.  A gradient-dtype bucket of E elements is cut into
- * chunks of OPT_NORM_CHUNK_MIN elements when E < 2^29, 2 OPT_NORM_CHUNK_MIN
- * when E < 2^31, OPT_CHUNK_ELEMS otherwise -- doubled while any of the
+ * chunks of OPT_NORM_CHUNK_MIN elements when E < 2^28, 2 OPT_NORM_CHUNK_MIN
+ * when E < 2^29, 4 OPT_NORM_CHUNK_MIN when E < 2^31, OPT_CHUNK_ELEMS
+ * otherwise -- doubled while any of the
  * bucket's OPT_NORM_SLOTS slots would own more than OPT_NORM_MAX_PART chunks
  * (slot s owns chunks s, s + OPT_NORM_SLOTS, ...).  A small list then gives
  * every slot's warps many chunks to share, a large one fewer per-chunk costs.
  * The size depends on the sizes alone, so the result stays bit-identical run
  * to run; a bucket whose tensors alone exceed the bound (more than
  * OPT_NORM_SLOTS * OPT_NORM_MAX_PART of them) returns OPT_ELIMIT. */
-#define OPT_NORM_CHUNK_MIN 8192
+#define OPT_NORM_CHUNK_MIN 4096
 #define OPT_CHUNK_ELEMS 32768
 /* Fixed partial-sum slots per gradient-dtype bucket: one CTA of 24 warps each
  * (one per SM of a GB300). */

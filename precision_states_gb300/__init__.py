@@ -26,7 +26,7 @@ OPT_STEP_RESET_STATES = 1
 OPT_STEP_DEVICE_COUNTER = 2
 OPT_STEP_WAIT_DRILL = 4
 OPT_FLAG_WAIT_TIMEOUT, OPT_FLAG_DRAIN_TIMEOUT = 1, 2
-OPT_NORM_CHUNK_MIN, OPT_CHUNK_ELEMS = 8192, 32768
+OPT_NORM_CHUNK_MIN, OPT_CHUNK_ELEMS = 4096, 32768
 OPT_NORM_SLOTS, OPT_NORM_MAX_PART = 152, 4096
 
 DTYPES = {"f32": OPT_F32, "bf16": OPT_BF16, "e4m3": OPT_E4M3, "e2m2": OPT_E2M2}

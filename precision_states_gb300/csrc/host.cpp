@@ -63,9 +63,12 @@ int64_t build_table(int32_t n, const int64_t* numel, const int32_t* grad_dtype, 
 
 // The norm's chunk size for one dtype bucket (the rule stated at
 // OPT_NORM_CHUNK_MIN in opt.h).  Measured on GB300 with the norm's
-// one-CTA-per-SM kernel: 8K-element chunks were fastest on the 740-tensor
-// list (197M elements; 16K and 4K 3 % slower), 32K on the Llama-3-8B list
-// (8.03e9; 16K 1 % slower).
+// one-CTA-per-SM kernel: on the 740-tensor list (197M elements), each norm
+// right after an AdamW step whose dirty L2 lines it evicts, 4K-element
+// chunks took 0.080 ms against 0.084 with 8K and 0.088 with 16K, and the
+// whole step ran 0.45 % faster (with L2 clean first 8K was faster, 0.0705
+// against 0.073 ms); 32K chunks were fastest on the Llama-3-8B list (8.03e9;
+// 16K 1 % slower).
 int64_t norm_chunk_elems(int32_t n, const int64_t* numel, const int32_t* grad_dtype, int bucket) {
   if (n < 0 || (n > 0 && (numel == nullptr || grad_dtype == nullptr)) || bucket < 0 || bucket > 1)
     return OPT_EINVAL;
@@ -76,8 +79,9 @@ int64_t norm_chunk_elems(int32_t n, const int64_t* numel, const int32_t* grad_dt
     if (grad_dtype[i] != OPT_F32 && grad_dtype[i] != OPT_BF16) return OPT_EUNSUPPORTED;
     if (grad_dtype[i] == want) elems += numel[i];
   }
-  int64_t ce = elems < (int64_t(1) << 29) ? OPT_NORM_CHUNK_MIN
-             : elems < (int64_t(1) << 31) ? 2 * OPT_NORM_CHUNK_MIN : OPT_CHUNK_ELEMS;
+  int64_t ce = elems < (int64_t(1) << 28) ? OPT_NORM_CHUNK_MIN
+             : elems < (int64_t(1) << 29) ? 2 * OPT_NORM_CHUNK_MIN
+             : elems < (int64_t(1) << 31) ? 4 * OPT_NORM_CHUNK_MIN : OPT_CHUNK_ELEMS;
   for (; ce <= (int64_t(1) << 31); ce *= 2) {
     int64_t chunks = 0;
     for (int32_t i = 0; i < n; ++i)

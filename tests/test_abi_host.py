@@ -83,18 +83,23 @@ def test_chunk_table_covers_each_tensor_once(seed):
 
 
 def test_norm_chunk_size_rule():
-    """The norm's chunk size comes from a bucket's size alone: 8K elements
-    below 2^29, 16K below 2^31, 32K above, doubled while a slot would own
-    more than OPT_NORM_MAX_PART chunks; the other bucket does not matter."""
+    """The norm's chunk size comes from a bucket's size alone: 4K elements
+    below 2^28, 8K below 2^29, 16K below 2^31, 32K above, doubled while a
+    slot would own more than OPT_NORM_MAX_PART chunks; the other bucket does
+    not matter."""
     f = ps.opt_norm_chunk_elems
     B, F = ps.OPT_BF16, ps.OPT_F32
     assert f([], [], 0) == f([], [], 1) == ps.OPT_NORM_CHUNK_MIN
+    assert ps.OPT_NORM_CHUNK_MIN == 4096
+    assert f([(1 << 28) - 1], [B], 1) == 4096
+    assert f([1 << 28], [B], 1) == 8192
+    assert f([197_281_486], [B], 1) == 4096                # the 740-tensor list's size
     assert f([(1 << 29) - 1], [B], 1) == 8192
     assert f([1 << 29], [B], 1) == 16384
     assert f([(1 << 31) - 1], [B], 1) == 16384
     assert f([1 << 31], [B], 1) == 32768
     assert f([8_030_261_248], [B], 1) == 32768             # the Llama-3-8B list's size
-    assert f([1 << 31, 5], [F, B], 1) == 8192              # buckets apart
+    assert f([1 << 31, 5], [F, B], 1) == 4096              # buckets apart
     assert f([1 << 31, 5], [F, B], 0) == 32768
     # 32K chunks would give a slot more than OPT_NORM_MAX_PART: doubled
     lim = ps.OPT_NORM_SLOTS * ps.OPT_NORM_MAX_PART * 32768

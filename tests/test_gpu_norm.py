@@ -190,7 +190,7 @@ def _noalloc_norm(grads, max_norm, d_out):
     return ps.opt_norm_result.from_buffer_copy(bytes(d_out.cpu().numpy()))
 
 
-@pytest.mark.parametrize("name", ["clip_740", "llama3_8b", "mixed", "mid"])
+@pytest.mark.parametrize("name", ["clip_740", "llama3_8b", "mixed", "tier8k", "mid"])
 def test_norm_counts_every_element_once(name):
     """Every gradient element enters the norm exactly once, over whole lists:
     with BF16 gradients all 1 and FP32 gradients all 2, the sum of squares is
@@ -201,6 +201,10 @@ def test_norm_counts_every_element_once(name):
     if name == "mixed":
         sizes = [32768 * 3 + 5, 1, 70001, 32768, 32767, 4097, 0, 9]
         dts = [torch.bfloat16 if i % 2 == 0 else torch.float32 for i in range(len(sizes))]
+    elif name == "tier8k":   # a BF16 bucket of 2^28 elements and more: 8K-element chunks
+        sizes = [(1 << 28) - 4093, 8195, 9, 4096]
+        dts = [torch.bfloat16] * len(sizes)
+        assert ps.opt_norm_chunk_elems(sizes, [ps.OPT_BF16] * 4, 1) == 8192
     elif name == "mid":      # a BF16 bucket of 2^29 elements and more: 16K-element chunks
         sizes = [(1 << 29) - 4099, 12345, 7, 4097]
         dts = [torch.bfloat16] * len(sizes)
