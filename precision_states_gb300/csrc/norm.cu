@@ -24,7 +24,7 @@
 //
 // Pass 1 runs OPT_NORM_SLOTS CTAs per dtype bucket, one per SM of a GB300,
 // each of 24 warps.  Slot s owns chunks s, s + OPT_NORM_SLOTS, ... of the
-// bucket (chunks of 8K-32K elements, the size from the bucket's size, each
+// bucket (chunks of 4K-32K elements, the size from the bucket's size, each
 // chunk's first element resolved to an address in the table); the slot's
 // warps take its chunks one at a time from a counter in shared memory, and
 // each chunk's sum, reduced by the warp that read it in a fixed shuffle
