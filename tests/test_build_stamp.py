@@ -19,3 +19,19 @@ def test_comment_edits_keep_the_stamp_and_code_edits_change_it(tmp_path, monkeyp
     assert b.source_stamp(["k.cuh"]) == s0
     f.write_text("// header\nint f(int x) { return x + 2; }\n")
     assert b.source_stamp(["k.cuh"]) != s0
+
+
+def test_committed_traffic_records_match_the_current_sources():
+    """profiles/traffic.json holds DRAM counters for the step kernel as it
+    was when they were taken; the bench reports them only while the stamp
+    matches.  A source change without a new capture must show here, not as
+    a silently null figure in the bench line."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "profiles", "traffic.json")
+    with open(path) as fh:
+        records = json.load(fh)
+    assert records
+    want = b.source_stamp(b.STEP_KERNEL_SOURCES)
+    for name, rec in records.items():
+        assert rec["source_stamp"] == want, name
