@@ -57,9 +57,9 @@ constexpr int kStepThreads = 256;
 //   c, c + G, ... -- except for AdEMAMix, whose five fp32 streams ran faster
 //   with one CTA per tile here (0.993 against 0.944 of measured).  The
 //   FP32-state steps (AdamW and AdEMAMix) now run step_dyn_kernel
-//   (step_dyn.cuh) instead, whose warps take tiles from a counter; this
-//   kernel keeps the nearest E4M3 / E2M2 states (3 CTAs per SM) and the
-//   stochastic and BF16-v states where they are not staged.
+//   (step_dyn.cuh) instead, whose warps take tiles from a counter, and the
+//   stochastic and BF16-v states are staged (below); this kernel runs the
+//   nearest E4M3 / E2M2 states (3 CTAs per SM with BF16 gradients).
 // - Staging: the low-precision AdamW instantiations with stochastic rounding,
 //   and BF16 v with nearest rounding, take their input tiles through shared
 //   memory from a producer warp's bulk copies (step_bulk.cuh): 0.956 / 0.917
