@@ -223,7 +223,8 @@ class ClockSampler:
 def step_kernel_name(w, rounding: str) -> str:
     """The step's kernel as the library dispatches it (the roofline's label
     and the key of its traffic record): LAMB's three passes; the short-list
-    kernel for at most 8 tensors and 4,096 tiles of 2,048 elements; the
+    kernel for at most 8 tensors and 4,096 tiles of 2,048 elements (its
+    four-elements-per-thread form with FP32 states); the
     warp-dynamic kernel for FP32 states (AdamW, AdEMAMix); the staged kernel for
     low-precision states with stochastic rounding and for BF16 v; else the
     register-pipelined kernel."""
@@ -233,7 +234,7 @@ def step_kernel_name(w, rounding: str) -> str:
     if w.algo == "lamb":
         return f"lamb_stats_kernel + lamb_ratio_kernel + lamb_apply_kernel<{args}>"
     if len(nonempty) <= 8 and tiles <= 4096:
-        return f"step_small_kernel<{args}>"
+        return f"step_small4_kernel<{args}>" if w.m_dtype == "f32" else f"step_small_kernel<{args}>"
     if w.m_dtype == "f32":
         return f"step_dyn_kernel<{args}>"
     if w.m_dtype != "f32" and w.algo == "adamw" and (rounding == "stochastic" or w.v_dtype == "bf16"):

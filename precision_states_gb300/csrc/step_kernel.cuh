@@ -218,7 +218,7 @@ __device__ __forceinline__ void load_partial(const TensorDesc& td, int64_t e0, i
   }
 }
 
-template <int GT, int COMBO, int ALGO, bool SR>
+template <int GT, int COMBO, int ALGO, bool SR, int N = 8>
 __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e0, int cnt,
                                                  const Frag<GT, COMBO, ALGO>& f, float coef,
                                                  const opt_step_scalars& sc, uint32_t tensor,
@@ -228,6 +228,9 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
   constexpr int MD = F::MD, VD = F::VD;
   constexpr bool LOWP = COMBO != SC_F32;
   constexpr int VBITS = VD == OPT_F32 ? 32 : VD == OPT_BF16 ? 16 : VD == OPT_E4M3 ? 8 : 4;
+  // N: the elements of the group the lanes hold, 8, or 4 with FP32 states
+  // (the short-list kernel's quarter groups: only elements 0..3 are touched)
+  static_assert(N == 8 || (N == 4 && COMBO == SC_F32), "four-element groups: FP32 states only");
 
   uint32_t words[8];
   if constexpr (LOWP && SR) {
@@ -240,7 +243,7 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
   // decode to fp32 (exact)
   float g[8], m[8], v[8];
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < N; ++j) {
     g[j] = GT == OPT_BF16 ? bf16_dec(code_at<16>(f.g, j)) : u2f(f.g[j]);
     m[j] = MD == OPT_F32 ? u2f(f.m[j]) : bf16_dec(code_at<16>(f.m, j));
     if constexpr (VD == OPT_F32) v[j] = u2f(f.v[j]);
@@ -308,7 +311,7 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
     // definition (no contraction), so the values before rounding match bit
     // for bit
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < N; ++j) {
       const float ge = __fmul_rn(g[j], coef);
       mnv[j] = __fadd_rn(__fmul_rn(sc.beta1, m[j]), __fmul_rn(sc.omb1, ge));
       vnv[j] = __fadd_rn(__fmul_rn(sc.beta2, v[j]), __fmul_rn(sc.omb2, __fmul_rn(ge, ge)));
@@ -317,7 +320,7 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
     }
     // the update term (not a stored code)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < N; ++j) {
       float num = __fmul_rn(mnv[j], sc.inv_bc1);
       if constexpr (ALGO == ALGO_ADEMAMIX) num = __fadd_rn(num, __fmul_rn(sc.alpha, m2n[j]));
       const float den = __fadd_rn(sqrt_approx(__fmul_rn(vnv[j], sc.inv_bc2)), sc.eps);
@@ -328,7 +331,7 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
     // it, the converters' E3M2 grid, in the same one multiplication)
     const float vinv = VD == OPT_E2M2 ? __fmul_rn(td.v_inv_scale, 0.25f) : td.v_inv_scale;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) vs[j] = VD == OPT_F32 ? vnv[j] : __fmul_rn(vnv[j], vinv);
+    for (int j = 0; j < N; ++j) vs[j] = VD == OPT_F32 ? vnv[j] : __fmul_rn(vnv[j], vinv);
   }
   // encode, two elements per converter instruction: pair k holds elements
   // 2k (low half / low byte) and 2k+1 -- for stochastic E4M3 / E2M2 v in
@@ -340,7 +343,7 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
   constexpr int HI = WIDE ? 16 : 8;            // bit position of element 2k+1 in an 8-bit-code pair
   uint32_t mpair[4], vpair[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < N / 2; ++k) {
     const uint32_t rm = SR ? __byte_perm(words[2 * k], words[2 * k + 1], 0x5410) : 0u;
     const uint32_t rv = SR ? __byte_perm(words[2 * k], words[2 * k + 1], 0x7632) : 0u;
     const float v0 = vs[2 * k], v1 = vs[2 * k + 1];
@@ -358,11 +361,11 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
   uint32_t same = 0;
   if (count) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < N; ++j)
       same += (j < cnt && vcode_at(j) == (VBITS == 32 ? f.v[j] : code_at<VBITS>(f.v, j))) ? 1u : 0u;
   }
 
-  if (cnt == 8) {
+  if (N == 8 && cnt == 8) {
     st_cs_u4(td.p + e0, make_uint4(f2u(pn[0]), f2u(pn[1]), f2u(pn[2]), f2u(pn[3])));
     st_cs_u4(td.p + e0 + 4, make_uint4(f2u(pn[4]), f2u(pn[5]), f2u(pn[6]), f2u(pn[7])));
     if constexpr (MD == OPT_F32) {
@@ -404,9 +407,17 @@ __device__ __forceinline__ uint32_t update_store(const TensorDesc& td, int64_t e
       st_cs_u4(td.m2 + e0, make_uint4(f2u(m2n[0]), f2u(m2n[1]), f2u(m2n[2]), f2u(m2n[3])));
       st_cs_u4(td.m2 + e0 + 4, make_uint4(f2u(m2n[4]), f2u(m2n[5]), f2u(m2n[6]), f2u(m2n[7])));
     }
+  } else if (COMBO == SC_F32 && cnt == 4) {
+    // four FP32-state elements (the short-list kernel's quarter groups, or a
+    // tensor's last group of exactly four): e0 is a multiple of 4, so 16 bytes
+    st_cs_u4(td.p + e0, make_uint4(f2u(pn[0]), f2u(pn[1]), f2u(pn[2]), f2u(pn[3])));
+    st_cs_u4(static_cast<float*>(td.m) + e0, make_uint4(f2u(mnv[0]), f2u(mnv[1]), f2u(mnv[2]), f2u(mnv[3])));
+    st_cs_u4(static_cast<float*>(td.v) + e0, make_uint4(f2u(vnv[0]), f2u(vnv[1]), f2u(vnv[2]), f2u(vnv[3])));
+    if constexpr (ALGO == ALGO_ADEMAMIX)
+      st_cs_u4(td.m2 + e0, make_uint4(f2u(m2n[0]), f2u(m2n[1]), f2u(m2n[2]), f2u(m2n[3])));
   } else {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < N; ++j) {
       if (j >= cnt) break;
       const int64_t e = e0 + j;
       td.p[e] = pn[j];

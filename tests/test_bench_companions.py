@@ -36,3 +36,20 @@ def test_companions_cover_every_workload_and_state_mode():
 def test_companions_only_in_the_default_single_gpu_run(monkeypatch, argv, world, want):
     monkeypatch.setattr(sys, "argv", ["bench.py", *argv])
     assert bench.companions_wanted(bench.parse(), world) is want
+
+
+def test_step_kernel_labels_follow_the_dispatch():
+    """The roofline's kernel label names what the library launches for each
+    list: the short-list shapes, the warp-dynamic FP32 step, the staged and
+    register-pipelined low-precision steps, LAMB's passes."""
+    import bench
+    import workloads as W
+    one = W.workload("adamw_1m")
+    assert bench.step_kernel_name(one, "nearest").startswith("step_small4_kernel<")
+    lowp_short = W.workload("sweep", sizes=[4097, 5], m_dtype="bf16", v_dtype="e4m3")
+    assert bench.step_kernel_name(lowp_short, "nearest").startswith("step_small_kernel<")
+    assert bench.step_kernel_name(W.workload("clip_740"), "nearest").startswith("step_dyn_kernel<")
+    assert bench.step_kernel_name(W.workload("ademamix_gpt2"), "nearest").startswith("step_dyn_kernel<")
+    lowp = W.workload("lowp_gpt2", v_dtype="e2m2")
+    assert bench.step_kernel_name(lowp, "stochastic").startswith("step_bulk_kernel<")
+    assert bench.step_kernel_name(lowp, "nearest").startswith("step_kernel<")

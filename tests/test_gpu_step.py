@@ -55,7 +55,7 @@ def test_lowp_states_codes(v_dtype, rounding, gdt):
     run_parity(w, 12, 1e-6, rounding=rounding, count=True, check_every=4)
 
 
-SHORT = [1, 3, 2049, 4097, 70001, 300001]     # six tensors: the short-list launch shape
+SHORT = [1, 3, 2049, 4097, 70001, 300001, 2052]   # seven tensors: the short-list launch shape (2052: a last group of four)
 
 
 @pytest.mark.parametrize("v_dtype,rounding", [("f32", "nearest"), ("bf16", "nearest"), ("bf16", "stochastic"),
@@ -64,7 +64,8 @@ SHORT = [1, 3, 2049, 4097, 70001, 300001]     # six tensors: the short-list laun
 @pytest.mark.parametrize("gdt", ["bf16", "f32"])
 def test_short_list_path(v_dtype, rounding, gdt):
     """A bucket of at most eight tensors and 4096 tiles takes the short-list
-    launch shape (descriptors in the kernel parameters, one CTA per tile):
+    launch shape (descriptors in the kernel parameters, one CTA per tile, two
+    with FP32 states):
     parity with the oracle, clipped, with unchanged counts."""
     m_dtype = "f32" if v_dtype == "f32" else "bf16"
     w = W.workload("sweep", sizes=SHORT, grad_dtype=gdt, m_dtype=m_dtype, v_dtype=v_dtype,
@@ -81,8 +82,8 @@ def test_short_list_path_ademamix():
 @pytest.mark.parametrize("v_dtype,rounding", [("f32", "nearest"), ("bf16", "stochastic"), ("e4m3", "nearest"),
                                               ("e2m2", "stochastic")])
 def test_short_and_persistent_shapes_agree_bitwise(v_dtype, rounding):
-    """The same six tensors stepped alone (short-list shape) and with three
-    one-element tensors appended (nine tensors: the persistent kernel) end
+    """The same seven tensors stepped alone (short-list shape) and with three
+    one-element tensors appended (ten tensors: the persistent kernel) end
     with the same bits in p, m and v (no clipping: the extra tensors would
     change the norm)."""
     m_dtype = "f32" if v_dtype == "f32" else "bf16"
@@ -96,7 +97,7 @@ def test_short_and_persistent_shapes_agree_bitwise(v_dtype, rounding):
             W.fill_grads(w, gpu.grads, t, 11)
             gpu.step(t, ghp, clip=False)
         torch.cuda.synchronize()
-        out.append([x.clone() for x in gpu.params[:6] + gpu.m[:6] + gpu.v[:6]])
+        out.append([x.clone() for x in gpu.params[:7] + gpu.m[:7] + gpu.v[:7]])
     for a, b in zip(*out):
         assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
 
