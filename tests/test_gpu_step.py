@@ -234,15 +234,48 @@ def test_scaled_v_codes(v_dtype, rounding):
     assert all(got == want for got, want in counts)
 
 
+@pytest.mark.parametrize("shape", ["persistent", "short"])
+def test_ademamix_reset_step_starts_from_zero_states(shape):
+    """The reset flag starts AdEMAMix's three moments from zero: its reset
+    step equals, bit for bit, a step at t = 1 after zeroing m, v and m2 by
+    hand (the warp-dynamic kernel on the sweep list, the short-list kernel on
+    seven tensors)."""
+    extra = dict(sizes=SHORT) if shape == "short" else {}
+    w = W.workload("sweep", algo="ademamix", hp=dict(lr=1e-2, weight_decay=0.1), **extra)
+    w.max_norm = 0.0
+    a, b = GpuSide(w, seed=6), GpuSide(w, seed=6)
+    ghp, _ = hp_for(w)
+    for t in (1, 2, 3):                       # both accumulate the same states
+        for side in (a, b):
+            W.fill_grads(w, side.grads, t, 6)
+            side.step(t, ghp, clip=False)
+    for side in (a, b):
+        W.fill_grads(w, side.grads, 4, 6)
+    for x in b.m + b.v + b.m2:
+        x.zero_()
+    b.step(1, ghp, clip=False)
+    rhp = hp_for(w)[0]
+    rhp.flags = ps.OPT_STEP_RESET_STATES
+    a.step(1, rhp, clip=False)
+    torch.cuda.synchronize()
+    assert any(bool(x.any()) for x in a.m2)
+    for x, y in zip(a.params + a.m + a.v + a.m2, b.params + b.m + b.v + b.m2):
+        assert torch.equal(x, y)
+
+
 @pytest.mark.parametrize("v_dtype,rounding", [("f32", "nearest"), ("bf16", "nearest"), ("e2m2", "nearest"),
                                               ("bf16", "stochastic"), ("e4m3", "stochastic"),
                                               ("e2m2", "stochastic")])
-def test_reset_step_starts_from_zero_states(v_dtype, rounding):
+@pytest.mark.parametrize("shape", ["persistent", "short"])
+def test_reset_step_starts_from_zero_states(v_dtype, rounding, shape):
     """"When Small Updates Disappear" sec. 5: a reset step starts from zero
     moments.  It must equal (bitwise) a step at t = 1 after zeroing the
-    states by hand, and match the oracle run from zeroed states."""
+    states by hand, and match the oracle run from zeroed states.  Both list
+    shapes: the sweep list (persistent kernels) and seven tensors (the
+    short-list kernels, four elements per thread with FP32 states)."""
     md = "f32" if v_dtype == "f32" else "bf16"
-    w = W.workload("sweep", m_dtype=md, v_dtype=v_dtype, hp=dict(lr=1e-2, weight_decay=0.1))
+    extra = dict(sizes=SHORT) if shape == "short" else {}
+    w = W.workload("sweep", m_dtype=md, v_dtype=v_dtype, hp=dict(lr=1e-2, weight_decay=0.1), **extra)
     w.max_norm = 0.0
     a, b = GpuSide(w, seed=4), GpuSide(w, seed=4)
     sr = rounding == "stochastic"
