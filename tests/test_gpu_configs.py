@@ -10,12 +10,14 @@ tensors and of slices of the large ones.
   exact.
 * llama3_8b: the 8.03e9-parameter list, all 5 steps; each step the norm over
   all of it and the clipped step on 16 sampled tensors (always the embedding
-  and a 4096-vector).
+  and a 4096-vector).  LAMB on the same list (the bench's LAMB run), 2 steps,
+  8 sampled whole tensors.
 """
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import precision_states_gb300 as ps
 import workloads as W
 from harness import GpuSide, OracleSide, fp32_tol, hp_for, oracle_norm_parallel, rel_err, run_lockstep
@@ -115,6 +117,41 @@ def test_llama3_8b_five_steps():
     first = gpu.plan.grad_norm(w.max_norm)
     again = gpu.plan.grad_norm(w.max_norm)
     assert again.as_dict() == first.as_dict()
+    del gpu, orc
+    free()
+
+
+def test_llama3_8b_lamb_two_steps():
+    """LAMB with max_unorm 1.0 on the whole Llama-3-8B list, as the bench
+    times it (its three passes over every tile): each step the oracle's own
+    norm over all 8.03e9 gradients gives the clip coefficient (relative error
+    <= 1e-12, identical coefficient), and on 8 sampled whole tensors (always
+    the embedding and a 4096-vector) the oracle's LAMB step, with that
+    coefficient, gives p, m and v within 1e-5 (1+|x|) after 2 steps."""
+    from concurrent.futures import ThreadPoolExecutor
+    w = W.workload("llama3_8b")
+    gpu = GpuSide(w, seed=5)
+    vec = next(i for i, n in enumerate(w.sizes) if n == 4096)
+    samples = sample_tensors(w, 8, seed=9, always=(0, vec))
+    orc = OracleSide(gpu, samples)
+    ghp, ohp = hp_for(w)
+    ratios = []
+    for t in (1, 2):
+        W.fill_grads(w, gpu.grads, t, 5)
+        g_all = [W.to_numpy_codes(g) for g in gpu.grads]
+        want = oracle_norm_parallel(g_all, w.max_norm)
+        del g_all
+        got = gpu.plan.grad_norm(w.max_norm)
+        assert rel_err(got.norm2, want["norm2"]) <= 1e-12, (t, got.norm2, want["norm2"])
+        assert got.clip_coef == want["clip_coef"] and got.clip_coef < 1.0
+        g_np = orc.grads(gpu.grads)
+        with ThreadPoolExecutor(8) as ex:        # one whole tensor each; the C calls release the GIL
+            ratios += list(ex.map(lambda k: oracle.lamb_tensor(orc.p[k], g_np[k], orc.m[k], orc.v[k], ohp, t, 1.0,
+                                                               want["clip_coef"]), range(len(orc.samples))))
+        gpu.plan.lamb_step(ghp, t, 1.0, gpu.plan.norm_buffer())
+    torch.cuda.synchronize()
+    assert any(r < 1.0 for r in ratios)          # the bound binds somewhere
+    orc.compare(gpu, 1e-5, False)
     del gpu, orc
     free()
 
